@@ -1,0 +1,17 @@
+"""fp64 CPU oracle for the MoE-layer forward (test infrastructure only).
+
+This package is the checker, not the product.  Only the tests, the smoke
+check of ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` use it.
+It shares no code with the CUDA path and imports nothing from it.
+"""
+from .moe_oracle import (  # noqa: F401
+    route_topk,
+    softmax_rows,
+    dispatch,
+    permute,
+    silu,
+    expert_mlp,
+    combine,
+    moe_forward,
+    moe_forward_tokens,
+)

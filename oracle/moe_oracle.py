@@ -1,0 +1,203 @@
+"""Plain, slow, fp64 oracle of one Mixture-of-Experts layer forward.
+
+TEST INFRASTRUCTURE.  This module is the checker that the CUDA path is
+compared against.  It is imported only by ``tests/``, by
+``__graft_entry__.smoke()`` and by the CPU-baseline leg of ``bench.py``.  It
+shares no code with the CUDA kernels or their binding and never calls them.
+
+Source of the method: "Scalable Pretraining of Large MoE LMs on Aurora Super
+Computer", §3.1 FastSparseMoE, Algorithm 1 (FastSparseMoEBlock):
+  stage 1  router logits -> Softmax -> TopK           (weights, indices [S,K])
+  stage 2  per-expert token counts and prefix sums    (group boundaries)
+  stage 3  index generation: input_indices (row -> token) and
+           output_indices ((token, slot) -> row)
+  stage 4  mlp_in = input[input_indices]; gate/up grouped GEMMs; Silu(gate)*up;
+           down grouped GEMM
+  stage 5  output reduction: out[t] = sum over the token's slots of
+           weights[t][slot] * mlp_out[row of (t, slot)]
+Renormalisation of the k selected gates is not in Algorithm 1; it is the
+workload's stated routing ("softmax top-k renormalised") and is a flag here.
+
+Each function is the plain definition of its step, written out with numpy
+primitives (sort, cumsum, matmul) and no blocking or fusion.  All floating
+point is fp64; inputs that are bf16 or fp32 on the GPU are passed in as
+float arrays holding exactly those values.
+
+Readings of points the pages leave open (each is pinned by a test):
+  * experts are ranked by the fp32 router logit (softmax is monotone, so the
+    set and order equal those of ranking by probability), ties broken by the
+    smaller expert index; -0.0 equals +0.0;
+  * slot j of a token holds its (j+1)-th best expert;
+  * within an expert's group, rows are in ascending token order (the order
+    Algorithm 1's thread-block layout of partial counts produces);
+  * the expert MLP and the reduction are exact fp64 on the bf16 inputs, with
+    no intermediate rounding.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------- stage 1
+def softmax_rows(logits: np.ndarray) -> np.ndarray:
+    """Row softmax in fp64: p[t,e] = exp(l[t,e] - m_t) / sum_e' exp(l[t,e'] - m_t).
+
+    Algorithm 1, stage 1 (probs = Softmax(logits)).
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    m = l.max(axis=1, keepdims=True)
+    z = np.exp(l - m)
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def route_topk(logits: np.ndarray, k: int, renormalize: bool = True):
+    """Top-k routing of each token.
+
+    Algorithm 1, stage 1 (weights, indices = TopK(probs)).  Returns
+    ``idx`` int32 [T,k] and ``w`` float64 [T,k].
+
+    The k experts with the largest logits are chosen under the total order
+    (logit descending, expert index ascending); slot j holds the (j+1)-th.
+    ``w[t,j]`` is the softmax probability of that expert, divided by the sum
+    of the k selected probabilities when ``renormalize``.
+    """
+    l32 = np.asarray(logits, dtype=np.float32)
+    T, E = l32.shape
+    if not (1 <= k <= E):
+        raise ValueError("need 1 <= k <= E")
+    # a stable sort of the negated values orders by value descending with
+    # ties kept in ascending expert order; -0.0 and +0.0 compare equal
+    order = np.argsort(-l32, axis=1, kind="stable")
+    idx = order[:, :k].astype(np.int32)
+    probs = softmax_rows(l32)
+    w = np.take_along_axis(probs, idx.astype(np.int64), axis=1)
+    if renormalize:
+        w = w / w.sum(axis=1, keepdims=True)
+    return idx, w
+
+
+# ---------------------------------------------------------- stages 2 and 3
+def dispatch(idx: np.ndarray, E: int):
+    """Counts, group boundaries and the two index maps.
+
+    Algorithm 1, stages 2-3, written as the stable counting sort they
+    compute.  With pairs p = t*k + j taken in increasing p:
+      counts[e]    number of pairs routed to e (token counts)
+      offsets      exclusive prefix sum of counts, length E+1 (cum_token_counts)
+      dest_row[p]  offsets[e] + number of earlier pairs q < p with idx[q] == e
+                   (output_indices)
+      src_token[r] token of the pair placed at row r (input_indices)
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    flat = idx.reshape(-1).astype(np.int64)
+    if flat.size and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert index out of range")
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    pair_of_row = np.argsort(flat, kind="stable")     # rows grouped by expert, pair order kept
+    dest_row = np.empty(T * k, dtype=np.int64)
+    dest_row[pair_of_row] = np.arange(T * k, dtype=np.int64)
+    src_token = pair_of_row // k
+    return counts, offsets, src_token, dest_row
+
+
+# ---------------------------------------------------------------- stage 4
+def permute(x: np.ndarray, src_token: np.ndarray) -> np.ndarray:
+    """mlp_in = input[input_indices] (Algorithm 1, stage 4): a row gather."""
+    return np.asarray(x)[np.asarray(src_token, dtype=np.int64)]
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
+    z = np.asarray(z, dtype=np.float64)
+    return z / (1.0 + np.exp(-z))
+
+
+def expert_mlp(x_perm, offsets, w_gate, w_up, w_down, experts=None):
+    """Grouped SwiGLU expert MLP on expert-contiguous rows.
+
+    Algorithm 1, stage 4: for expert e and its rows [offsets[e], offsets[e+1]):
+      gate = X_e @ Wg[e]       Wg[e] is [d, f]
+      up   = X_e @ Wu[e]
+      h    = Silu(gate) * up
+      y    = h @ Wd[e]         Wd[e] is [f, d]
+    Returns (h [P,f], y [P,d]) in fp64.  ``experts`` limits the work to a
+    subset (rows of other experts stay zero).
+    """
+    x_perm = np.asarray(x_perm, dtype=np.float64)
+    P = x_perm.shape[0]
+    E = len(offsets) - 1
+    f = w_gate.shape[2]
+    d = w_down.shape[2]
+    h = np.zeros((P, f), dtype=np.float64)
+    y = np.zeros((P, d), dtype=np.float64)
+    for e in (range(E) if experts is None else experts):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a == b:
+            continue
+        X = x_perm[a:b]
+        gate = X @ np.asarray(w_gate[e], dtype=np.float64)
+        up = X @ np.asarray(w_up[e], dtype=np.float64)
+        he = silu(gate) * up
+        h[a:b] = he
+        y[a:b] = he @ np.asarray(w_down[e], dtype=np.float64)
+    return h, y
+
+
+# ---------------------------------------------------------------- stage 5
+def combine(y, dest_row, w):
+    """Output reduction (Algorithm 1, stage 5, forward):
+    out[t] = sum_j w[t,j] * y[dest_row[t*k + j]], slots in order j = 0..k-1.
+    """
+    y = np.asarray(y, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T, k = w.shape
+    rows = np.asarray(dest_row, dtype=np.int64).reshape(T, k)
+    out = np.zeros((T, y.shape[1]), dtype=np.float64)
+    for j in range(k):
+        out += w[:, j:j + 1] * y[rows[:, j]]
+    return out
+
+
+# ------------------------------------------------------------ whole layer
+def moe_forward(x, logits, w_gate, w_up, w_down, k, renormalize=True):
+    """Every stage of the layer forward, in order, with all intermediates."""
+    E = w_gate.shape[0]
+    idx, w = route_topk(logits, k, renormalize)
+    counts, offsets, src_token, dest_row = dispatch(idx, E)
+    x_perm = permute(x, src_token)
+    h, y = expert_mlp(x_perm, offsets, w_gate, w_up, w_down)
+    out = combine(y, dest_row, w)
+    row_w = np.empty(len(dest_row), dtype=np.float64)
+    row_w[dest_row] = w.reshape(-1)
+    return dict(idx=idx, w=w, counts=counts, offsets=offsets, src_token=src_token,
+                dest_row=dest_row, row_w=row_w, x_perm=x_perm, h=h, y=y, out=out)
+
+
+def moe_forward_tokens(x_rows, logits_rows, w_gate, w_up, w_down, k, renormalize=True):
+    """Layer output for a few tokens only.
+
+    Routing, the expert MLP and the reduction of one token depend on that
+    token's own row of x and logits alone, so the layer restricted to a
+    token subset is the layer applied to those rows.  Returns idx, w,
+    per-slot h [n,k,f] and y [n,k,d] (unscaled) and out [n,d].
+    """
+    x_rows = np.asarray(x_rows, dtype=np.float64)
+    idx, w = route_topk(logits_rows, k, renormalize)
+    n = x_rows.shape[0]
+    f = w_gate.shape[2]
+    d = w_down.shape[2]
+    h = np.zeros((n, k, f))
+    y = np.zeros((n, k, d))
+    for e in np.unique(idx):
+        sel = np.nonzero(idx == e)          # (token, slot) pairs routed to e
+        X = x_rows[sel[0]]
+        gate = X @ np.asarray(w_gate[e], dtype=np.float64)
+        up = X @ np.asarray(w_up[e], dtype=np.float64)
+        he = silu(gate) * up
+        h[sel] = he
+        y[sel] = he @ np.asarray(w_down[e], dtype=np.float64)
+    out = np.einsum("nk,nkd->nd", w, y)
+    return dict(idx=idx, w=w, h=h, y=y, out=out)

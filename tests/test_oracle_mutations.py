@@ -1,0 +1,99 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each test swaps one oracle step for a plausibly wrong variant (on the CPU,
+through monkeypatch) and checks that a pin of tests/test_oracle_pins.py
+then fails.  This shows the pins are sensitive to a dropped term, a wrong
+order or sign, and a transposed operand.
+"""
+import numpy as np
+import pytest
+
+import oracle.moe_oracle as om
+from tests import test_oracle_pins as pins
+from tests.conftest import load_golden
+
+
+def _fails(fn, *args, **kw):
+    with pytest.raises((AssertionError, ValueError)):
+        fn(*args, **kw)
+
+
+def test_silu_without_input_factor_is_caught(monkeypatch):
+    monkeypatch.setattr(om, "silu", lambda z: 1.0 / (1.0 + np.exp(-np.asarray(z, dtype=np.float64))))
+    _fails(pins.test_swiglu_scalar_golden, load_golden)
+    _fails(pins.test_layer_matches_per_token_brute_force, 21, 16, 6, 2, 24, True)
+
+
+def test_silu_wrong_sign_is_caught(monkeypatch):
+    monkeypatch.setattr(om, "silu", lambda z: np.asarray(z) / (1.0 + np.exp(np.asarray(z, dtype=np.float64))))
+    _fails(pins.test_swiglu_scalar_golden, load_golden)
+
+
+def test_dropped_up_projection_is_caught(monkeypatch):
+    real = om.expert_mlp
+
+    def no_up(x_perm, offsets, w_gate, w_up, w_down, experts=None):
+        return real(x_perm, offsets, w_gate, np.ones_like(w_up) / w_up.shape[1], w_down, experts)
+    monkeypatch.setattr(om, "expert_mlp", no_up)
+    _fails(pins.test_single_expert_layer_is_dense_swiglu_mlp)
+
+
+def test_transposed_down_projection_is_caught(monkeypatch):
+    real = om.expert_mlp
+
+    def transposed(x_perm, offsets, w_gate, w_up, w_down, experts=None):
+        wd = np.ascontiguousarray(np.transpose(w_down, (0, 2, 1)))
+        if wd.shape[1] != w_gate.shape[2]:
+            raise ValueError("shape mismatch")
+        return real(x_perm, offsets, w_gate, w_up, wd, experts)
+    monkeypatch.setattr(om, "expert_mlp", transposed)
+    _fails(pins.test_layer_matches_per_token_brute_force, 12, 8, 4, 4, 8, True)
+
+
+def test_reversed_tie_break_is_caught(monkeypatch):
+    def bad_route(logits, k, renormalize=True):
+        l32 = np.asarray(logits, dtype=np.float32)
+        E = l32.shape[1]
+        order = (E - 1 - np.argsort(-l32[:, ::-1], axis=1, kind="stable"))  # ties -> larger index
+        idx = order[:, :k].astype(np.int32)
+        w = np.take_along_axis(om.softmax_rows(l32), idx.astype(np.int64), axis=1)
+        return idx, (w / w.sum(axis=1, keepdims=True) if renormalize else w)
+    monkeypatch.setattr(om, "route_topk", bad_route)
+    import oracle
+    monkeypatch.setattr(oracle, "route_topk", bad_route)
+    _fails(pins.test_route_indices_match_brute_force, 40, 8, 8, True)
+    _fails(pins.test_route_golden, load_golden)
+
+
+def test_missing_renormalisation_is_caught(monkeypatch):
+    real = om.route_topk
+    import oracle
+    monkeypatch.setattr(oracle, "route_topk", lambda l, k, renormalize=True: real(l, k, False))
+    _fails(pins.test_route_weights_closed_form, True)
+
+
+def test_unstable_group_order_is_caught(monkeypatch):
+    import oracle
+    real = om.dispatch
+
+    def bad_dispatch(idx, E):
+        counts, offsets, src, dst = real(idx, E)
+        # reverse the rows inside every expert group
+        new_dst = dst.copy()
+        for e in range(E):
+            a, b = offsets[e], offsets[e + 1]
+            sel = (dst >= a) & (dst < b)
+            new_dst[sel] = a + b - 1 - dst[sel]
+        new_src = np.empty_like(src)
+        new_src[new_dst] = np.arange(len(new_dst)) // idx.shape[1]
+        return counts, offsets, new_src, new_dst
+    monkeypatch.setattr(oracle, "dispatch", bad_dispatch)
+    _fails(pins.test_dispatch_matches_alg1_thread_blocks, 64, 16, 4, 8)
+    _fails(pins.test_index_golden_matches_hand_example, load_golden)
+
+
+def test_combine_without_gates_is_caught(monkeypatch):
+    import oracle
+    real = om.combine
+    monkeypatch.setattr(oracle, "combine", lambda y, dest_row, w: real(y, dest_row, np.ones_like(w)))
+    _fails(pins.test_combine_of_identity_experts_returns_input)
