@@ -1,0 +1,394 @@
+#!/usr/bin/env python
+"""Throughput of one MoE-layer forward on GB300.
+
+A step is one pass of the whole path — route + token counts, look-back
+index, permute, gate/up grouped GEMM with SwiGLU, down grouped GEMM with
+gate scale, combine — over one batch of T tokens, with inputs and packed
+weights resident in HBM.  Default workload: one layer of the 951.9B model
+(T=16,384 tokens, d=6,144, E=384 experts, top-8, f=1,792), seeded
+synthetic inputs.  The working set (25 GB of weights, 201 MB of tokens)
+is far larger than L2, so no flush is needed between steps.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
+Under torchrun (N > 1) every rank runs its own replica (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s and grouped-GEMM TFLOP/s (% bf16 peak); permute GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_STEP = 6  # route, index, permute, gate/up GEMM, down GEMM, combine
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+GEMM_SOURCE = os.path.join(ROOT, "sparse_expert_gb300", "csrc", "grouped_gemm.cu")
+
+
+# ----------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the job time)."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------------- peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def file_sha256(path):
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the gate/up GEMM from a committed ncu summary,
+    or None when absent or taken on a different kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if rec.get("workload") != workload or rec.get("source_sha256") != file_sha256(GEMM_SOURCE):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------- algorithmic work
+def stage_work(cfg):
+    """Algorithmic bytes / FLOPs per launch of each stage (real rows only)."""
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
+    P = T * k
+    return {
+        "route": {"bytes": T * E * 4 + P * 8},
+        "index": {"bytes": P * 4 + P * 4 + 3 * P * 4 + E * 8},
+        "permute": {"bytes": T * d * 2 + P * d * 2 + P * 4},
+        "gate_up": {"flops": 4 * P * d * f},
+        "down": {"flops": 2 * P * d * f},
+        "combine": {"bytes": P * d * 2 + T * d * 2 + P * 4},
+    }
+
+
+def weight_bytes_read(cfg, counts):
+    nonempty = int((np.asarray(counts) > 0).sum())
+    return nonempty * 3 * cfg.d * cfg.f * 2
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(cfg, x, logits, w_gate, w_up, w_down, tokens):
+    """Host copies of what the oracle needs for a token sample: the sampled
+    rows and the weights of every expert they route to."""
+    import oracle
+    idx, _ = oracle.route_topk(logits[tokens].cpu().numpy(), cfg.k, cfg.renormalize)
+    experts = sorted(set(idx.reshape(-1).tolist()))
+
+    class Host:
+        def __init__(self, w):
+            self.shape = tuple(w.shape)
+            self.data = {e: w[e].float().cpu().numpy() for e in experts}
+
+        def __getitem__(self, e):
+            return self.data[int(e)]
+    return (x[tokens].float().cpu().numpy(), logits[tokens].cpu().numpy(), Host(w_gate), Host(w_up), Host(w_down),
+            len(experts))
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def time_oracle(cfg, sample):
+    import oracle
+    x_rows, l_rows, wg, wu, wd, _ = sample
+    t0 = time.perf_counter()
+    oracle.moe_forward_tokens(x_rows, l_rows, wg, wu, wd, cfg.k, cfg.renormalize)
+    return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------------ arms
+def gpu_arm(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    import sparse_expert_gb300 as moe
+
+    cfg = workloads.get(args.workload)
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
+    P = T * k
+    inp = workloads.generate(cfg, seed=args.seed + rank, device="cuda")
+    x, logits = inp["x"], inp["logits"]
+    packed = moe.moe_pack_weights(inp["w_gate"], inp["w_up"], inp["w_down"])
+    ws = torch.empty(moe.moe_forward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device="cuda")
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    nstage = len(moe.FORWARD_STAGES)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)] for _ in range(args.steps)]
+    warm_events = [torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)]
+
+    for _ in range(args.warmup):
+        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, warm_events, cfg.renormalize, stream)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0, "device status after warm-up"
+    inter = moe.forward_intermediates(ws, T, E, k, d, f)
+    counts = inter["counts"].cpu().numpy()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, events[s], cfg.renormalize, stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    status = moe.moe_read_device_status(ws)
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed steps")
+    max_s = max_over_ranks(elapsed_ms / 1e3, world, device="cuda")
+    value = job_throughput(T * args.steps, world, max_s)
+
+    stage_ms = {name: statistics.mean(events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps))
+                for i, name in enumerate(moe.FORWARD_STAGES)}
+    work = stage_work(cfg)
+    peaks = load_peaks()
+    stages = {}
+    for name, ms in stage_ms.items():
+        st = {"ms": round(ms, 4)}
+        if "flops" in work[name]:
+            st["tflops"] = round(work[name]["flops"] / (ms * 1e-3) / 1e12, 2)
+            st["frac_bf16_peak"] = round(st["tflops"] / peaks["bf16_tflops"], 4)
+        else:
+            st["gbs"] = round(work[name]["bytes"] / (ms * 1e-3) / 1e9, 1)
+            st["frac_hbm"] = round(st["gbs"] / peaks["hbm_gbs"], 4)
+        stages[name] = st
+    gemm_ms = stage_ms["gate_up"] + stage_ms["down"]
+    gemm_tflops = (work["gate_up"]["flops"] + work["down"]["flops"]) / (gemm_ms * 1e-3) / 1e12
+    dominant = max(("gate_up", "down"), key=lambda n: stage_ms[n])
+    achieved = work[dominant]["flops"] / (stage_ms[dominant] * 1e-3) / 1e12
+    traffic = recorded_traffic(args.workload) if dominant == "gate_up" else None
+    roofline = {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({dominant})", "achieved": round(achieved, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic, "peak_source": f"bf16 dense burst, {peaks['source']}"}
+
+    # end to end: host buffers through the C ABI, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        x_h = x.cpu().pin_memory()
+        l_h = logits.cpu().pin_memory()
+        o_h = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+        x_d, l_d, o_d = torch.empty_like(x), torch.empty_like(logits), torch.empty_like(out)
+        for _ in range(max(1, args.warmup)):
+            moe.moe_forward_host(x_h, l_h, o_h, x_d, l_d, o_d, packed, E, k, f, ws, cfg.renormalize, stream)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            moe.moe_forward_host(x_h, l_h, o_h, x_d, l_d, o_d, packed, E, k, f, ws, cfg.renormalize, stream)
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, device="cuda")
+        e2e = {"value": round(job_throughput(T * args.steps, world, e2e_s), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": x_h.numel() * 2 + l_h.numel() * 4, "d2h_bytes_per_step": o_h.numel() * 2}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = min(args.cpu_sample_tokens, T)
+        tokens = torch.arange(n, device="cuda")
+        sample = oracle_sample(cfg, x, logits, inp["w_gate"], inp["w_up"], inp["w_down"], tokens)
+        secs = time_oracle(cfg, sample)
+        cpu = {"value": round(n / secs, 3), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"fp64 numpy oracle, full layer forward of the first {n} tokens of the {args.workload} "
+                         f"workload ({sample[5]} experts touched), {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: MoE layer forward, T={T} tokens, d={d}, E={E} experts, "
+                                   f"top-{k}, f={f}, bf16, fp32 router logits ({cfg.routing} routing), seed "
+                                   f"{args.seed}",
+                       "T": T, "d": d, "E": E, "k": k, "f": f, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (weights 3*E*d*f*2 bytes streamed every step)"},
+            "grouped_gemm": {"tflops": round(gemm_tflops, 2), "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
+                             "weight_bytes_read": weight_bytes_read(cfg, counts)},
+            "permute_gbs": stages["permute"]["gbs"],
+            "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def reference_arm(args):
+    """The fp64 oracle on the host cores, on samples of the same workload."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    cfg = workloads.get(args.workload)
+    n = min(args.ref_sample_tokens, cfg.T)
+    dev = f"cuda:{local}" if torch.cuda.is_available() else "cpu"
+    inp = workloads.generate(cfg, seed=args.seed, device=dev)
+    secs = []
+    for s in range(args.warmup + args.steps):
+        # step s: the oracle on n consecutive tokens; only the oracle call is timed
+        tokens = (torch.arange(n) + (s * n) % max(1, cfg.T - n + 1)).to(dev)
+        sample = oracle_sample(cfg, inp["x"], inp["logits"], inp["w_gate"], inp["w_up"], inp["w_down"], tokens)
+        t = time_oracle(cfg, sample)
+        if s >= args.warmup:
+            secs.append(t)
+        del sample
+    total = sum(secs)
+    value = n * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total * 1e3 / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: MoE layer forward, T={cfg.T} tokens, d={cfg.d}, E={cfg.E} "
+                               f"experts, top-{cfg.k}, f={cfg.f}", "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"each step: fp64 numpy oracle, full layer forward of {n} consecutive tokens"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--workload", choices=sorted(workloads.CONFIGS), default="t1")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    ap.add_argument("--ref-sample-tokens", type=int, default=4)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,267 @@
+/*
+ * moe_gb300.h — C ABI of the single-GPU Mixture-of-Experts layer forward
+ * (GB300, sm_103a).
+ *
+ * The layer follows "Scalable Pretraining of Large MoE LMs on Aurora Super
+ * Computer", §3.1 FastSparseMoE, Algorithm 1 (FastSparseMoEBlock), on one
+ * device without expert parallelism:
+ *   stage 1  Softmax and TopK of the router logits        -> moe_route_topk
+ *   stage 2  per-expert token counts and prefix sums      -> moe_dispatch_scan
+ *   stage 3  index generation (row->token, pair->row)     -> moe_dispatch_scan
+ *   stage 4  mlp_in = input[input_indices]                -> moe_permute
+ *            grouped gate/up GEMMs, Silu(gate)*up, grouped
+ *            down GEMM                                    -> moe_grouped_swiglu
+ *   stage 5  output reduction weighted by the TopK weights -> moe_combine
+ * and moe_forward runs all of them.  Sizes follow the problem statement of
+ * that section: T tokens of hidden size d, E routed experts, top-k, expert
+ * hidden size f; P = T*k routed (token, slot) pairs.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE memory owned by the caller unless a parameter says
+ *     "host".  Nothing is allocated by the library; scratch comes from a
+ *     caller-provided workspace sized by the matching *_workspace_bytes query
+ *     and must be 256-byte aligned.
+ *   - Tensors are dense and row-major.  "bf16" buffers hold IEEE bfloat16
+ *     bit patterns (2 bytes each); they are typed void* here.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and returns without waiting for it.  Only
+ *     moe_read_device_status and moe_forward_host synchronise.
+ *   - Argument errors are found on the host and returned at once with no
+ *     work enqueued.  Errors found by a kernel (a bounded wait that ran out,
+ *     an out-of-range expert index) are written to a status word at the
+ *     start of the workspace and read back with moe_read_device_status.
+ *   - Calls that share a workspace must not overlap on the GPU.
+ *   - Supported sizes: 1 <= E <= 1024, 1 <= k <= min(E, 32), 0 <= T,
+ *     T*k < 2^31.  The GEMM stages and moe_forward need d and f to be
+ *     multiples of 64 in [64, 65536] (whole 128-byte K blocks for the
+ *     tensor cores); moe_permute and moe_combine need d % 8 == 0 (16-byte
+ *     rows).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_GB300_ABI_VERSION 1
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 32
+
+typedef void* moe_stream_t; /* cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* NULL pointer, negative or inconsistent size   */
+  MOE_ERR_UNSUPPORTED = 2,   /* size outside the supported range above        */
+  MOE_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed   */
+  MOE_ERR_TIMEOUT = 4,       /* a kernel's bounded wait ran out (device)      */
+  MOE_ERR_BAD_INDEX = 5,     /* an expert index outside [0, E) (device)       */
+  MOE_ERR_WORKSPACE = 6,     /* workspace NULL, misaligned or too small       */
+  MOE_ERR_NO_DEVICE = 7      /* no CUDA device, or not an sm_103 device       */
+} moe_status_t;
+
+/* ABI version of the loaded library (MOE_GB300_ABI_VERSION). */
+MOE_API int moe_abi_version(void);
+
+/* Static text for a status code. */
+MOE_API const char* moe_status_string(moe_status_t status);
+
+/* Text describing the last error returned on the calling host thread
+ * (thread-local; valid until the next call on that thread). */
+MOE_API const char* moe_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Stage 1 — router Softmax and TopK (Algorithm 1, stage 1).
+ *   logits    [T, E] fp32, one row per token.
+ *   topk_idx  [T, k] int32 out: slot j holds the (j+1)-th largest logit;
+ *             ties go to the smaller expert index, -0.0 equals +0.0.
+ *   topk_w    [T, k] fp32 out: softmax probability of that expert; when
+ *             renormalize != 0, divided by the sum over the k selected
+ *             (equal to the softmax over the k selected logits).
+ * Logits must be finite.  T == 0 enqueues nothing.
+ * Errors: MOE_ERR_INVALID_ARG (NULL with T > 0, T < 0),
+ *         MOE_ERR_UNSUPPORTED (E or k out of range), MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_route_topk(const float* logits, int64_t T, int32_t E, int32_t k,
+                            int32_t renormalize, int32_t* topk_idx, float* topk_w,
+                            moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stages 2 and 3 — token counts, group boundaries and index generation
+ * (Algorithm 1, stages 2-3), as one stable counting sort of the P pairs
+ * p = t*k + j by expert:
+ *   counts    [E] int32 out: pairs routed to each expert (token counts).
+ *   offsets   [E+1] int32 out: exclusive prefix sum of counts, offsets[E]=P
+ *             (cumulative token counts: expert e owns rows
+ *             [offsets[e], offsets[e+1])).
+ *   dest_row  [P] int32 out: row of pair p (output indices) =
+ *             offsets[e] + number of pairs q < p routed to the same expert;
+ *             rows of one expert are therefore in ascending token order.
+ *   src_token [P] int32 out: token of the pair placed at each row (input
+ *             indices); src_token[dest_row[p]] == p / k.
+ *   row_w     [P] fp32 out, optional (NULL skips it): row_w[dest_row[p]] =
+ *             topk_w[p]; needs topk_w.
+ *   topk_idx  [T, k] int32 in; topk_w [T, k] fp32 in, optional.
+ * Implementation: a block histogram, then one pass in which each block of
+ * pairs takes its per-expert base from its predecessors by decoupled
+ * look-back.  An expert index outside [0, E) sets MOE_ERR_BAD_INDEX in the
+ * device status word and its pair is dropped.
+ * Workspace: moe_dispatch_workspace_bytes(T, E, k) bytes.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE,
+ *         MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API size_t moe_dispatch_workspace_bytes(int64_t T, int32_t E, int32_t k);
+MOE_API moe_status_t moe_dispatch_scan(const int32_t* topk_idx, const float* topk_w,
+                               int64_t T, int32_t E, int32_t k,
+                               int32_t* counts, int32_t* offsets,
+                               int32_t* src_token, int32_t* dest_row, float* row_w,
+                               void* workspace, size_t workspace_bytes,
+                               moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 4, first step — mlp_in = input[input_indices] (Algorithm 1,
+ * stage 4), done from the token side: each token row of x is read once and
+ * written to its k rows, x_perm[dest_row[t*k + j]] = x[t].  The result is
+ * the same as gathering x_perm[r] = x[src_token[r]].
+ *   x [T, d] bf16 in; dest_row [T*k] int32 in (a bijection onto [0, T*k));
+ *   x_perm [T*k, d] bf16 out.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_permute(const void* x, int64_t T, int32_t d, const int32_t* dest_row,
+                         int32_t k, void* x_perm, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Expert weights in the layout the grouped GEMM reads.  Algorithm 1,
+ * stage 4 concatenates the per-expert weights of one projection into one
+ * tensor; this call does that once, ahead of the forward (it is a layout
+ * transform, not part of the per-step path):
+ *   w_gate, w_up [E, d, f] bf16 in (gate = x @ w_gate[e]);
+ *   w_down       [E, f, d] bf16 in (y = h @ w_down[e]);
+ *   packed       moe_packed_weight_bytes(E, d, f) bytes out (3*E*d*f bf16):
+ *                gate and up transposed to [f, d] per expert and
+ *                interleaved in blocks of the GEMM's N tile, then down
+ *                transposed to [d, f] per expert.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API size_t moe_packed_weight_bytes(int32_t E, int32_t d, int32_t f);
+MOE_API moe_status_t moe_pack_weights(const void* w_gate, const void* w_up, const void* w_down,
+                              int32_t E, int32_t d, int32_t f, void* packed,
+                              moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 4, expert computation — the grouped gate/up GEMM with
+ * Silu(gate)*up and the grouped down GEMM (Algorithm 1, stage 4), over the
+ * expert groups given by offsets, on the tensor cores (bf16 operands, fp32
+ * accumulation):
+ *   h[r, :] = bf16( silu(x_perm[r] @ Wg[e]) * (x_perm[r] @ Wu[e]) )
+ *   y[r, :] = bf16( row_scale[r] * (h[r] @ Wd[e]) )   (scale 1 if NULL)
+ * for every row r in [offsets[e], offsets[e+1]).
+ *   x_perm [P, d] bf16 in; offsets [E+1] int32 in (offsets[E] == P, as
+ *   moe_dispatch_scan writes it); packed from moe_pack_weights;
+ *   row_scale [P] fp32 in, optional (the gate of each row, row_w);
+ *   h [P, f] bf16 out; y [P, d] bf16 out.
+ * Experts with no rows cost nothing.  Tiles are handed to persistent
+ * blocks from an atomic counter.
+ * Workspace: moe_grouped_swiglu_workspace_bytes() bytes.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE,
+ *         MOE_ERR_NO_DEVICE, MOE_ERR_CUDA; MOE_ERR_TIMEOUT in the status word.
+ * ---------------------------------------------------------------------- */
+MOE_API size_t moe_grouped_swiglu_workspace_bytes(void);
+MOE_API moe_status_t moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, int64_t P,
+                                int32_t E, int32_t d, int32_t f, const void* packed,
+                                const float* row_scale, void* h, void* y,
+                                void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 5 — output reduction, forward (Algorithm 1, stage 5):
+ *   out[t, :] = bf16( sum_{j<k} w[t, j] * y[dest_row[t*k + j], :] )
+ * summed in fp32 in slot order; w = topk_w, or 1 when topk_w is NULL (the
+ * rows already carry their gate, as moe_grouped_swiglu writes them with
+ * row_scale).
+ *   y [T*k, d] bf16 in; dest_row [T*k] int32 in; topk_w [T, k] fp32 in,
+ *   optional; out [T, d] bf16 out.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_combine(const void* y, const int32_t* dest_row, const float* topk_w,
+                         int64_t T, int32_t k, int32_t d, void* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The whole layer forward (Algorithm 1, stages 1-5) on one stream, with no
+ * host synchronisation: route + histogram, look-back index pass, permute,
+ * gate/up GEMM with SwiGLU, down GEMM scaled by each row's gate, combine.
+ *   x [T, d] bf16; logits [T, E] fp32; packed from moe_pack_weights;
+ *   out [T, d] bf16 out; topk_idx_out [T, k] int32 and topk_w_out [T, k]
+ *   fp32 out, optional (the workspace keeps its own copy).
+ * Workspace: moe_forward_workspace_bytes(T, E, k, d, f); the intermediates
+ * stay there after the call at the byte offsets moe_forward_layout gives.
+ * Errors: as the stages.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  size_t topk_idx, topk_w, counts, offsets, src_token, dest_row, row_w;
+  size_t x_perm, h, y;
+  size_t total;
+} moe_forward_layout_t;
+
+MOE_API size_t moe_forward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f);
+MOE_API moe_status_t moe_forward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f,
+                                moe_forward_layout_t* layout);
+MOE_API moe_status_t moe_forward(const void* x, const float* logits, const void* packed,
+                         int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
+                         int32_t renormalize, void* out,
+                         int32_t* topk_idx_out, float* topk_w_out,
+                         void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_forward with stage timing: identical work, plus cudaEventRecord of
+ * events[i] (caller-created cudaEvent_t handles, MOE_FORWARD_STAGES + 1 of
+ * them) on `stream` at the stage boundaries
+ *   0 start | route | 1 | look-back index | 2 | permute | 3 | gate/up GEMM |
+ *   4 | down GEMM | 5 | combine | 6
+ * so that cudaEventElapsedTime(events[i], events[i+1]) is the time of one
+ * stage's kernel (stage 0 also holds the workspace clear).
+ * ---------------------------------------------------------------------- */
+#define MOE_FORWARD_STAGES 6
+MOE_API moe_status_t moe_forward_timed(const void* x, const float* logits, const void* packed,
+                               int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
+                               int32_t renormalize, void* out,
+                               void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                               void* const* events);
+
+/* ------------------------------------------------------------------------
+ * moe_forward from HOST buffers: copies x_host [T, d] bf16 and logits_host
+ * [T, E] fp32 into device staging buffers, runs moe_forward, copies the
+ * result into out_host [T, d] bf16, and waits for the stream.  Host buffers
+ * should be page-locked for the copies to run at full speed.  The staging
+ * buffers (x_dev, logits_dev, out_dev) are caller-owned device memory.
+ * Errors: as moe_forward, plus MOE_ERR_CUDA for a failed copy.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_forward_host(const void* x_host, const float* logits_host, void* out_host,
+                              void* x_dev, float* logits_dev, void* out_dev,
+                              const void* packed, int64_t T, int32_t d, int32_t E, int32_t k,
+                              int32_t f, int32_t renormalize,
+                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Reads the device status word at the start of a workspace used by
+ * moe_dispatch_scan, moe_grouped_swiglu or moe_forward, after waiting for
+ * `stream`.  *status receives MOE_OK or the first device error.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream,
+                                    int32_t* status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

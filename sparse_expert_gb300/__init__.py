@@ -1,0 +1,26 @@
+"""Single-GPU Mixture-of-Experts layer forward for GB300 (sm_103a).
+
+The compute lives in libmoe_gb300.so (hand-written CUDA kernels behind a C
+ABI, declared in include/moe_gb300.h); this package is its Python binding.
+Importing it fails if the library has not been built.
+"""
+from ._lib import (  # noqa: F401
+    MoEError,
+    abi_version,
+    forward_intermediates,
+    moe_combine,
+    moe_dispatch_scan,
+    moe_dispatch_workspace_bytes,
+    moe_forward,
+    moe_forward_host,
+    moe_forward_layout,
+    moe_forward_timed,
+    FORWARD_STAGES,
+    moe_forward_workspace_bytes,
+    moe_grouped_swiglu,
+    moe_pack_weights,
+    moe_packed_weight_bytes,
+    moe_permute,
+    moe_read_device_status,
+    moe_route_topk,
+)

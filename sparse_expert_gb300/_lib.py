@@ -1,0 +1,280 @@
+"""ctypes binding of libmoe_gb300.so: argument marshalling only.
+
+Every function here allocates its outputs with torch on the inputs' device,
+passes raw pointers, sizes and the current CUDA stream to the C entry point
+of the same name, and raises MoEError on a non-OK status.  All arithmetic
+runs in the library's CUDA kernels.  There is no fallback: if the library
+is missing, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
+                4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_BAD_INDEX", 6: "MOE_ERR_WORKSPACE", 7: "MOE_ERR_NO_DEVICE"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {detail}")
+        self.status = status
+
+
+class ForwardLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("topk_idx", "topk_w", "counts", "offsets", "src_token", "dest_row", "row_w",
+                 "x_perm", "h", "y", "total")]
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run sparse_expert_gb300/build.py (nvcc, sm_103a)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_S = ctypes.c_int  # moe_status_t
+
+SIGNATURES = {
+    "moe_abi_version": (ctypes.c_int, []),
+    "moe_status_string": (ctypes.c_char_p, [_S]),
+    "moe_last_error": (ctypes.c_char_p, []),
+    "moe_route_topk": (_S, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
+    "moe_dispatch_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
+    "moe_dispatch_scan": (_S, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute": (_S, [_P, _I64, _I32, _P, _I32, _P, _P]),
+    "moe_packed_weight_bytes": (_SZ, [_I32, _I32, _I32]),
+    "moe_pack_weights": (_S, [_P, _P, _P, _I32, _I32, _I32, _P, _P]),
+    "moe_grouped_swiglu_workspace_bytes": (_SZ, []),
+    "moe_grouped_swiglu": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_combine": (_S, [_P, _P, _P, _I64, _I32, _I32, _P, _P]),
+    "moe_forward_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
+    "moe_forward_layout": (_S, [_I64, _I32, _I32, _I32, _I32, ctypes.POINTER(ForwardLayout)]),
+    "moe_forward": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_timed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
+    "moe_forward_host": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P]),
+    "moe_read_device_status": (_S, [_P, _P, ctypes.POINTER(_I32)]),
+}
+for _name, (_res, _args) in SIGNATURES.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoEError(status, where, lib.moe_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _contig(t, dtype, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def abi_version() -> int:
+    return lib.moe_abi_version()
+
+
+# --------------------------------------------------------------- stage 1
+def moe_route_topk(logits, k, renormalize=True, stream=None):
+    """topk_idx int32 [T,k], topk_w fp32 [T,k] of fp32 router logits [T,E]."""
+    _contig(logits, torch.float32, "logits")
+    T, E = logits.shape
+    idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _check(lib.moe_route_topk(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(idx), _ptr(w), _stream(stream)),
+           "moe_route_topk")
+    return idx, w
+
+
+# ------------------------------------------------------------ stages 2-3
+def moe_dispatch_workspace_bytes(T, E, k) -> int:
+    return lib.moe_dispatch_workspace_bytes(T, E, k)
+
+
+def moe_dispatch_scan(topk_idx, E, topk_w=None, row_w=True, workspace=None, stream=None):
+    """counts [E], offsets [E+1], src_token [P], dest_row [P], row_w [P] (or None)."""
+    _contig(topk_idx, torch.int32, "topk_idx")
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    P = T * k
+    if topk_w is not None:
+        _contig(topk_w, torch.float32, "topk_w")
+    need = lib.moe_dispatch_workspace_bytes(T, E, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    src = torch.empty(P, dtype=torch.int32, device=dev)
+    dst = torch.empty(P, dtype=torch.int32, device=dev)
+    rw = torch.empty(P, dtype=torch.float32, device=dev) if (row_w and topk_w is not None) else None
+    _check(lib.moe_dispatch_scan(_ptr(topk_idx), _ptr(topk_w), T, E, k, _ptr(counts), _ptr(offsets), _ptr(src),
+                                 _ptr(dst), _ptr(rw), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_dispatch_scan")
+    return dict(counts=counts, offsets=offsets, src_token=src, dest_row=dst, row_w=rw, workspace=workspace)
+
+
+# ---------------------------------------------------------- stage 4 / 5
+def moe_permute(x, dest_row, k, stream=None):
+    """x_perm [T*k, d] with x_perm[dest_row[t*k+j]] = x[t]."""
+    _contig(x, torch.bfloat16, "x")
+    _contig(dest_row, torch.int32, "dest_row")
+    T, d = x.shape
+    out = torch.empty(T * k, d, dtype=torch.bfloat16, device=x.device)
+    _check(lib.moe_permute(_ptr(x), T, d, _ptr(dest_row), k, _ptr(out), _stream(stream)), "moe_permute")
+    return out
+
+
+def moe_packed_weight_bytes(E, d, f) -> int:
+    return lib.moe_packed_weight_bytes(E, d, f)
+
+
+def moe_pack_weights(w_gate, w_up, w_down, stream=None):
+    """Packed expert weights (uint8 buffer) for moe_grouped_swiglu / moe_forward."""
+    for t, n in ((w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down")):
+        _contig(t, torch.bfloat16, n)
+    E, d, f = w_gate.shape
+    packed = torch.empty(lib.moe_packed_weight_bytes(E, d, f), dtype=torch.uint8, device=w_gate.device)
+    _check(lib.moe_pack_weights(_ptr(w_gate), _ptr(w_up), _ptr(w_down), E, d, f, _ptr(packed), _stream(stream)),
+           "moe_pack_weights")
+    return packed
+
+
+def moe_grouped_swiglu(x_perm, offsets, E, f, packed, row_scale=None, workspace=None, stream=None):
+    """(h [P,f], y [P,d]) of the grouped SwiGLU expert MLP."""
+    _contig(x_perm, torch.bfloat16, "x_perm")
+    _contig(offsets, torch.int32, "offsets")
+    P, d = x_perm.shape
+    dev = x_perm.device
+    if row_scale is not None:
+        _contig(row_scale, torch.float32, "row_scale")
+    if workspace is None:
+        workspace = torch.empty(lib.moe_grouped_swiglu_workspace_bytes(), dtype=torch.uint8, device=dev)
+    h = torch.empty(P, f, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(P, d, dtype=torch.bfloat16, device=dev)
+    _check(lib.moe_grouped_swiglu(_ptr(x_perm), _ptr(offsets), P, E, d, f, _ptr(packed), _ptr(row_scale), _ptr(h),
+                                  _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_grouped_swiglu")
+    return h, y
+
+
+def moe_combine(y, dest_row, T, k, topk_w=None, stream=None):
+    """out [T, d] = sum_j w[t,j] * y[dest_row[t*k+j]] (w = 1 when topk_w is None)."""
+    _contig(y, torch.bfloat16, "y")
+    _contig(dest_row, torch.int32, "dest_row")
+    if topk_w is not None:
+        _contig(topk_w, torch.float32, "topk_w")
+    d = y.shape[1]
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=y.device)
+    _check(lib.moe_combine(_ptr(y), _ptr(dest_row), _ptr(topk_w), T, k, d, _ptr(out), _stream(stream)),
+           "moe_combine")
+    return out
+
+
+# ------------------------------------------------------------ the layer
+def moe_forward_workspace_bytes(T, E, k, d, f) -> int:
+    return lib.moe_forward_workspace_bytes(T, E, k, d, f)
+
+
+def moe_forward_layout(T, E, k, d, f) -> ForwardLayout:
+    lay = ForwardLayout()
+    _check(lib.moe_forward_layout(T, E, k, d, f, ctypes.byref(lay)), "moe_forward_layout")
+    return lay
+
+
+def moe_forward(x, logits, packed, E, k, f, renormalize=True, workspace=None, out=None, topk_idx=None,
+                topk_w=None, stream=None):
+    """out [T, d] of the whole layer.  The workspace keeps every intermediate."""
+    _contig(x, torch.bfloat16, "x")
+    _contig(logits, torch.float32, "logits")
+    T, d = x.shape
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(lib.moe_forward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    _check(lib.moe_forward(_ptr(x), _ptr(logits), _ptr(packed), T, d, E, k, f, int(bool(renormalize)), _ptr(out),
+                           _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_forward")
+    return out
+
+
+FORWARD_STAGES = ("route", "index", "permute", "gate_up", "down", "combine")
+
+
+def moe_forward_timed(x, logits, packed, E, k, f, workspace, out, events, renormalize=True, stream=None):
+    """moe_forward that records events[0..6] (torch.cuda.Event, timing enabled)
+    at the stage boundaries on the launching stream."""
+    T, d = x.shape
+    s = stream if stream is not None else torch.cuda.current_stream()
+    for ev in events:
+        if ev.cuda_event == 0:
+            ev.record(s)  # materialise the handle
+    handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    _check(lib.moe_forward_timed(_ptr(x), _ptr(logits), _ptr(packed), T, d, E, k, f, int(bool(renormalize)),
+                                 _ptr(out), _ptr(workspace), workspace.numel(), _stream(s), handles),
+           "moe_forward_timed")
+    return out
+
+
+def moe_forward_host(x_host, logits_host, out_host, x_dev, logits_dev, out_dev, packed, E, k, f, workspace,
+                     renormalize=True, stream=None):
+    """moe_forward from host tensors (pinned for full-speed copies); waits for the stream."""
+    T, d = x_host.shape
+    _check(lib.moe_forward_host(_ptr(x_host), _ptr(logits_host), _ptr(out_host), _ptr(x_dev), _ptr(logits_dev),
+                                _ptr(out_dev), _ptr(packed), T, d, E, k, f, int(bool(renormalize)),
+                                _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_forward_host")
+    return out_host
+
+
+def forward_intermediates(workspace, T, E, k, d, f):
+    """Views of the intermediates that moe_forward leaves in its workspace."""
+    lay = moe_forward_layout(T, E, k, d, f)
+    P = T * k
+
+    def view(off, n, dtype):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return workspace[off:off + nbytes].view(dtype)
+    return dict(
+        counts=view(lay.counts, E, torch.int32),
+        offsets=view(lay.offsets, E + 1, torch.int32),
+        topk_idx=view(lay.topk_idx, P, torch.int32).view(T, k),
+        topk_w=view(lay.topk_w, P, torch.float32).view(T, k),
+        src_token=view(lay.src_token, P, torch.int32),
+        dest_row=view(lay.dest_row, P, torch.int32),
+        row_w=view(lay.row_w, P, torch.float32),
+        x_perm=view(lay.x_perm, P * d, torch.bfloat16).view(P, d),
+        h=view(lay.h, P * f, torch.bfloat16).view(P, f),
+        y=view(lay.y, P * d, torch.bfloat16).view(P, d),
+    )
+
+
+def moe_read_device_status(workspace, stream=None) -> int:
+    st = _I32(0)
+    _check(lib.moe_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(st)), "moe_read_device_status")
+    return st.value

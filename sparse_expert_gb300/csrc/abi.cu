@@ -1,0 +1,452 @@
+// C ABI of the MoE-layer forward: argument checks, workspace layout and the
+// order of launches.  Every entry point validates on the host before it
+// touches CUDA, so argument errors never reach the GPU.
+#include <cstdio>
+#include <algorithm>
+#include <cstring>
+#include <string>
+
+#include "../../include/moe_gb300.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t fail(moe_status_t s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+moe_status_t cuda_fail(cudaError_t e, const char* where) {
+  g_last_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_CUDA(call, where)                   \
+  do {                                          \
+    cudaError_t err_ = (call);                  \
+    if (err_ != cudaSuccess) return cuda_fail(err_, where); \
+  } while (0)
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status_t check_routing(int64_t T, int32_t E, int32_t k) {
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
+  if (k < 1 || k > E || k > MOE_MAX_TOPK) return fail(MOE_ERR_UNSUPPORTED, "k must be in [1, min(E, 32)]");
+  if (T * static_cast<int64_t>(k) >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  return MOE_OK;
+}
+
+moe_status_t check_row(int32_t d, const char* name) {
+  if (d < 8 || d > 65536 || d % 8 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, std::string(name) + " must be a multiple of 8 in [8, 65536]");
+  return MOE_OK;
+}
+
+moe_status_t check_gemm_dims(int32_t d, int32_t f) {
+  if (d < 64 || d > 65536 || d % 64 != 0) return fail(MOE_ERR_UNSUPPORTED, "d must be a multiple of 64 in [64, 65536]");
+  if (f < 64 || f > 65536 || f % 64 != 0) return fail(MOE_ERR_UNSUPPORTED, "f must be a multiple of 64 in [64, 65536]");
+  return MOE_OK;
+}
+
+// Upper bound on the flat tile index of the grouped GEMMs must fit int32.
+moe_status_t check_tile_space(int64_t P, int32_t E, int32_t d, int32_t f) {
+  const int64_t mt = P / 128 + E;
+  const int64_t nt = std::max<int64_t>(2 * static_cast<int64_t>(f) / 128, static_cast<int64_t>(d) / 64);
+  if (mt * nt >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "problem too large for the tile index");
+  return MOE_OK;
+}
+
+moe_status_t device_info(DeviceInfo* info) {
+  cudaError_t e = current_device_info(info);
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver)
+    return fail(MOE_ERR_NO_DEVICE, "no CUDA device available");
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  if (info->cc_major != 10 || info->cc_minor != 3)
+    return fail(MOE_ERR_NO_DEVICE, "the library is built for sm_103a (GB300); device has compute capability " +
+                                       std::to_string(info->cc_major) + "." + std::to_string(info->cc_minor));
+  return MOE_OK;
+}
+
+// ---- moe_forward workspace layout
+struct ForwardLayout {
+  size_t header, flags_end, counts, dispatch_state, offsets;
+  size_t topk_idx, topk_w, src_token, dest_row, row_w, x_perm, h, y, total;
+  size_t clear_bytes;
+};
+
+ForwardLayout forward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f) {
+  const int64_t P = T * k;
+  ForwardLayout L{};
+  size_t o = 0;
+  L.header = o;
+  o = dispatch_clear_bytes(P);  // header + look-back flags
+  L.flags_end = o;
+  L.counts = o;
+  o += align_up(static_cast<size_t>(E) * 4);
+  L.clear_bytes = o;            // header, flags and counts start at zero
+  L.dispatch_state = o;
+  // flags live in the cleared region; the state's agg/incl arrays follow
+  o += dispatch_state_bytes(P, E);
+  L.offsets = o;
+  o += align_up(static_cast<size_t>(E + 1) * 4);
+  L.topk_idx = o;
+  o += align_up(static_cast<size_t>(P) * 4);
+  L.topk_w = o;
+  o += align_up(static_cast<size_t>(P) * 4);
+  L.src_token = o;
+  o += align_up(static_cast<size_t>(P) * 4);
+  L.dest_row = o;
+  o += align_up(static_cast<size_t>(P) * 4);
+  L.row_w = o;
+  o += align_up(static_cast<size_t>(P) * 4);
+  L.x_perm = o;
+  o += align_up(static_cast<size_t>(P) * d * 2);
+  L.h = o;
+  o += align_up(static_cast<size_t>(P) * f * 2);
+  L.y = o;
+  o += align_up(static_cast<size_t>(P) * d * 2);
+  L.total = o;
+  return L;
+}
+
+// Dispatch state inside a workspace: flags right after the header (cleared
+// with it), agg/incl at `state_at` (not cleared).
+DispatchState dispatch_state_split(void* ws, size_t state_at, int64_t P, int E) {
+  DispatchState st = dispatch_state_at(static_cast<char*>(ws) + state_at, P, E);
+  st.flags = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(WsHeader));
+  return st;
+}
+
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* info) {
+  static DeviceInfo cache[64];
+  static bool have[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && have[dev]) {
+    *info = cache[dev];
+    return cudaSuccess;
+  }
+  DeviceInfo d{};
+  d.device = dev;
+  e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *info = d;
+  return cudaSuccess;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_GB300_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    case MOE_ERR_BAD_INDEX: return "expert index out of range";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_NO_DEVICE: return "no supported CUDA device";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_status_t moe_route_topk(const float* logits, int64_t T, int32_t E, int32_t k, int32_t renormalize,
+                            int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if (T > 0 && (!logits || !topk_idx || !topk_w)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T == 0) return MOE_OK;
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  MOE_CUDA(launch_route_topk(logits, T, E, k, renormalize, topk_idx, topk_w, nullptr, dev.num_sms,
+                             static_cast<cudaStream_t>(stream)),
+           "route_topk launch");
+  return MOE_OK;
+}
+
+size_t moe_dispatch_workspace_bytes(int64_t T, int32_t E, int32_t k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  const int64_t P = T * k;
+  return dispatch_clear_bytes(P) + dispatch_state_bytes(P, E);
+}
+
+moe_status_t moe_dispatch_scan(const int32_t* topk_idx, const float* topk_w, int64_t T, int32_t E, int32_t k,
+                               int32_t* counts, int32_t* offsets, int32_t* src_token, int32_t* dest_row,
+                               float* row_w, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if (!counts || !offsets) return fail(MOE_ERR_INVALID_ARG, "NULL counts/offsets");
+  if (T > 0 && (!topk_idx || !src_token || !dest_row)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (row_w && !topk_w) return fail(MOE_ERR_INVALID_ARG, "row_w needs topk_w");
+  const size_t need = moe_dispatch_workspace_bytes(T, E, k);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, kAlign))
+    return fail(MOE_ERR_WORKSPACE, "dispatch workspace needs " + std::to_string(need) + " bytes, 256-byte aligned");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t P = T * k;
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, dispatch_clear_bytes(P), st), "workspace clear");
+  MOE_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, st), "counts clear");
+  if (P == 0) {
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st), "offsets clear");
+    return MOE_OK;
+  }
+  auto* hdr = static_cast<WsHeader*>(workspace);
+  MOE_CUDA(launch_histogram(topk_idx, P, E, counts, &hdr->status, dev.num_sms, st), "histogram launch");
+  DispatchState dst = dispatch_state_split(workspace, dispatch_clear_bytes(P), P, E);
+  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, workspace, dst, st),
+           "index launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_permute(const void* x, int64_t T, int32_t d, const int32_t* dest_row, int32_t k, void* x_perm,
+                         moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > MOE_MAX_TOPK) return fail(MOE_ERR_INVALID_ARG, "bad T or k");
+  if (T * static_cast<int64_t>(k) >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  moe_status_t s = check_row(d, "d");
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!x || !dest_row || !x_perm) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(x, 16) || !aligned(x_perm, 16)) return fail(MOE_ERR_INVALID_ARG, "x and x_perm must be 16-byte aligned");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, dev.num_sms, static_cast<cudaStream_t>(stream)),
+           "permute launch");
+  return MOE_OK;
+}
+
+size_t moe_packed_weight_bytes(int32_t E, int32_t d, int32_t f) {
+  if (E < 1 || d < 1 || f < 1) return 0;
+  return static_cast<size_t>(3) * E * static_cast<size_t>(d) * f * 2;
+}
+
+moe_status_t moe_pack_weights(const void* w_gate, const void* w_up, const void* w_down, int32_t E, int32_t d,
+                              int32_t f, void* packed, moe_stream_t stream) {
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
+  moe_status_t s = check_gemm_dims(d, f);
+  if (s != MOE_OK) return s;
+  if (!w_gate || !w_up || !w_down || !packed) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  MOE_CUDA(launch_pack_weights(w_gate, w_up, w_down, E, d, f, packed, static_cast<cudaStream_t>(stream)),
+           "pack launch");
+  return MOE_OK;
+}
+
+size_t moe_grouped_swiglu_workspace_bytes(void) { return sizeof(WsHeader); }
+
+moe_status_t moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, int64_t P, int32_t E, int32_t d,
+                                int32_t f, const void* packed, const float* row_scale, void* h, void* y,
+                                void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (P < 0 || P >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "P must be in [0, 2^31)");
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
+  moe_status_t s = check_gemm_dims(d, f);
+  if (s != MOE_OK) return s;
+  if ((s = check_tile_space(P, E, d, f)) != MOE_OK) return s;
+  if (!offsets || !packed) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (P > 0 && (!x_perm || !h || !y)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!workspace || workspace_bytes < sizeof(WsHeader) || !aligned(workspace, kAlign))
+    return fail(MOE_ERR_WORKSPACE, "grouped GEMM workspace needs 256 bytes, 256-byte aligned");
+  if (!aligned(x_perm, 16) || !aligned(h, 16) || !aligned(y, 16) || !aligned(packed, 16))
+    return fail(MOE_ERR_INVALID_ARG, "x_perm, h, y and packed must be 16-byte aligned");
+  if (P == 0) return MOE_OK;
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* hdr = static_cast<WsHeader*>(workspace);
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st), "workspace clear");
+  const auto* wgu = static_cast<const __nv_bfloat16*>(packed);
+  const auto* wdn = wgu + static_cast<int64_t>(E) * 2 * f * d;
+  GroupedGemmProblem g1{x_perm, wgu, offsets, nullptr, h, P, E, d, 2 * f, f, &hdr->tile_counter[0], &hdr->status};
+  MOE_CUDA(launch_grouped_gemm(g1, Epilogue::kSwiGLU, dev.num_sms, st), "gate/up GEMM launch");
+  GroupedGemmProblem g2{h, wdn, offsets, row_scale, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
+  MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_combine(const void* y, const int32_t* dest_row, const float* topk_w, int64_t T, int32_t k,
+                         int32_t d, void* out, moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > MOE_MAX_TOPK) return fail(MOE_ERR_INVALID_ARG, "bad T or k");
+  if (T * static_cast<int64_t>(k) >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  moe_status_t s = check_row(d, "d");
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!y || !dest_row || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(y, 16) || !aligned(out, 16)) return fail(MOE_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  MOE_CUDA(launch_combine(y, dest_row, topk_w, T, k, d, out, dev.num_sms, static_cast<cudaStream_t>(stream)),
+           "combine launch");
+  return MOE_OK;
+}
+
+size_t moe_forward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f) {
+  if (T < 0 || E < 1 || k < 1 || d < 1 || f < 1) return 0;
+  return forward_layout(T, E, k, d, f).total;
+}
+
+moe_status_t moe_forward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f,
+                                moe_forward_layout_t* layout) {
+  if (!layout) return fail(MOE_ERR_INVALID_ARG, "NULL layout");
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if ((s = check_gemm_dims(d, f)) != MOE_OK) return s;
+  const ForwardLayout L = forward_layout(T, E, k, d, f);
+  layout->topk_idx = L.topk_idx;
+  layout->topk_w = L.topk_w;
+  layout->counts = L.counts;
+  layout->offsets = L.offsets;
+  layout->src_token = L.src_token;
+  layout->dest_row = L.dest_row;
+  layout->row_w = L.row_w;
+  layout->x_perm = L.x_perm;
+  layout->h = L.h;
+  layout->y = L.y;
+  layout->total = L.total;
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_status_t forward_impl(const void* x, const float* logits, const void* packed, int64_t T, int32_t d, int32_t E,
+                          int32_t k, int32_t f, int32_t renormalize, void* out, int32_t* topk_idx_out,
+                          float* topk_w_out, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                          void* const* events) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if ((s = check_gemm_dims(d, f)) != MOE_OK) return s;
+  const int64_t P = T * k;
+  if ((s = check_tile_space(P, E, d, f)) != MOE_OK) return s;
+  if (!packed) return fail(MOE_ERR_INVALID_ARG, "NULL packed weights");
+  if (T > 0 && (!x || !logits || !out)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(packed, 16))
+    return fail(MOE_ERR_INVALID_ARG, "x, out and packed must be 16-byte aligned");
+  const ForwardLayout L = forward_layout(T, E, k, d, f);
+  if (!workspace || workspace_bytes < L.total || !aligned(workspace, kAlign))
+    return fail(MOE_ERR_WORKSPACE, "forward workspace needs " + std::to_string(L.total) + " bytes, 256-byte aligned");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  auto* hdr = reinterpret_cast<WsHeader*>(ws);
+  auto* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  auto* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* topk_idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t*>(ws + L.topk_idx);
+  float* topk_w = topk_w_out ? topk_w_out : reinterpret_cast<float*>(ws + L.topk_w);
+  auto* src_token = reinterpret_cast<int32_t*>(ws + L.src_token);
+  auto* dest_row = reinterpret_cast<int32_t*>(ws + L.dest_row);
+  auto* row_w = reinterpret_cast<float*>(ws + L.row_w);
+  void* x_perm = ws + L.x_perm;
+  void* h = ws + L.h;
+  void* y = ws + L.y;
+
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+  };
+  MOE_CUDA(mark(0), "event record");
+  MOE_CUDA(cudaMemsetAsync(ws, 0, L.clear_bytes, st), "workspace clear");
+  if (T == 0) {
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st), "offsets clear");
+    for (int i = 1; i <= MOE_FORWARD_STAGES; ++i) MOE_CUDA(mark(i), "event record");
+    return MOE_OK;
+  }
+  // stage 1 (+ token counts)
+  MOE_CUDA(launch_route_topk(logits, T, E, k, renormalize, topk_idx, topk_w, counts, dev.num_sms, st), "route launch");
+  MOE_CUDA(mark(1), "event record");
+  // stages 2-3: offsets, index maps and the gate of every row
+  DispatchState dstate = dispatch_state_split(ws, L.dispatch_state, P, E);
+  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, ws, dstate, st),
+           "index launch");
+  MOE_CUDA(mark(2), "event record");
+  // stage 4
+  MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, dev.num_sms, st), "permute launch");
+  MOE_CUDA(mark(3), "event record");
+  const auto* wgu = static_cast<const __nv_bfloat16*>(packed);
+  const auto* wdn = wgu + static_cast<int64_t>(E) * 2 * f * d;
+  GroupedGemmProblem g1{x_perm, wgu, offsets, nullptr, h, P, E, d, 2 * f, f, &hdr->tile_counter[0], &hdr->status};
+  MOE_CUDA(launch_grouped_gemm(g1, Epilogue::kSwiGLU, dev.num_sms, st), "gate/up GEMM launch");
+  MOE_CUDA(mark(4), "event record");
+  GroupedGemmProblem g2{h, wdn, offsets, row_w, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
+  MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
+  MOE_CUDA(mark(5), "event record");
+  // stage 5 (rows already carry their gate)
+  MOE_CUDA(launch_combine(y, dest_row, nullptr, T, k, d, out, dev.num_sms, st), "combine launch");
+  MOE_CUDA(mark(6), "event record");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_forward(const void* x, const float* logits, const void* packed, int64_t T, int32_t d, int32_t E,
+                         int32_t k, int32_t f, int32_t renormalize, void* out, int32_t* topk_idx_out,
+                         float* topk_w_out, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return forward_impl(x, logits, packed, T, d, E, k, f, renormalize, out, topk_idx_out, topk_w_out, workspace,
+                      workspace_bytes, stream, nullptr);
+}
+
+moe_status_t moe_forward_timed(const void* x, const float* logits, const void* packed, int64_t T, int32_t d,
+                               int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out, void* workspace,
+                               size_t workspace_bytes, moe_stream_t stream, void* const* events) {
+  if (!events) return fail(MOE_ERR_INVALID_ARG, "NULL events");
+  for (int i = 0; i <= MOE_FORWARD_STAGES; ++i)
+    if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "NULL event handle");
+  return forward_impl(x, logits, packed, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
+                      workspace_bytes, stream, events);
+}
+
+moe_status_t moe_forward_host(const void* x_host, const float* logits_host, void* out_host, void* x_dev,
+                              float* logits_dev, void* out_dev, const void* packed, int64_t T, int32_t d, int32_t E,
+                              int32_t k, int32_t f, int32_t renormalize, void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if (T > 0 && (!x_host || !logits_host || !out_host || !x_dev || !logits_dev || !out_dev))
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xb = static_cast<size_t>(T) * d * 2, lb = static_cast<size_t>(T) * E * 4;
+  if (T > 0) {
+    MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, st), "x copy to device");
+    MOE_CUDA(cudaMemcpyAsync(logits_dev, logits_host, lb, cudaMemcpyHostToDevice, st), "logits copy to device");
+  }
+  s = moe_forward(x_dev, logits_dev, packed, T, d, E, k, f, renormalize, out_dev, nullptr, nullptr, workspace,
+                  workspace_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (T > 0) MOE_CUDA(cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, st), "out copy to host");
+  MOE_CUDA(cudaStreamSynchronize(st), "stream synchronize");
+  return MOE_OK;
+}
+
+moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream, int32_t* status) {
+  if (!workspace || !status) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  MOE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");
+  MOE_CUDA(cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost), "status read");
+  return MOE_OK;
+}
+
+}  // extern "C"

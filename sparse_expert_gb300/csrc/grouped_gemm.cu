@@ -1,0 +1,455 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// "Scalable Pretraining of Large MoE LMs on Aurora Super Computer", §3.1,
+// Algorithm 1, stage 4: the expert MLP of every expert is one grouped GEMM
+// per projection over expert-contiguous rows, with boundaries given by the
+// cumulative token counts:
+//   gate_out = Grouped_mm(mlp_in, gate_weight); up_out likewise;
+//   mul_out = Silu(gate_out) * up_out;  mlp_out = Grouped_mm(mul_out, down_weight).
+// Here gate and up are one GEMM whose N tile holds matching gate and up
+// columns, so SiLU(gate)*up is the epilogue of that GEMM (H is written once,
+// in bf16); the down GEMM's epilogue multiplies each row by its gate.
+//
+// Scheduling follows "Training a 1T-Params MoE on EU public infrastructure",
+// Dynamic tile scheduling in SonicMoE: persistent blocks take tiles from a
+// shared atomic counter instead of a fixed per-block list, so blocks that
+// start late (their SM busy with other work) do not hold up the GEMM.
+//
+// Block of 192 threads, one per SM:
+//   warp 0   TMA producer: takes tile ids, streams A and B K-blocks into a
+//            ring of shared-memory stages (128-byte swizzle);
+//   warp 1   MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16)
+//            into one of two TMEM accumulators (double buffered);
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator, fp32 math, bf16
+//            stores; TMEM lane quadrant = warp % 4.
+// Tiles: BM=128 rows of one expert's group (the last tile of a group is
+// partial; rows past the group are computed and not stored), BN columns of
+// that expert's weights.  Tile t of the flat order walks experts in order,
+// and inside an expert the N tiles in order, each over all M tiles of the
+// group, so consecutive tiles share a weight tile in L2.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes: one swizzle row
+constexpr int UMMA_K = 16;
+constexpr int kThreads = 192;
+constexpr int kRing = 4;  // tile ids fetched ahead
+// dynamic shared memory for stage buffers: 227 KB per block minus room for
+// the alignment slack, barriers and two [E+1] tables (E <= 1024)
+constexpr int kStageBudget = 227 * 1024 - 1024 - 1024 - 2 * 1025 * 4;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kStageBudget / kStageBytes > 8 ? 8 : kStageBudget / kStageBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators
+  static constexpr uint32_t kIdesc = umma_idesc_bf16_f32(BM, BN);
+};
+
+struct Params {
+  const int32_t* offsets;
+  const float* row_scale;
+  __nv_bfloat16* out;
+  int32_t* tile_counter;
+  int32_t* status;
+  int E;
+  int K;
+  int n_per_expert;
+  int n_tiles;
+  int out_cols;
+};
+
+struct Smem {
+  uint64_t full[8], empty[8];
+  uint64_t tfull[2], tempty[2];
+  uint64_t rfull[kRing], rempty[kRing];
+  uint64_t drain;
+  int32_t ring[kRing];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Expert, M tile and N tile of flat tile t.  s_pre[e] = M tiles of experts
+// before e (s_pre[E] = all).  The largest e with s_pre[e]*nt <= t has a
+// non-empty range containing t.
+__device__ __forceinline__ void decode_tile(int t, const int32_t* s_pre, int E, int n_tiles, int& e, int& mt,
+                                            int& nt) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pre[mid] * n_tiles <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  e = lo;
+  const int mtiles = s_pre[e + 1] - s_pre[e];
+  const int local = t - s_pre[e] * n_tiles;
+  nt = local / mtiles;
+  mt = local - nt * mtiles;
+}
+
+template <int BN, bool kSwiGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ __align__(1024) uint8_t dyn_smem[];
+  // stage buffers need 1024-byte alignment for the 128-byte swizzle
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + C::kStages * C::kABytes;
+  Smem* S = reinterpret_cast<Smem*>(sB + C::kStages * C::kBBytes);
+  int32_t* s_off = reinterpret_cast<int32_t*>(S + 1);  // [E+1] group boundaries
+  int32_t* s_pre = s_off + (p.E + 1);                 // [E+1] M-tile prefix
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &S->abort;
+
+  // ---- set-up: group boundaries and M-tile prefix in shared memory
+  if (warp == 0) {
+    int carry = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      int lo = 0, hi = 0;
+      if (e < p.E) {
+        lo = __ldg(p.offsets + e);
+        hi = __ldg(p.offsets + e + 1);
+        s_off[e] = lo;
+        if (e == p.E - 1) s_off[p.E] = hi;
+      }
+      int v = (hi - lo + BM - 1) / BM;
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, s);
+        if (lane >= s) v += o;
+      }
+      if (e < p.E) s_pre[e + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_pre[0] = 0;
+  } else if (warp == 1) {
+    tmem_alloc(&S->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  } else if (warp == 2 && lane == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&S->full[i], 1);
+      mbar_init(&S->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S->tfull[i], 1);
+      mbar_init(&S->tempty[i], 4);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&S->rfull[i], 1);
+      mbar_init(&S->rempty[i], 1 + 4);
+    }
+    mbar_init(&S->drain, 1);
+    S->abort = 0;
+    fence_barrier_init();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+
+  const int total_tiles = s_pre[p.E] * p.n_tiles;
+  const int num_kb = (p.K + BK - 1) / BK;
+  const uint32_t tmem_base = S->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      int stage = 0;
+      uint32_t phase = 0;
+      int rs = 0;
+      uint32_t rphase = 0;
+      bool ok = true;
+      int last_stage = -1;
+      uint32_t last_phase = 0;
+      for (;;) {
+        if (!mbar_wait(&S->rempty[rs], rphase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        int t = atomicAdd(p.tile_counter, 1);
+        if (t >= total_tiles) t = -1;
+        S->ring[rs] = t;
+        mbar_arrive(&S->rfull[rs]);
+        if (++rs == kRing) {
+          rs = 0;
+          rphase ^= 1u;
+        }
+        if (t < 0) break;
+        int e, mt, nt;
+        decode_tile(t, s_pre, p.E, p.n_tiles, e, mt, nt);
+        const int row0 = s_off[e] + mt * BM;
+        const int brow = e * p.n_per_expert + nt * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&S->empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&S->full[stage], C::kStageBytes);
+          tma_load_2d(sA + stage * C::kABytes, &tm_a, &S->full[stage], kb * BK, row0);
+          tma_load_2d(sB + stage * C::kBBytes, &tm_b, &S->full[stage], kb * BK, brow);
+          last_stage = stage;
+          last_phase = phase;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (!ok) {
+        record_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        // let the last copy land before the block can exit
+        if (last_stage >= 0) {
+          volatile int never = 0;
+          mbar_wait(&S->full[last_stage], last_phase, &never);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int rs = 0;
+      uint32_t rphase = 0;
+      int acc = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (;;) {
+        if (!mbar_wait(&S->rfull[rs], rphase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int t = S->ring[rs];
+        mbar_arrive(&S->rempty[rs]);
+        if (++rs == kRing) {
+          rs = 0;
+          rphase ^= 1u;
+        }
+        if (t < 0) break;
+        if (!mbar_wait(&S->tempty[acc], aphase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&S->full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
+          const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t da = sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
+            const uint64_t db = sw128_kmajor_desc(b0 + kk * UMMA_K * 2);
+            umma_bf16(d_tmem, da, db, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&S->empty[stage]);  // frees the stage when these MMAs finish
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&S->tfull[acc]);  // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1u;
+      }
+      if (!ok) {
+        record_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      // every MMA issued by this thread has completed once drain flips
+      umma_commit(&S->drain);
+      volatile int never = 0;
+      mbar_wait(&S->drain, 0, &never);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    const int row_in_tile = quad * 32 + lane;
+    int rs = 0;
+    uint32_t rphase = 0;
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (;;) {
+      if (!mbar_wait_warp(&S->rfull[rs], rphase, abort_flag)) break;
+      const int t = S->ring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S->rempty[rs]);
+      if (++rs == kRing) {
+        rs = 0;
+        rphase ^= 1u;
+      }
+      if (t < 0) break;
+      int e, mt, nt;
+      decode_tile(t, s_pre, p.E, p.n_tiles, e, mt, nt);
+      const int64_t grow = static_cast<int64_t>(s_off[e]) + mt * BM + row_in_tile;
+      const bool valid = grow < s_off[e + 1];
+      if (!mbar_wait_warp(&S->tfull[acc], aphase, abort_flag)) {
+        if (lane == 0) {
+          record_status(p.status, kStatusTimeout);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (kSwiGLU) {
+        constexpr int H = BN / 2;  // gate columns [0, H), up columns [H, 2H)
+        __nv_bfloat16* dst = p.out + grow * p.out_cols + static_cast<int64_t>(nt) * H;
+#pragma unroll 1
+        for (int c = 0; c < H; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld_32x32(taddr + c, g);
+          tmem_ld_32x32(taddr + H + c, u);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float h0 = silu_f32(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+            const float h1 = silu_f32(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+            packed[i] = pack_bf16x2(h0, h1);
+          }
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        }
+      } else {
+        const float scale = (valid && p.row_scale != nullptr) ? __ldg(p.row_scale + grow) : 1.0f;
+        __nv_bfloat16* dst = p.out + grow * p.out_cols + static_cast<int64_t>(nt) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32(taddr + c, v);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = pack_bf16x2(scale * __uint_as_float(v[2 * i]), scale * __uint_as_float(v[2 * i + 1]));
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S->tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) aphase ^= 1u;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix, box [box_rows, 64],
+// 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool kSwiGLU>
+cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t stream) {
+  using C = Cfg<BN>;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, pb.a, pb.P, pb.K, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, pb.b, static_cast<int64_t>(pb.E) * pb.n_per_expert, pb.K, BN)) return cudaErrorInvalidValue;
+  Params prm;
+  prm.offsets = pb.offsets;
+  prm.row_scale = pb.row_scale;
+  prm.out = static_cast<__nv_bfloat16*>(pb.out);
+  prm.tile_counter = pb.tile_counter;
+  prm.status = pb.status;
+  prm.E = pb.E;
+  prm.K = pb.K;
+  prm.n_per_expert = pb.n_per_expert;
+  prm.n_tiles = pb.n_per_expert / BN;
+  prm.out_cols = pb.out_cols;
+  const size_t smem = 1024 + static_cast<size_t>(C::kStages) * C::kStageBytes + sizeof(Smem) +
+                      2 * static_cast<size_t>(pb.E + 1) * sizeof(int32_t);
+  auto kernel = grouped_gemm_kernel<BN, kSwiGLU>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  // persistent: one block per SM, never more blocks than an upper bound on tiles
+  const int64_t max_tiles = (pb.P / BM + pb.E) * static_cast<int64_t>(prm.n_tiles);
+  const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
+  kernel<<<grid, kThreads, smem, stream>>>(ma, mb, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream) {
+  if (pb.P == 0) return cudaSuccess;
+  if (epi == Epilogue::kSwiGLU) {
+    // N tile = matching gate and up halves of gate_up_half_tile(f) columns
+    const int half = pb.out_cols % 128 == 0 ? 128 : 64;
+    return half == 128 ? launch_bn<256, true>(pb, num_sms, stream) : launch_bn<128, true>(pb, num_sms, stream);
+  }
+  if (pb.out_cols % 256 == 0) return launch_bn<256, false>(pb, num_sms, stream);
+  if (pb.out_cols % 128 == 0) return launch_bn<128, false>(pb, num_sms, stream);
+  return launch_bn<64, false>(pb, num_sms, stream);
+}
+
+}  // namespace moe

@@ -1,0 +1,77 @@
+// Host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+// ---- stage 1
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renormalize, int32_t* topk_idx,
+                              float* topk_w, int32_t* counts, int num_sms, cudaStream_t stream);
+
+// ---- stages 2-3
+constexpr int kDispatchThreads = 256;
+constexpr int kDispatchPairsPerThread = 4;
+constexpr int kDispatchChunk = kDispatchThreads * kDispatchPairsPerThread;  // pairs per block
+
+inline int64_t dispatch_blocks(int64_t P) { return (P + kDispatchChunk - 1) / kDispatchChunk; }
+
+// Look-back state inside a workspace, after the 256-byte header.
+struct DispatchState {
+  int32_t* flags;  // [NB], cleared with the header
+  int32_t* agg;    // [NB, E]
+  int32_t* incl;   // [NB, E]
+};
+size_t dispatch_state_bytes(int64_t P, int E);            // flags + agg + incl, aligned
+size_t dispatch_clear_bytes(int64_t P);                   // header + flags
+DispatchState dispatch_state_at(void* base, int64_t P, int E);  // base = just after the header
+
+cudaError_t launch_histogram(const int32_t* topk_idx, int64_t P, int E, int32_t* counts, int32_t* status,
+                             int num_sms, cudaStream_t stream);
+cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P, int E, int k,
+                         const int32_t* counts, int32_t* offsets, int32_t* src_token, int32_t* dest_row,
+                         float* row_w, void* header, DispatchState st, cudaStream_t stream);
+
+// ---- stage 4 data movement and stage 5
+cudaError_t launch_permute(const void* x, int64_t T, int d, const int32_t* dest_row, int k, void* x_perm,
+                           int num_sms, cudaStream_t stream);
+cudaError_t launch_combine(const void* y, const int32_t* dest_row, const float* topk_w, int64_t T, int k, int d,
+                           void* out, int num_sms, cudaStream_t stream);
+
+// ---- weights
+int gate_up_half_tile(int f);  // N columns of gate (and of up) in one GEMM tile
+cudaError_t launch_pack_weights(const void* w_gate, const void* w_up, const void* w_down, int E, int d, int f,
+                                void* packed, cudaStream_t stream);
+
+// ---- stage 4 expert GEMMs
+struct GroupedGemmProblem {
+  const void* a;           // [P, K] bf16 (x_perm or h)
+  const void* b;           // packed weights of this projection, [E * n_per_expert, K] bf16
+  const int32_t* offsets;  // [E+1]
+  const float* row_scale;  // [P] or null (down projection only)
+  void* out;               // [P, out_cols] bf16
+  int64_t P;
+  int E;
+  int K;
+  int n_per_expert;        // 2f (gate/up) or d (down)
+  int out_cols;            // f or d
+  int32_t* tile_counter;   // zeroed before launch
+  int32_t* status;
+};
+enum class Epilogue { kSwiGLU, kScale };
+cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
+
+// Device properties of the current device (cached per device).
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int cc_major, cc_minor;
+};
+cudaError_t current_device_info(DeviceInfo* info);
+
+}  // namespace moe

@@ -1,0 +1,139 @@
+"""Parity of the whole layer forward (moe_forward) with the fp64 oracle.
+
+tiny and small: every intermediate and every output element.
+t1, skew, long (the 1T-model layer shape, 25 GB of weights): routing,
+counts, offsets and both index maps for all tokens bit for bit, and the
+values of H, Y and the output on a seeded token sample that includes
+tokens of the largest and smallest non-empty expert groups.  This is the
+launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.parity import (ExpertSlices, assert_gates_close, assert_values_close, pick_sample_tokens, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import sparse_expert_gb300 as m
+    return m
+
+
+def _run_forward(moe, inp):
+    cfg = inp["cfg"]
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
+    packed = moe.moe_pack_weights(inp["w_gate"], inp["w_up"], inp["w_down"])
+    ws = torch.empty(moe.moe_forward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device="cuda")
+    out = moe.moe_forward(inp["x"], inp["logits"], packed, E, k, f, cfg.renormalize, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    return out, ws, packed
+
+
+def _check_routing_and_index(inter, ridx, rw, E, k):
+    counts, offsets, src, dst = oracle.dispatch(ridx, E)
+    assert np.array_equal(to_np(inter["topk_idx"]), ridx)
+    assert_gates_close(to_np(inter["topk_w"]), rw, k)
+    assert np.array_equal(to_np(inter["counts"]), counts)
+    assert np.array_equal(to_np(inter["offsets"]), offsets)
+    assert np.array_equal(to_np(inter["src_token"]), src)
+    assert np.array_equal(to_np(inter["dest_row"]), dst)
+    return counts, offsets, src, dst
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_forward_full_parity(moe, name):
+    cfg = workloads.get(name)
+    inp = {kk: (v.cuda() if torch.is_tensor(v) else v) for kk, v in workloads.generate(cfg, seed=1).items()}
+    out, ws, _ = _run_forward(moe, inp)
+    inter = moe.forward_intermediates(ws, cfg.T, cfg.E, cfg.k, cfg.d, cfg.f)
+    ref = oracle.moe_forward(to_np(inp["x"]), to_np(inp["logits"]), to_np(inp["w_gate"]), to_np(inp["w_up"]),
+                             to_np(inp["w_down"]), cfg.k, cfg.renormalize)
+    _check_routing_and_index(inter, ref["idx"], ref["w"], cfg.E, cfg.k)
+    assert np.array_equal(to_np(inter["x_perm"]), ref["x_perm"])
+    assert_values_close(to_np(inter["h"]), ref["h"], "h")
+    row_w_gpu = to_np(inter["row_w"]).astype(np.float64)
+    assert_values_close(to_np(inter["y"]), ref["y"] * row_w_gpu[:, None], "y")
+    assert_values_close(to_np(out), ref["out"], "out")
+
+
+@pytest.mark.parametrize("name", ["t1", "skew", "long"])
+def test_forward_full_size_sampled(moe, name):
+    cfg = workloads.get(name)
+    inp = workloads.generate(cfg, seed=0, device="cuda")
+    out, ws, packed = _run_forward(moe, inp)
+    del packed
+    inter = moe.forward_intermediates(ws, cfg.T, cfg.E, cfg.k, cfg.d, cfg.f)
+    logits = to_np(inp["logits"])
+    ridx, rw = oracle.route_topk(logits, cfg.k, cfg.renormalize)
+    counts, offsets, src, dst = _check_routing_and_index(inter, ridx, rw, cfg.E, cfg.k)
+    if name == "long":
+        assert set(counts.tolist()) == {1365, 1366}
+    if name == "skew":
+        assert (counts == 0).sum() > 100 and counts.max() > 10000
+    toks = pick_sample_tokens(ridx, counts, n_random=16, seed=7)
+    x_rows = to_np(inp["x"][torch.from_numpy(toks).cuda()])
+    ref = oracle.moe_forward_tokens(x_rows, logits[toks], ExpertSlices(inp["w_gate"]), ExpertSlices(inp["w_up"]),
+                                    ExpertSlices(inp["w_down"]), cfg.k, cfg.renormalize)
+    rows = dst.reshape(cfg.T, cfg.k)[toks]                        # [n, k]
+    rows_t = torch.from_numpy(rows.reshape(-1)).cuda()
+    xp = to_np(inter["x_perm"][rows_t]).reshape(len(toks), cfg.k, cfg.d)
+    assert np.array_equal(xp, np.repeat(x_rows[:, None, :], cfg.k, axis=1))
+    h = to_np(inter["h"][rows_t]).reshape(len(toks), cfg.k, cfg.f)
+    y = to_np(inter["y"][rows_t]).reshape(len(toks), cfg.k, cfg.d)
+    assert_values_close(h, ref["h"], "h (sampled)")
+    assert_values_close(y, ref["y"] * ref["w"][:, :, None], "y (sampled)")
+    assert_values_close(to_np(out[torch.from_numpy(toks).cuda()]), ref["out"], "out (sampled)")
+    # every output row is finite and rows of untouched tokens were written
+    assert torch.isfinite(out.float()).all()
+
+
+def test_forward_is_deterministic(moe):
+    cfg = workloads.get("small")
+    inp = {kk: (v.cuda() if torch.is_tensor(v) else v) for kk, v in workloads.generate(cfg, seed=2).items()}
+    out1, ws, packed = _run_forward(moe, inp)
+    out2 = moe.moe_forward(inp["x"], inp["logits"], packed, cfg.E, cfg.k, cfg.f, True, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+
+
+def test_forward_from_host_buffers_matches(moe):
+    cfg = workloads.get("tiny")
+    inp = workloads.generate(cfg, seed=3)
+    dev = {kk: (v.cuda() if torch.is_tensor(v) else v) for kk, v in inp.items()}
+    out_dev, ws, packed = _run_forward(moe, dev)
+    x_h = inp["x"].pin_memory()
+    l_h = inp["logits"].pin_memory()
+    out_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(dev["x"])
+    l_d = torch.empty_like(dev["logits"])
+    o_d = torch.empty_like(dev["x"])
+    moe.moe_forward_host(x_h, l_h, out_h, x_d, l_d, o_d, packed, cfg.E, cfg.k, cfg.f, ws)
+    assert torch.equal(out_h, out_dev.cpu())
+
+
+def test_forward_without_renormalisation(moe):
+    cfg = workloads.custom("norenorm", T=300, d=128, E=16, k=4, f=128, renormalize=False)
+    inp = {kk: (v.cuda() if torch.is_tensor(v) else v) for kk, v in workloads.generate(cfg, seed=4).items()}
+    out, ws, _ = _run_forward(moe, inp)
+    ref = oracle.moe_forward(to_np(inp["x"]), to_np(inp["logits"]), to_np(inp["w_gate"]), to_np(inp["w_up"]),
+                             to_np(inp["w_down"]), cfg.k, False)
+    inter = moe.forward_intermediates(ws, cfg.T, cfg.E, cfg.k, cfg.d, cfg.f)
+    assert_gates_close(to_np(inter["topk_w"]), ref["w"], cfg.E)
+    assert_values_close(to_np(out), ref["out"], "out")
+
+
+def test_forward_zero_tokens(moe):
+    cfg = workloads.custom("empty", T=0, d=128, E=8, k=2, f=64)
+    packed = torch.zeros(moe.moe_packed_weight_bytes(8, 128, 64), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(256, moe.moe_forward_workspace_bytes(0, 8, 2, 128, 64)), dtype=torch.uint8, device="cuda")
+    out = moe.moe_forward(torch.empty(0, 128, dtype=torch.bfloat16, device="cuda"),
+                          torch.empty(0, 8, device="cuda"), packed, 8, 2, 64, workspace=ws)
+    assert out.shape == (0, 128)
+    assert moe.moe_read_device_status(ws) == 0
