@@ -9,6 +9,7 @@ MOE_ERR_NO_DEVICE).
 from __future__ import annotations
 
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -17,7 +18,7 @@ from concurrent.futures import ThreadPoolExecutor
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-BUILD = os.path.join(PKG, "_build")
+BUILD = os.path.join(PKG, "_build", platform.machine())
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 SOURCES = ["abi.cu", "route.cu", "dispatch.cu", "permute_combine.cu", "pack.cu", "grouped_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
