@@ -129,6 +129,34 @@ MOE_API moe_status_t moe_dispatch_scan(const int32_t* topk_idx, const float* top
                                moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_dispatch_scan_noalloc — the same counts, offsets and index maps as
+ * moe_dispatch_scan, for callers that cannot allocate device memory at
+ * call time: plugins and framework extensions that receive only their
+ * input and output buffers, and latency-critical loops that must not call
+ * cudaMalloc.  The pages have no counterpart of this entry point.
+ *   Arguments and outputs are those of moe_dispatch_scan, without the
+ *   workspace.  The scratch is a fixed 4 MiB device array inside the
+ *   library (held on every GPU that loads it until the process exits):
+ *   problems whose scratch, moe_dispatch_workspace_bytes(T, E, k), exceeds
+ *   4 MiB are rejected with MOE_ERR_UNSUPPORTED (for example E = 384 and
+ *   k = 8 fit up to about 170,000 tokens).
+ *   The first call on a device looks up the array's address with that
+ *   device current; make it before any stream capture.  All calls share
+ *   the array: calls that overlap on the GPU race and must be serialised
+ *   by the caller.  Allocates nothing (no cudaMalloc, cudaFree or
+ *   allocating library routine).  Device-detected errors are not readable
+ *   through moe_read_device_status; a pair with an out-of-range expert
+ *   index still gets dest_row = -1.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_NO_DEVICE,
+ *         MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_dispatch_scan_noalloc(const int32_t* topk_idx, const float* topk_w,
+                                       int64_t T, int32_t E, int32_t k,
+                                       int32_t* counts, int32_t* offsets,
+                                       int32_t* src_token, int32_t* dest_row, float* row_w,
+                                       moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Stage 4, first step — mlp_in = input[input_indices] (Algorithm 1,
  * stage 4), done from the token side: each token row of x is read once and
  * written to its k rows, x_perm[dest_row[t*k + j]] = x[t].  The result is

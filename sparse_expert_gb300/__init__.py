@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     forward_intermediates,
     moe_combine,
     moe_dispatch_scan,
+    moe_dispatch_scan_noalloc,
     moe_dispatch_workspace_bytes,
     moe_forward,
     moe_forward_host,

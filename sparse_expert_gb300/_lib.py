@@ -51,6 +51,7 @@ SIGNATURES = {
     "moe_route_topk": (_S, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_dispatch_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "moe_dispatch_scan": (_S, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_scan_noalloc": (_S, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (_S, [_P, _I64, _I32, _P, _I32, _P, _P]),
     "moe_packed_weight_bytes": (_SZ, [_I32, _I32, _I32]),
     "moe_pack_weights": (_S, [_P, _P, _P, _I32, _I32, _I32, _P, _P]),
@@ -136,6 +137,27 @@ def moe_dispatch_scan(topk_idx, E, topk_w=None, row_w=True, workspace=None, stre
                                  _ptr(dst), _ptr(rw), _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_dispatch_scan")
     return dict(counts=counts, offsets=offsets, src_token=src, dest_row=dst, row_w=rw, workspace=workspace)
+
+
+def moe_dispatch_scan_noalloc(topk_idx, E, topk_w=None, row_w=True, stream=None):
+    """moe_dispatch_scan without a workspace, for callers that cannot
+    allocate device memory at call time (the library's fixed 4 MiB device
+    scratch is used instead; overlapping calls race on it)."""
+    _contig(topk_idx, torch.int32, "topk_idx")
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    P = T * k
+    if topk_w is not None:
+        _contig(topk_w, torch.float32, "topk_w")
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    src = torch.empty(P, dtype=torch.int32, device=dev)
+    dst = torch.empty(P, dtype=torch.int32, device=dev)
+    rw = torch.empty(P, dtype=torch.float32, device=dev) if (row_w and topk_w is not None) else None
+    _check(lib.moe_dispatch_scan_noalloc(_ptr(topk_idx), _ptr(topk_w), T, E, k, _ptr(counts), _ptr(offsets),
+                                         _ptr(src), _ptr(dst), _ptr(rw), _stream(stream)),
+           "moe_dispatch_scan_noalloc")
+    return dict(counts=counts, offsets=offsets, src_token=src, dest_row=dst, row_w=rw)
 
 
 # ---------------------------------------------------------- stage 4 / 5

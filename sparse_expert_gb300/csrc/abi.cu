@@ -124,6 +124,8 @@ DispatchState dispatch_state_split(void* ws, size_t state_at, int64_t P, int E) 
 
 }  // namespace
 
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+
 cudaError_t current_device_info(DeviceInfo* info) {
   static DeviceInfo cache[64];
   static bool have[64] = {false};

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <string>
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -73,5 +74,8 @@ struct DeviceInfo {
   int cc_major, cc_minor;
 };
 cudaError_t current_device_info(DeviceInfo* info);
+
+// Sets the text moe_last_error returns on the calling host thread.
+void set_last_error(const std::string& msg);
 
 }  // namespace moe
