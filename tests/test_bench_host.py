@@ -1,0 +1,77 @@
+"""bench.py host logic on the CPU: the multi-rank timing reduction with two
+gloo ranks, the throughput formula, the algorithmic work per stage and the
+reference arm on the tiny workload."""
+import contextlib
+import io
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+import workloads
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    bench.dist_init(world, "gloo")
+    seconds = [0.25, 0.40][rank]            # rank 1 is the slow one
+    bench.barrier(world)
+    slowest = bench.max_over_ranks(seconds, world, device="cpu")
+    value = bench.job_throughput(1000, world, slowest)
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as fh:
+        json.dump({"slowest": slowest, "value": value}, fh)
+    torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks(tmp_path):
+    port = _free_port()
+    mp.spawn(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    for r in range(2):
+        res = json.load(open(tmp_path / f"r{r}.json"))
+        assert res["slowest"] == pytest.approx(0.40)
+        assert res["value"] == pytest.approx(2 * 1000 / 0.40)
+
+
+def test_single_rank_reduction_is_identity():
+    assert bench.max_over_ranks(1.5, 1) == 1.5
+    assert bench.job_throughput(16384 * 100, 1, 0.778) == pytest.approx(16384 * 100 / 0.778)
+
+
+def test_stage_work_of_the_1t_layer():
+    cfg = workloads.get("t1")
+    w = bench.stage_work(cfg)
+    P = 16384 * 8
+    assert w["gate_up"]["flops"] == 4 * P * 6144 * 1792 == 5_772_436_045_824
+    assert w["down"]["flops"] == 2 * P * 6144 * 1792
+    assert w["permute"]["bytes"] == 16384 * 6144 * 2 + P * 6144 * 2 + P * 4
+    assert w["combine"]["bytes"] == P * 6144 * 2 + 16384 * 6144 * 2 + P * 4
+    assert bench.weight_bytes_read(cfg, [1] * 384) == 384 * 3 * 6144 * 1792 * 2
+
+
+def test_peaks_fall_back_when_unmeasured(monkeypatch, tmp_path):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    p = bench.load_peaks()
+    assert p["source"] == "fallback" and p["hbm_gbs"] == 6800.0
+
+
+def test_reference_arm_prints_one_json_line():
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"])
+    lines = [l for l in buf.getvalue().splitlines() if l.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["unit"] == "tokens/s" and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+    assert rec["warmup"] >= 3
