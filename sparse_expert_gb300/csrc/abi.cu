@@ -6,7 +6,7 @@
 #include <cstring>
 #include <string>
 
-#include "../../include/moe_gb300.h"
+#include "moe_gb300.h"
 #include "common.cuh"
 #include "internal.h"
 

@@ -22,7 +22,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/moe_gb300.h"
+#include "moe_gb300.h"
 #include "common.cuh"
 #include "internal.h"
 
