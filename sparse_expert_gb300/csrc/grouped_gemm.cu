@@ -15,13 +15,14 @@
 // shared atomic counter instead of a fixed per-block list, so blocks that
 // start late (their SM busy with other work) do not hold up the GEMM.
 //
-// Block of 192 threads, one per SM:
+// Block of 320 threads, one per SM:
 //   warp 0   TMA producer: takes tile ids, streams A and B K-blocks into a
 //            ring of shared-memory stages (128-byte swizzle);
 //   warp 1   MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16)
 //            into one of two TMEM accumulators (double buffered);
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator, fp32 math, bf16
-//            stores; TMEM lane quadrant = warp % 4.
+//   warps 2-9 epilogue: tcgen05.ld of the accumulator, fp32 math, bf16
+//            stores; TMEM lane quadrant = warp % 4, and the two warps of a
+//            quadrant take one half of the tile's columns each.
 // Tiles: BM=128 rows of one expert's group (the last tile of a group is
 // partial; rows past the group are computed and not stored), BN columns of
 // that expert's weights.  Tile t of the flat order walks experts in order,
@@ -38,11 +39,14 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes: one swizzle row
 constexpr int UMMA_K = 16;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kRing = 4;  // tile ids fetched ahead
+constexpr int kStoreStageBytes = kEpiWarps * 32 * 64;  // epilogue store transpose, 2 KB per epilogue warp
 // dynamic shared memory for stage buffers: 227 KB per block minus room for
-// the alignment slack, barriers and two [E+1] tables (E <= 1024)
-constexpr int kStageBudget = 227 * 1024 - 1024 - 1024 - 2 * 1025 * 4;
+// the alignment slack, barriers, two [E+1] tables (E <= 1024) and the
+// epilogue store buffers
+constexpr int kStageBudget = 227 * 1024 - 1024 - 1024 - 2 * 1025 * 4 - 16 - kStoreStageBytes;
 
 template <int BN>
 struct Cfg {
@@ -97,6 +101,29 @@ __device__ __forceinline__ void decode_tile(int t, const int32_t* s_pre, int E, 
   mt = local - nt * mtiles;
 }
 
+// Stores one 32-column chunk of the epilogue warp's 32 tile rows.  Thread
+// `lane` holds row `lane` as 16 packed bf16x2 words (64 bytes).  Through a
+// 2 KB shared-memory transpose, each 16-byte global store instruction then
+// covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes.  In
+// the buffer, 16-byte piece j of row r sits at slot j ^ ((r >> 1) & 3),
+// so the row-wise writes and the row-pair reads are free of bank
+// conflicts.  Rows at or past `valid_rows` are not stored.
+__device__ __forceinline__ void store_chunk_coalesced(const uint32_t (&w)[16], uint4* sbuf, int lane,
+                                                      __nv_bfloat16* row0, int64_t ld, int valid_rows) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    sbuf[lane * 4 + (j ^ ((lane >> 1) & 3))] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2);
+    const int g = lane & 3;
+    const uint4 v = sbuf[r * 4 + (g ^ ((r >> 1) & 3))];
+    if (r < valid_rows) *reinterpret_cast<uint4*>(row0 + r * ld + g * 8) = v;
+  }
+  __syncwarp();
+}
+
 template <int BN, bool kSwiGLU>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -110,6 +137,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
   Smem* S = reinterpret_cast<Smem*>(sB + C::kStages * C::kBBytes);
   int32_t* s_off = reinterpret_cast<int32_t*>(S + 1);  // [E+1] group boundaries
   int32_t* s_pre = s_off + (p.E + 1);                 // [E+1] M-tile prefix
+  // [epilogue warps][32 rows][4 x 16 bytes] store transpose buffers
+  uint4* s_stage = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(s_pre + p.E + 1) + 15) & ~uintptr_t(15));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -147,11 +176,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S->tfull[i], 1);
-      mbar_init(&S->tempty[i], 4);
+      mbar_init(&S->tempty[i], kEpiWarps);
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&S->rfull[i], 1);
-      mbar_init(&S->rempty[i], 1 + 4);
+      mbar_init(&S->rempty[i], 1 + kEpiWarps);
     }
     mbar_init(&S->drain, 1);
     S->abort = 0;
@@ -286,8 +315,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
-    const int row_in_tile = quad * 32 + lane;
+    const int quad = warp & 3;         // TMEM lanes 32*quad .. 32*quad+31
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns
+    uint4* sbuf = s_stage + (warp - 2) * 32 * 4;
     int rs = 0;
     uint32_t rphase = 0;
     int acc = 0;
@@ -304,8 +334,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       if (t < 0) break;
       int e, mt, nt;
       decode_tile(t, s_pre, p.E, p.n_tiles, e, mt, nt);
-      const int64_t grow = static_cast<int64_t>(s_off[e]) + mt * BM + row_in_tile;
-      const bool valid = grow < s_off[e + 1];
+      // this warp's 32 rows of the tile start at global row wrow0
+      const int64_t wrow0 = static_cast<int64_t>(s_off[e]) + mt * BM + quad * 32;
+      const int valid_rows = static_cast<int>(min(static_cast<int64_t>(32), max(static_cast<int64_t>(0),
+                                                                                 s_off[e + 1] - wrow0)));
       if (!mbar_wait_warp(&S->tfull[acc], aphase, abort_flag)) {
         if (lane == 0) {
           record_status(p.status, kStatusTimeout);
@@ -315,15 +347,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       }
       tc_fence_after_sync();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      // hands the accumulator back to the MMA warp once this warp has read
+      // its last columns (the stores of the last chunk still follow)
+      auto release_accumulator = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S->tempty[acc]);
+      };
       if constexpr (kSwiGLU) {
         constexpr int H = BN / 2;  // gate columns [0, H), up columns [H, 2H)
-        __nv_bfloat16* dst = p.out + grow * p.out_cols + static_cast<int64_t>(nt) * H;
+        constexpr int kCols = H / 2;
+        const int c0 = half * kCols;
+        __nv_bfloat16* dst = p.out + wrow0 * p.out_cols + static_cast<int64_t>(nt) * H + c0;
 #pragma unroll 1
-        for (int c = 0; c < H; c += 32) {
+        for (int c = 0; c < kCols; c += 32) {
           uint32_t g[32], u[32];
-          tmem_ld_32x32(taddr + c, g);
-          tmem_ld_32x32(taddr + H + c, u);
+          tmem_ld_32x32(taddr + c0 + c, g);
+          tmem_ld_32x32(taddr + H + c0 + c, u);
           tmem_ld_wait();
+          if (c + 32 == kCols) release_accumulator();
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -331,36 +373,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             const float h1 = silu_f32(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
             packed[i] = pack_bf16x2(h0, h1);
           }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-          }
+          store_chunk_coalesced(packed, sbuf, lane, dst + c, p.out_cols, valid_rows);
         }
       } else {
-        const float scale = (valid && p.row_scale != nullptr) ? __ldg(p.row_scale + grow) : 1.0f;
-        __nv_bfloat16* dst = p.out + grow * p.out_cols + static_cast<int64_t>(nt) * BN;
+        constexpr int kCols = BN / 2;
+        const int c0 = half * kCols;
+        const float scale = (lane < valid_rows && p.row_scale != nullptr) ? __ldg(p.row_scale + wrow0 + lane) : 1.0f;
+        __nv_bfloat16* dst = p.out + wrow0 * p.out_cols + static_cast<int64_t>(nt) * BN + c0;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < kCols; c += 32) {
           uint32_t v[32];
-          tmem_ld_32x32(taddr + c, v);
+          tmem_ld_32x32(taddr + c0 + c, v);
           tmem_ld_wait();
+          if (c + 32 == kCols) release_accumulator();
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             packed[i] = pack_bf16x2(scale * __uint_as_float(v[2 * i]), scale * __uint_as_float(v[2 * i + 1]));
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-          }
+          store_chunk_coalesced(packed, sbuf, lane, dst + c, p.out_cols, valid_rows);
         }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S->tempty[acc]);
       acc ^= 1;
       if (acc == 0) aphase ^= 1u;
     }
@@ -427,7 +459,7 @@ cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t st
   prm.n_tiles = pb.n_per_expert / BN;
   prm.out_cols = pb.out_cols;
   const size_t smem = 1024 + static_cast<size_t>(C::kStages) * C::kStageBytes + sizeof(Smem) +
-                      2 * static_cast<size_t>(pb.E + 1) * sizeof(int32_t);
+                      2 * static_cast<size_t>(pb.E + 1) * sizeof(int32_t) + 16 + kStoreStageBytes;
   auto kernel = grouped_gemm_kernel<BN, kSwiGLU>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
