@@ -176,9 +176,15 @@ MOE_API moe_status_t moe_permute(const void* x, int64_t T, int32_t d, const int3
  *   w_gate, w_up [E, d, f] bf16 in (gate = x @ w_gate[e]);
  *   w_down       [E, f, d] bf16 in (y = h @ w_down[e]);
  *   packed       moe_packed_weight_bytes(E, d, f) bytes out (3*E*d*f bf16):
- *                gate and up transposed to [f, d] per expert and
- *                interleaved in blocks of the GEMM's N tile, then down
- *                transposed to [d, f] per expert.
+ *                the gate/up projection, then the down projection, each
+ *                stored K-major and tile-major: element (e, n, k) of a
+ *                projection with N tile BN and K = 64 * nkb sits at
+ *                (((e * N/BN + n/BN) * nkb + k/64) * BN + n%BN) * 64 + k%64,
+ *                so that one GEMM stage's weights are one contiguous block.
+ *                Gate/up: N = 2f, K = d, BN = 2h (h = 128 if f % 128 == 0,
+ *                else 64) and N tile t holds gate columns t*h .. t*h+h-1
+ *                then the same up columns.  Down: N = d, K = f, BN = 256,
+ *                128 or 64, the largest dividing d.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 MOE_API size_t moe_packed_weight_bytes(int32_t E, int32_t d, int32_t f);

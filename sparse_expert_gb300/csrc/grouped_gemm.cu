@@ -223,7 +223,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         int e, mt, nt;
         decode_tile(t, s_pre, p.E, p.n_tiles, e, mt, nt);
         const int row0 = s_off[e] + mt * BM;
-        const int brow = e * p.n_per_expert + nt * BN;
+        // weight tiles are stored tile-major: block (e, nt, kb) is BN x 64
+        const int bblk = (e * p.n_tiles + nt) * num_kb;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&S->empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -231,7 +232,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
           }
           mbar_arrive_expect_tx(&S->full[stage], C::kStageBytes);
           tma_load_2d(sA + stage * C::kABytes, &tm_a, &S->full[stage], kb * BK, row0);
-          tma_load_2d(sB + stage * C::kBBytes, &tm_b, &S->full[stage], kb * BK, brow);
+          tma_load_3d(sB + stage * C::kBBytes, &tm_b, &S->full[stage], 0, 0, bblk + kb);
           last_stage = stage;
           last_phase = phase;
           if (++stage == C::kStages) {
@@ -441,12 +442,27 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over tile-major weights: [blocks][bn rows][64], box one
+// block, 128-byte swizzle.
+bool make_weight_map(CUtensorMap* map, const void* ptr, int64_t blocks, int bn) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(bn), static_cast<cuuint64_t>(blocks)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(BK) * 2, static_cast<cuuint64_t>(bn) * BK * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(bn), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, bool kSwiGLU>
 cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap ma, mb;
   if (!make_map(&ma, pb.a, pb.P, pb.K, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, pb.b, static_cast<int64_t>(pb.E) * pb.n_per_expert, pb.K, BN)) return cudaErrorInvalidValue;
+  const int64_t blocks = static_cast<int64_t>(pb.E) * (pb.n_per_expert / BN) * ((pb.K + BK - 1) / BK);
+  if (!make_weight_map(&mb, pb.b, blocks, BN)) return cudaErrorInvalidValue;
   Params prm;
   prm.offsets = pb.offsets;
   prm.row_scale = pb.row_scale;
@@ -476,12 +492,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int 
   if (pb.P == 0) return cudaSuccess;
   if (epi == Epilogue::kSwiGLU) {
     // N tile = matching gate and up halves of gate_up_half_tile(f) columns
-    const int half = pb.out_cols % 128 == 0 ? 128 : 64;
-    return half == 128 ? launch_bn<256, true>(pb, num_sms, stream) : launch_bn<128, true>(pb, num_sms, stream);
+    return gate_up_tile_n(pb.out_cols) == 256 ? launch_bn<256, true>(pb, num_sms, stream)
+                                              : launch_bn<128, true>(pb, num_sms, stream);
   }
-  if (pb.out_cols % 256 == 0) return launch_bn<256, false>(pb, num_sms, stream);
-  if (pb.out_cols % 128 == 0) return launch_bn<128, false>(pb, num_sms, stream);
-  return launch_bn<64, false>(pb, num_sms, stream);
+  // N tile of the packed down weights
+  switch (down_tile_n(pb.out_cols)) {
+    case 256: return launch_bn<256, false>(pb, num_sms, stream);
+    case 128: return launch_bn<128, false>(pb, num_sms, stream);
+    default: return launch_bn<64, false>(pb, num_sms, stream);
+  }
 }
 
 }  // namespace moe

@@ -46,6 +46,8 @@ cudaError_t launch_combine(const void* y, const int32_t* dest_row, const float* 
 
 // ---- weights
 int gate_up_half_tile(int f);  // N columns of gate (and of up) in one GEMM tile
+int gate_up_tile_n(int f);     // N rows of one packed gate/up weight tile (2 * half tile)
+int down_tile_n(int d);        // N rows of one packed down weight tile (256, 128 or 64)
 cudaError_t launch_pack_weights(const void* w_gate, const void* w_up, const void* w_down, int E, int d, int f,
                                 void* packed, cudaStream_t stream);
 

@@ -159,7 +159,13 @@ def test_combine_single_slot_is_exact(moe):
 
 
 # ------------------------------------------------------------------- pack
-@pytest.mark.parametrize("E,d,f", [(8, 128, 64), (3, 256, 384), (2, 192, 192)])
+def _tile_major(w_nk, bn):
+    """[E, N, K] (K contiguous) -> blocks of bn rows x 64 K values, block order (e, N tile, K block)."""
+    E, N, K = w_nk.shape
+    return w_nk.reshape(E, N // bn, bn, K // 64, 64).permute(0, 1, 3, 2, 4).reshape(-1)
+
+
+@pytest.mark.parametrize("E,d,f", [(8, 128, 64), (3, 256, 384), (2, 192, 192), (2, 640, 128)])
 def test_pack_layout(moe, E, d, f):
     g = torch.Generator().manual_seed(E * d + f)
     wg = torch.randn(E, d, f, generator=g).to(torch.bfloat16)
@@ -167,14 +173,15 @@ def test_pack_layout(moe, E, d, f):
     wd = torch.randn(E, f, d, generator=g).to(torch.bfloat16)
     packed = moe.moe_pack_weights(wg.cuda(), wu.cuda(), wd.cuda()).cpu()
     h = 128 if f % 128 == 0 else 64
-    # gate/up: per expert, N blocks of [h gate rows | h up rows], each row a column of W over d
+    # gate/up: N tiles of [h gate columns | the same h up columns], each a row of K = d weights
     gt = wg.transpose(1, 2).reshape(E, f // h, h, d)
     ut = wu.transpose(1, 2).reshape(E, f // h, h, d)
-    want_gu = torch.stack([gt, ut], dim=2).reshape(E, 2 * f, d)
-    want_dn = wd.transpose(1, 2).contiguous()
+    gu_nk = torch.stack([gt, ut], dim=2).reshape(E, 2 * f, d)
+    bn_down = 256 if d % 256 == 0 else 128 if d % 128 == 0 else 64
+    dn_nk = wd.transpose(1, 2).contiguous()
     got = packed.view(torch.bfloat16)
-    assert torch.equal(got[: E * 2 * f * d].view(E, 2 * f, d), want_gu)
-    assert torch.equal(got[E * 2 * f * d:].view(E, d, f), want_dn)
+    assert torch.equal(got[: E * 2 * f * d], _tile_major(gu_nk, 2 * h))
+    assert torch.equal(got[E * 2 * f * d:], _tile_major(dn_nk, bn_down))
 
 
 # ------------------------------------------------------ grouped SwiGLU GEMM
