@@ -97,6 +97,23 @@ MOE_API moe_status_t moe_route_topk(const float* logits, int64_t T, int32_t E, i
                             moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stage 1 with group-limited routing ("Training a 1T-Params MoE on EU
+ * public infrastructure", Group-limited expert routing): the E experts are
+ * split into n_groups groups of consecutive indices, [g*E/G, (g+1)*E/G),
+ * and each token takes exactly k/G experts from every group (its best ones
+ * inside the group, same order and ties as moe_route_topk), so every group
+ * receives exactly T*k/G pairs.  Slots hold the k selected experts in
+ * descending logit order; gates as in moe_route_topk (softmax over all E,
+ * renormalised over the selected k when renormalize != 0).
+ * n_groups = 1 is moe_route_topk.
+ * Errors: as moe_route_topk, and MOE_ERR_UNSUPPORTED when n_groups < 1 or
+ * does not divide both E and k.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_route_topk_grouped(const float* logits, int64_t T, int32_t E, int32_t k,
+                                    int32_t n_groups, int32_t renormalize,
+                                    int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Stages 2 and 3 — token counts, group boundaries and index generation
  * (Algorithm 1, stages 2-3), as one stable counting sort of the P pairs
  * p = t*k + j by expert:

@@ -6,6 +6,7 @@ It shares no code with the CUDA path and imports nothing from it.
 """
 from .moe_oracle import (  # noqa: F401
     route_topk,
+    route_topk_grouped,
     softmax_rows,
     dispatch,
     permute,

@@ -76,6 +76,43 @@ def route_topk(logits: np.ndarray, k: int, renormalize: bool = True):
     return idx, w
 
 
+def route_topk_grouped(logits: np.ndarray, k: int, n_groups: int, renormalize: bool = True):
+    """Group-limited top-k routing.
+
+    "Training a 1T-Params MoE on EU public infrastructure", Group-limited
+    expert routing: the experts are split into n_groups equal groups
+    (consecutive expert indices) and the router selects the same number of
+    experts, k / n_groups, from every group.  Inside a group the choice is
+    the ordinary top-(k/n_groups) under (logit descending, expert index
+    ascending).  The k selected experts fill the slots in that same order
+    across groups, and the gates are their softmax probabilities over all
+    E experts (divided by the sum over the k selected when
+    ``renormalize``), as in ``route_topk``.
+    """
+    l32 = np.asarray(logits, dtype=np.float32)
+    T, E = l32.shape
+    if n_groups < 1 or E % n_groups or k % n_groups:
+        raise ValueError("n_groups must divide E and k")
+    size, per = E // n_groups, k // n_groups
+    if per > size:
+        raise ValueError("k / n_groups exceeds the group size")
+    chosen = []
+    for g in range(n_groups):
+        block = l32[:, g * size:(g + 1) * size]
+        order = np.argsort(-block, axis=1, kind="stable")[:, :per]
+        chosen.append(order + g * size)
+    cand = np.concatenate(chosen, axis=1)                       # [T, k], group order
+    vals = np.take_along_axis(l32, cand, axis=1)
+    # slot order over the selection: value descending, then expert ascending
+    slot = np.lexsort((cand, -vals), axis=1)
+    idx = np.take_along_axis(cand, slot, axis=1).astype(np.int32)
+    probs = softmax_rows(l32)
+    w = np.take_along_axis(probs, idx.astype(np.int64), axis=1)
+    if renormalize:
+        w = w / w.sum(axis=1, keepdims=True)
+    return idx, w
+
+
 # ---------------------------------------------------------- stages 2 and 3
 def dispatch(idx: np.ndarray, E: int):
     """Counts, group boundaries and the two index maps.

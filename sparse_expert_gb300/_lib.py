@@ -49,6 +49,7 @@ SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [_S]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_route_topk": (_S, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
+    "moe_route_topk_grouped": (_S, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "moe_dispatch_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "moe_dispatch_scan": (_S, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_scan_noalloc": (_S, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]),
@@ -101,14 +102,19 @@ def abi_version() -> int:
 
 
 # --------------------------------------------------------------- stage 1
-def moe_route_topk(logits, k, renormalize=True, stream=None):
-    """topk_idx int32 [T,k], topk_w fp32 [T,k] of fp32 router logits [T,E]."""
+def moe_route_topk(logits, k, renormalize=True, n_groups=1, stream=None):
+    """topk_idx int32 [T,k], topk_w fp32 [T,k] of fp32 router logits [T,E];
+    n_groups > 1 takes k/n_groups experts from each group of consecutive experts."""
     _contig(logits, torch.float32, "logits")
     T, E = logits.shape
     idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
     w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
-    _check(lib.moe_route_topk(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(idx), _ptr(w), _stream(stream)),
-           "moe_route_topk")
+    if n_groups == 1:
+        _check(lib.moe_route_topk(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(idx), _ptr(w),
+                                  _stream(stream)), "moe_route_topk")
+    else:
+        _check(lib.moe_route_topk_grouped(_ptr(logits), T, E, k, n_groups, int(bool(renormalize)), _ptr(idx),
+                                          _ptr(w), _stream(stream)), "moe_route_topk_grouped")
     return idx, w
 
 

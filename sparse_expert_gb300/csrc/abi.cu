@@ -182,9 +182,25 @@ moe_status_t moe_route_topk(const float* logits, int64_t T, int32_t E, int32_t k
   if (T == 0) return MOE_OK;
   DeviceInfo dev;
   if ((s = device_info(&dev)) != MOE_OK) return s;
-  MOE_CUDA(launch_route_topk(logits, T, E, k, renormalize, topk_idx, topk_w, nullptr, dev.num_sms,
+  MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, nullptr, dev.num_sms,
                              static_cast<cudaStream_t>(stream)),
            "route_topk launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_route_topk_grouped(const float* logits, int64_t T, int32_t E, int32_t k, int32_t n_groups,
+                                    int32_t renormalize, int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if (n_groups < 1 || E % n_groups != 0 || k % n_groups != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "n_groups must be >= 1 and divide both E and k");
+  if (T > 0 && (!logits || !topk_idx || !topk_w)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T == 0) return MOE_OK;
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  MOE_CUDA(launch_route_topk(logits, T, E, k, n_groups, renormalize, topk_idx, topk_w, nullptr, dev.num_sms,
+                             static_cast<cudaStream_t>(stream)),
+           "route_topk_grouped launch");
   return MOE_OK;
 }
 
@@ -377,7 +393,8 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* packed
     return MOE_OK;
   }
   // stage 1 (+ token counts)
-  MOE_CUDA(launch_route_topk(logits, T, E, k, renormalize, topk_idx, topk_w, counts, dev.num_sms, st), "route launch");
+  MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, counts, dev.num_sms, st),
+           "route launch");
   MOE_CUDA(mark(1), "event record");
   // stages 2-3: offsets, index maps and the gate of every row
   DispatchState dstate = dispatch_state_split(ws, L.dispatch_state, P, E);

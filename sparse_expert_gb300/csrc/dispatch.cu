@@ -6,7 +6,7 @@
 // (expert, thread), prefix-sum the expert-major count table, and let each
 // (expert, thread) write rows from its base with a running counter.  The
 // result is a stable counting sort of the pairs by expert.  Here the same
-// sort is done by blocks of 1,024 consecutive pairs:
+// sort is done by blocks of 2,048 consecutive pairs:
 //   1. a histogram gives complete per-expert counts (or the route kernel
 //      produces them on the fly);
 //   2. one pass in which every block ranks its pairs within the block

@@ -12,12 +12,12 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
 // ---- stage 1
-cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renormalize, int32_t* topk_idx,
-                              float* topk_w, int32_t* counts, int num_sms, cudaStream_t stream);
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int n_groups, int renormalize,
+                              int32_t* topk_idx, float* topk_w, int32_t* counts, int num_sms, cudaStream_t stream);
 
 // ---- stages 2-3
 constexpr int kDispatchThreads = 256;
-constexpr int kDispatchPairsPerThread = 4;
+constexpr int kDispatchPairsPerThread = 8;
 constexpr int kDispatchChunk = kDispatchThreads * kDispatchPairsPerThread;  // pairs per block
 
 inline int64_t dispatch_blocks(int64_t P) { return (P + kDispatchChunk - 1) / kDispatchChunk; }

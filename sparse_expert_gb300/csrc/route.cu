@@ -11,16 +11,60 @@ namespace {
 
 constexpr int kRouteWarps = 8;  // tokens per block
 
-// Strict total order of (value, expert): larger value first, then the
-// smaller expert index.  -0.0 == +0.0 under IEEE comparison.
-__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
-  return v > bv || (v == bv && e < be);
+// (logit, expert) as one 64-bit key whose unsigned order is the selection
+// order: larger logit first, then the smaller expert index.  The high word
+// is the float's bits made monotone (negative values inverted, sign bit set
+// on the others) after folding -0.0 onto +0.0; the low word decreases with
+// the expert index.  Key 0 is below every finite logit's key.
+__device__ __forceinline__ uint64_t route_key(float x, int e) {
+  uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+
+__device__ __forceinline__ float key_logit(uint64_t key) {
+  uint32_t u = static_cast<uint32_t>(key >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ int key_expert(uint64_t key) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t b) {
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, b, s);
+    b = o > b ? o : b;
+  }
+  return b;
+}
+
+// Bitonic sort of one key per lane into descending lane order.
+__device__ __forceinline__ uint64_t warp_sort_desc_u64(uint64_t v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    }
+  }
+  return v;
 }
 
 // NV logits per lane: lane l holds experts l, l+32, ..., l+32*(NV-1).
+// Round j takes the warp maximum of the lanes' best keys; only the lane
+// that held it drops that key and rescans its own values.
+// With n_groups > 1 ("Training a 1T-Params MoE on EU public
+// infrastructure", Group-limited expert routing), group g = experts
+// [g*E/G, (g+1)*E/G) gets k/G rounds restricted to its own experts, and a
+// warp sort puts the k winners back in descending slot order.
 template <int NV>
 __global__ void __launch_bounds__(kRouteWarps * 32)
-route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int renormalize,
+route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int n_groups, int renormalize,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts) {
   extern __shared__ int32_t s_hist[];  // [E] when counts != nullptr
   const int lane = threadIdx.x & 31;
@@ -34,71 +78,74 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp; t < T; t += warps_total) {
     const float* row = logits + t * E;
     float v[NV];
+    uint64_t key[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+      v[i] = (e < E) ? __ldg(row + e) : 0.0f;
     }
-    // the maximum is the best expert's logit; find it first for the softmax
-    float mx = -INFINITY;
+    uint64_t lbest = 0;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) mx = fmaxf(mx, v[i]);
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-    float denom_all = 0.f;
-    if (!renormalize) {
-#pragma unroll
-      for (int i = 0; i < NV; ++i)
-        if (lane + 32 * i < E) denom_all += expf(v[i] - mx);
-#pragma unroll
-      for (int s = 16; s > 0; s >>= 1) denom_all += __shfl_xor_sync(0xffffffffu, denom_all, s);
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = (e < E) ? route_key(v[i], e) : 0ull;
+      lbest = key[i] > lbest ? key[i] : lbest;
     }
-
-    // k rounds of a warp argmax under the total order; the winner is removed
-    float my_val = 0.f;  // lane j keeps the j-th selection
-    int my_idx = 0;
-    uint32_t taken = 0;  // bit i: this lane's expert lane + 32*i is already selected
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+    uint64_t mine = 0, first = 0;
+    if (n_groups == 1) {
+      for (int j = 0; j < k; ++j) {
+        const uint64_t b = warp_max_u64(lbest);
+        if (j == 0) first = b;
+        if (lane == j) mine = b;
+        if (lbest == b) {  // keys are unique: exactly one lane held it
+          lbest = 0;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, be)) {
-          bv = v[i];
-          be = e;
+          for (int i = 0; i < NV; ++i) {
+            if (key[i] == b) key[i] = 0;
+            lbest = key[i] > lbest ? key[i] : lbest;
+          }
         }
       }
+    } else {
+      const int gsize = E / n_groups, per = k / n_groups;
+      int j = 0;
+      for (int g = 0; g < n_groups; ++g) {
+        const int lo = g * gsize, hi = lo + gsize;
+        for (int r = 0; r < per; ++r, ++j) {
+          uint64_t lb = 0;
 #pragma unroll
-      for (int s = 16; s > 0; s >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, s);
-        if (better(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
+          for (int i = 0; i < NV; ++i) {
+            const int e = lane + 32 * i;
+            if (e >= lo && e < hi && key[i] > lb) lb = key[i];
+          }
+          const uint64_t b = warp_max_u64(lb);
+          if (lane == j) mine = b;
+#pragma unroll
+          for (int i = 0; i < NV; ++i)
+            if (key[i] == b) key[i] = 0;
         }
       }
-      if (lane == j) {
-        my_val = bv;
-        my_idx = be;
-      }
-      // remove the winner (it lives in lane be % 32, slot be / 32)
-#pragma unroll
-      for (int i = 0; i < NV; ++i)
-        if (lane + 32 * i == be) taken |= 1u << i;
+      mine = warp_sort_desc_u64(mine, lane);  // lanes >= k hold key 0
+      first = __shfl_sync(0xffffffffu, mine, 0);
     }
-    // gates
-    const float z = (lane < k) ? expf(my_val - mx) : 0.f;
-    float denom = denom_all;
+    const float mx = key_logit(first);
+    const float z = (lane < k) ? expf(key_logit(mine) - mx) : 0.0f;
+    float denom = 0.0f;
     if (renormalize) {
       denom = z;
+    } else {
 #pragma unroll
-      for (int s = 16; s > 0; s >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, s);
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i < E) denom += expf(v[i] - mx);
     }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, s);
+    denom = __shfl_sync(0xffffffffu, denom, 0);  // one rounding for every slot
     if (lane < k) {
-      topk_idx[t * k + lane] = my_idx;
+      const int e = key_expert(mine);
+      topk_idx[t * k + lane] = e;
       topk_w[t * k + lane] = z / denom;
-      if (counts) atomicAdd(&s_hist[my_idx], 1);
+      if (counts) atomicAdd(&s_hist[e], 1);
     }
   }
 
@@ -113,8 +160,8 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
 
 }  // namespace
 
-cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int renormalize, int32_t* topk_idx,
-                              float* topk_w, int32_t* counts, int num_sms, cudaStream_t stream) {
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int n_groups, int renormalize,
+                              int32_t* topk_idx, float* topk_w, int32_t* counts, int num_sms, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int64_t blocks_needed = (T + kRouteWarps - 1) / kRouteWarps;
   const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
@@ -122,8 +169,8 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int 
   const size_t smem = counts ? static_cast<size_t>(E) * sizeof(int32_t) : 0;
   const int nv = (E + 31) / 32;
 #define MOE_ROUTE_CASE(NV)                                                                                     \
-  route_topk_kernel<NV><<<grid, kRouteWarps * 32, smem, stream>>>(logits, T, E, k, renormalize, topk_idx, topk_w, \
-                                                                  counts);                                     \
+  route_topk_kernel<NV><<<grid, kRouteWarps * 32, smem, stream>>>(logits, T, E, k, n_groups, renormalize, topk_idx, \
+                                                                  topk_w, counts);                             \
   break;
   switch (nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : nv <= 12 ? 12 : nv <= 16 ? 16 : 32) {
     case 1: MOE_ROUTE_CASE(1)

@@ -234,3 +234,30 @@ def test_grouped_swiglu_empty_and_huge_groups(moe):
 def test_grouped_swiglu_single_expert_long_k(moe):
     # E=1: one group covering every row; d = 2048 gives 32 K blocks
     _gemm_case(moe, 700, 2048, 1, 1, 256, seed=9)
+
+
+# ---------------------------------------------------- group-limited routing
+@pytest.mark.parametrize("T,E,k,G,ties", [(16384, 384, 8, 4, False), (16384, 384, 8, 8, False), (500, 8, 4, 2, True),
+                                          (300, 64, 8, 2, True), (200, 48, 6, 3, False), (100, 64, 32, 4, False),
+                                          (257, 1024, 8, 4, True)])
+def test_grouped_route_matches_oracle(moe, T, E, k, G, ties):
+    g = torch.Generator().manual_seed(T + E + k + G)
+    l = torch.randn(T, E, generator=g)
+    if ties:
+        l = torch.round(l * 2) / 2
+        l[torch.rand(T, E, generator=g) < 0.1] = -0.0
+    for renorm in (True, False):
+        idx, w = moe.moe_route_topk(l.cuda(), k, renorm, n_groups=G)
+        ridx, rw = oracle.route_topk_grouped(l.numpy(), k, G, renorm)
+        assert np.array_equal(to_np(idx), ridx)
+        assert_gates_close(to_np(w), rw, k if renorm else E)
+
+
+def test_grouped_route_balances_expert_groups_on_gpu(moe):
+    cfg = workloads.get("skew")  # a router that strongly prefers a few experts
+    l = _logits_for("skew").cuda()
+    G = 4
+    idx, w = moe.moe_route_topk(l, cfg.k, True, n_groups=G)
+    res = moe.moe_dispatch_scan(idx, cfg.E, topk_w=w)
+    per_group = to_np(res["counts"]).reshape(G, -1).sum(axis=1)
+    assert per_group.tolist() == [cfg.T * cfg.k // G] * G

@@ -97,3 +97,11 @@ def test_combine_without_gates_is_caught(monkeypatch):
     real = om.combine
     monkeypatch.setattr(oracle, "combine", lambda y, dest_row, w: real(y, dest_row, np.ones_like(w)))
     _fails(pins.test_combine_of_identity_experts_returns_input)
+
+
+def test_grouped_route_ignoring_groups_is_caught(monkeypatch):
+    import oracle
+    real = om.route_topk
+    monkeypatch.setattr(oracle, "route_topk_grouped", lambda l, k, G, renormalize=True: real(l, k, renormalize))
+    _fails(pins.test_grouped_route_balances_the_groups)
+    _fails(pins.test_grouped_route_golden, load_golden)

@@ -307,3 +307,57 @@ def test_combine_k1_is_gate_times_row():
 def test_permute_is_row_gather():
     x = np.arange(12.0).reshape(4, 3)
     assert np.array_equal(oracle.permute(x, [3, 0, 0, 2]), x[[3, 0, 0, 2]])
+
+
+# ------------------------------------------------------- grouped routing
+def _brute_grouped(row, k, G):
+    E = len(row)
+    size, per = E // G, k // G
+    picked = []
+    for g in range(G):
+        sub = list(range(g * size, (g + 1) * size))
+        picked += [sub[i] for i in _brute_topk([row[e] for e in sub], per)]
+    # slots: value descending, then index ascending
+    return sorted(picked, key=lambda e: (-row[e], e))
+
+
+@pytest.mark.parametrize("T,E,k,G,ties", [(30, 8, 4, 2, False), (30, 16, 8, 4, True), (20, 12, 6, 3, True),
+                                          (10, 64, 8, 8, False), (15, 8, 8, 2, False)])
+def test_grouped_route_matches_brute_force(T, E, k, G, ties):
+    l = _random_logits(_rng(T + E + k + G), T, E, ties)
+    idx, w = oracle.route_topk_grouped(l, k, G)
+    for t in range(T):
+        assert list(idx[t]) == _brute_grouped([float(v) for v in l[t]], k, G)
+        np.testing.assert_allclose(w[t], scipy.special.softmax(l[t, idx[t]].astype(np.float64)), rtol=1e-14)
+
+
+def test_grouped_route_with_one_group_is_plain_topk():
+    l = _random_logits(_rng(21), 40, 16, ties=True)
+    for renorm in (True, False):
+        gi, gw = oracle.route_topk_grouped(l, 4, 1, renorm)
+        ri, rw = oracle.route_topk(l, 4, renorm)
+        assert np.array_equal(gi, ri)
+        np.testing.assert_allclose(gw, rw, rtol=1e-15)
+
+
+def test_grouped_route_balances_the_groups():
+    """Every group receives the same number of (token, expert) pairs,
+    T*k/G: the property the page uses to give every GPU the same load."""
+    T, E, k, G = 500, 384, 8, 4
+    l = _random_logits(_rng(5), T, E)
+    l[:, :96] += 2.0  # a router that prefers group 0 still gives it only T*k/G
+    idx, _ = oracle.route_topk_grouped(l, k, G)
+    counts, _, _, _ = oracle.dispatch(idx, E)
+    assert list(counts.reshape(G, -1).sum(axis=1)) == [T * k // G] * G
+    plain, _ = oracle.route_topk(l, k)
+    pc, _, _, _ = oracle.dispatch(plain, E)
+    assert pc.reshape(G, -1).sum(axis=1)[0] > T * k // G  # the unconstrained router is unbalanced
+
+
+def test_grouped_route_golden(golden):
+    g = golden("route_example.json")
+    for case in g["grouped_cases"]:
+        idx, w = oracle.route_topk_grouped(np.array([case["logits"]], dtype=np.float32), case["k"], case["n_groups"],
+                                           case["renormalize"])
+        assert list(idx[0]) == case["idx"]
+        np.testing.assert_allclose(w[0], case["w"], rtol=1e-15)
