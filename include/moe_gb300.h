@@ -114,6 +114,30 @@ MOE_API moe_status_t moe_route_topk_grouped(const float* logits, int64_t T, int3
                                     int32_t* topk_idx, float* topk_w, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stage 1 with the router linear layer fused (Algorithm 1, stage 1:
+ * logits = Router(input); Softmax; TopK): the logits x @ w_router of a
+ * 128-token tile are accumulated on the tensor cores (bf16 operands, fp32
+ * accumulation) and reduced to the top-k in the same kernel, without being
+ * written to memory.  Selection order, ties and gates as moe_route_topk,
+ * applied to those fp32 logits.
+ *   w_router  [d, E] bf16, packed once by moe_pack_router_weights into
+ *             moe_router_packed_bytes(d, E) bytes (K-major, E padded with
+ *             zero columns to a multiple of 128);
+ *   x         [T, d] bf16; topk_idx [T, k] int32 out; topk_w [T, k] fp32 out;
+ *   workspace 256 bytes (status word).
+ * Supported: E <= 512, d a multiple of 64 in [64, 65536], k <= min(E, 32).
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE,
+ *         MOE_ERR_NO_DEVICE, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API size_t moe_router_packed_bytes(int32_t d, int32_t E);
+MOE_API moe_status_t moe_pack_router_weights(const void* w_router, int32_t d, int32_t E, void* packed,
+                                     moe_stream_t stream);
+MOE_API moe_status_t moe_router_topk(const void* x, const void* router_packed, int64_t T, int32_t d,
+                             int32_t E, int32_t k, int32_t renormalize,
+                             int32_t* topk_idx, float* topk_w,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Stages 2 and 3 — token counts, group boundaries and index generation
  * (Algorithm 1, stages 2-3), as one stable counting sort of the P pairs
  * p = t*k + j by expert:
@@ -272,6 +296,18 @@ MOE_API moe_status_t moe_forward(const void* x, const float* logits, const void*
                          int32_t renormalize, void* out,
                          int32_t* topk_idx_out, float* topk_w_out,
                          void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_forward starting from the tokens and the router weights: stage 1 is
+ * the fused router (moe_router_topk, with the token counts of stage 2 kept
+ * on the side), so the router logits never exist in memory.  Other
+ * arguments, the workspace and the layout are those of moe_forward.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_forward_routed(const void* x, const void* router_packed, const void* packed,
+                                int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
+                                int32_t renormalize, void* out,
+                                int32_t* topk_idx_out, float* topk_w_out,
+                                void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_forward with stage timing: identical work, plus cudaEventRecord of

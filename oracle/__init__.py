@@ -7,6 +7,7 @@ It shares no code with the CUDA path and imports nothing from it.
 from .moe_oracle import (  # noqa: F401
     route_topk,
     route_topk_grouped,
+    router_topk,
     softmax_rows,
     dispatch,
     permute,

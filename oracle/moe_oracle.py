@@ -113,6 +113,29 @@ def route_topk_grouped(logits: np.ndarray, k: int, n_groups: int, renormalize: b
     return idx, w
 
 
+def router_topk(x, w_router, k: int, renormalize: bool = True):
+    """Router linear layer, then Softmax and TopK, all in fp64.
+
+    Algorithm 1, stage 1: logits = Router(input) with Router a linear layer
+    (logits[t, e] = sum_i x[t, i] * w_router[i, e]), probs = Softmax(logits),
+    weights, indices = TopK(probs).  The logits are exact fp64 products of
+    the bf16 inputs and are ranked in fp64 (logit descending, expert index
+    ascending).  Returns (idx int32 [T,k], w float64 [T,k], logits float64
+    [T,E]).
+    """
+    logits = np.asarray(x, dtype=np.float64) @ np.asarray(w_router, dtype=np.float64)
+    T, E = logits.shape
+    if not (1 <= k <= E):
+        raise ValueError("need 1 <= k <= E")
+    order = np.argsort(-logits, axis=1, kind="stable")
+    idx = order[:, :k].astype(np.int32)
+    probs = softmax_rows(logits)
+    w = np.take_along_axis(probs, idx.astype(np.int64), axis=1)
+    if renormalize:
+        w = w / w.sum(axis=1, keepdims=True)
+    return idx, w, logits
+
+
 # ---------------------------------------------------------- stages 2 and 3
 def dispatch(idx: np.ndarray, E: int):
     """Counts, group boundaries and the two index maps.
@@ -213,16 +236,20 @@ def moe_forward(x, logits, w_gate, w_up, w_down, k, renormalize=True):
                 dest_row=dest_row, row_w=row_w, x_perm=x_perm, h=h, y=y, out=out)
 
 
-def moe_forward_tokens(x_rows, logits_rows, w_gate, w_up, w_down, k, renormalize=True):
+def moe_forward_tokens(x_rows, logits_rows, w_gate, w_up, w_down, k, renormalize=True, routing=None):
     """Layer output for a few tokens only.
 
     Routing, the expert MLP and the reduction of one token depend on that
     token's own row of x and logits alone, so the layer restricted to a
-    token subset is the layer applied to those rows.  Returns idx, w,
+    token subset is the layer applied to those rows.  ``routing`` = (idx, w)
+    replaces the routing of ``logits_rows`` when given.  Returns idx, w,
     per-slot h [n,k,f] and y [n,k,d] (unscaled) and out [n,d].
     """
     x_rows = np.asarray(x_rows, dtype=np.float64)
-    idx, w = route_topk(logits_rows, k, renormalize)
+    if routing is None:
+        idx, w = route_topk(logits_rows, k, renormalize)
+    else:
+        idx, w = (np.asarray(a) for a in routing)
     n = x_rows.shape[0]
     f = w_gate.shape[2]
     d = w_down.shape[2]

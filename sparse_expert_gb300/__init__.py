@@ -16,6 +16,9 @@ from ._lib import (  # noqa: F401
     moe_forward_host,
     moe_forward_layout,
     moe_forward_timed,
+    moe_forward_routed,
+    moe_pack_router_weights,
+    moe_router_topk,
     FORWARD_STAGES,
     moe_forward_workspace_bytes,
     moe_grouped_swiglu,

@@ -50,6 +50,10 @@ SIGNATURES = {
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_route_topk": (_S, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_route_topk_grouped": (_S, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P]),
+    "moe_router_packed_bytes": (_SZ, [_I32, _I32]),
+    "moe_pack_router_weights": (_S, [_P, _I32, _I32, _P, _P]),
+    "moe_router_topk": (_S, [_P, _P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "moe_forward_routed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "moe_dispatch_scan": (_S, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_scan_noalloc": (_S, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]),
@@ -115,6 +119,27 @@ def moe_route_topk(logits, k, renormalize=True, n_groups=1, stream=None):
     else:
         _check(lib.moe_route_topk_grouped(_ptr(logits), T, E, k, n_groups, int(bool(renormalize)), _ptr(idx),
                                           _ptr(w), _stream(stream)), "moe_route_topk_grouped")
+    return idx, w
+
+
+def moe_pack_router_weights(w_router, stream=None):
+    """Router weights [d, E] bf16 in the fused router's layout (uint8 buffer)."""
+    _contig(w_router, torch.bfloat16, "w_router")
+    d, E = w_router.shape
+    packed = torch.empty(lib.moe_router_packed_bytes(d, E), dtype=torch.uint8, device=w_router.device)
+    _check(lib.moe_pack_router_weights(_ptr(w_router), d, E, _ptr(packed), _stream(stream)), "moe_pack_router_weights")
+    return packed
+
+
+def moe_router_topk(x, router_packed, E, k, renormalize=True, stream=None):
+    """Fused router: topk_idx [T,k], topk_w [T,k] of logits x @ w_router, never materialised."""
+    _contig(x, torch.bfloat16, "x")
+    T, d = x.shape
+    idx = torch.empty(T, k, dtype=torch.int32, device=x.device)
+    w = torch.empty(T, k, dtype=torch.float32, device=x.device)
+    ws = torch.empty(256, dtype=torch.uint8, device=x.device)
+    _check(lib.moe_router_topk(_ptr(x), _ptr(router_packed), T, d, E, k, int(bool(renormalize)), _ptr(idx), _ptr(w),
+                               _ptr(ws), ws.numel(), _stream(stream)), "moe_router_topk")
     return idx, w
 
 
@@ -252,6 +277,21 @@ def moe_forward(x, logits, packed, E, k, f, renormalize=True, workspace=None, ou
 
 
 FORWARD_STAGES = ("route", "index", "permute", "gate_up", "down", "combine")
+
+
+def moe_forward_routed(x, router_packed, packed, E, k, f, renormalize=True, workspace=None, out=None, stream=None):
+    """out [T, d] of the whole layer from the tokens and the packed router weights."""
+    _contig(x, torch.bfloat16, "x")
+    T, d = x.shape
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(lib.moe_forward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    _check(lib.moe_forward_routed(_ptr(x), _ptr(router_packed), _ptr(packed), T, d, E, k, f, int(bool(renormalize)),
+                                  _ptr(out), None, None, _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_forward_routed")
+    return out
 
 
 def moe_forward_timed(x, logits, packed, E, k, f, workspace, out, events, renormalize=True, stream=None):

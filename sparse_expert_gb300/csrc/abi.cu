@@ -33,6 +33,8 @@ moe_status_t cuda_fail(cudaError_t e, const char* where) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+constexpr int32_t kRouterMaxExperts = 512;  // the fused router's accumulator fits TMEM's 512 columns
+
 moe_status_t check_routing(int64_t T, int32_t E, int32_t k) {
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
   if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
@@ -204,6 +206,45 @@ moe_status_t moe_route_topk_grouped(const float* logits, int64_t T, int32_t E, i
   return MOE_OK;
 }
 
+size_t moe_router_packed_bytes(int32_t d, int32_t E) {
+  if (d < 1 || E < 1) return 0;
+  return static_cast<size_t>(d) * router_e_pad(E) * 2;
+}
+
+moe_status_t moe_pack_router_weights(const void* w_router, int32_t d, int32_t E, void* packed, moe_stream_t stream) {
+  if (E < 1 || E > kRouterMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "the fused router takes 1 <= E <= 512");
+  if (d < 64 || d > 65536 || d % 64 != 0) return fail(MOE_ERR_UNSUPPORTED, "d must be a multiple of 64 in [64, 65536]");
+  if (!w_router || !packed) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  DeviceInfo dev;
+  moe_status_t s = device_info(&dev);
+  if (s != MOE_OK) return s;
+  MOE_CUDA(launch_pack_router(w_router, d, E, packed, static_cast<cudaStream_t>(stream)), "router pack launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_router_topk(const void* x, const void* router_packed, int64_t T, int32_t d, int32_t E, int32_t k,
+                             int32_t renormalize, int32_t* topk_idx, float* topk_w, void* workspace,
+                             size_t workspace_bytes, moe_stream_t stream) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if (E > kRouterMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "the fused router takes E <= 512");
+  if (d < 64 || d > 65536 || d % 64 != 0) return fail(MOE_ERR_UNSUPPORTED, "d must be a multiple of 64 in [64, 65536]");
+  if (!router_packed) return fail(MOE_ERR_INVALID_ARG, "NULL router weights");
+  if (T > 0 && (!x || !topk_idx || !topk_w)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(x, 16) || !aligned(router_packed, 16)) return fail(MOE_ERR_INVALID_ARG, "x and weights must be 16-byte aligned");
+  if (!workspace || workspace_bytes < sizeof(WsHeader) || !aligned(workspace, kAlign))
+    return fail(MOE_ERR_WORKSPACE, "router workspace needs 256 bytes, 256-byte aligned");
+  if (T == 0) return MOE_OK;
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st), "workspace clear");
+  MOE_CUDA(launch_router_topk(x, router_packed, T, d, E, k, renormalize, topk_idx, topk_w, nullptr,
+                              &static_cast<WsHeader*>(workspace)->status, st),
+           "router launch");
+  return MOE_OK;
+}
+
 size_t moe_dispatch_workspace_bytes(int64_t T, int32_t E, int32_t k) {
   if (T < 0 || E < 1 || k < 1) return 0;
   const int64_t P = T * k;
@@ -350,17 +391,20 @@ moe_status_t moe_forward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int3
 
 namespace {
 
-moe_status_t forward_impl(const void* x, const float* logits, const void* packed, int64_t T, int32_t d, int32_t E,
-                          int32_t k, int32_t f, int32_t renormalize, void* out, int32_t* topk_idx_out,
-                          float* topk_w_out, void* workspace, size_t workspace_bytes, moe_stream_t stream,
-                          void* const* events) {
+// Stage 1 reads `logits` when router_packed is null, else computes the
+// logits from x and the packed router weights inside the route kernel.
+moe_status_t forward_impl(const void* x, const float* logits, const void* router_packed, const void* packed,
+                          int64_t T, int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out,
+                          int32_t* topk_idx_out, float* topk_w_out, void* workspace, size_t workspace_bytes,
+                          moe_stream_t stream, void* const* events) {
   moe_status_t s = check_routing(T, E, k);
   if (s != MOE_OK) return s;
   if ((s = check_gemm_dims(d, f)) != MOE_OK) return s;
   const int64_t P = T * k;
   if ((s = check_tile_space(P, E, d, f)) != MOE_OK) return s;
   if (!packed) return fail(MOE_ERR_INVALID_ARG, "NULL packed weights");
-  if (T > 0 && (!x || !logits || !out)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T > 0 && (!x || (!logits && !router_packed) || !out)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (router_packed && E > kRouterMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "the fused router takes E <= 512");
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(packed, 16))
     return fail(MOE_ERR_INVALID_ARG, "x, out and packed must be 16-byte aligned");
   const ForwardLayout L = forward_layout(T, E, k, d, f);
@@ -393,8 +437,14 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* packed
     return MOE_OK;
   }
   // stage 1 (+ token counts)
-  MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, counts, dev.num_sms, st),
-           "route launch");
+  if (router_packed) {
+    MOE_CUDA(launch_router_topk(x, router_packed, T, d, E, k, renormalize, topk_idx, topk_w, counts, &hdr->status,
+                                st),
+             "router launch");
+  } else {
+    MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, counts, dev.num_sms, st),
+             "route launch");
+  }
   MOE_CUDA(mark(1), "event record");
   // stages 2-3: offsets, index maps and the gate of every row
   DispatchState dstate = dispatch_state_split(ws, L.dispatch_state, P, E);
@@ -425,8 +475,17 @@ extern "C" {
 moe_status_t moe_forward(const void* x, const float* logits, const void* packed, int64_t T, int32_t d, int32_t E,
                          int32_t k, int32_t f, int32_t renormalize, void* out, int32_t* topk_idx_out,
                          float* topk_w_out, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-  return forward_impl(x, logits, packed, T, d, E, k, f, renormalize, out, topk_idx_out, topk_w_out, workspace,
-                      workspace_bytes, stream, nullptr);
+  return forward_impl(x, logits, nullptr, packed, T, d, E, k, f, renormalize, out, topk_idx_out, topk_w_out,
+                      workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status_t moe_forward_routed(const void* x, const void* router_packed, const void* packed, int64_t T, int32_t d,
+                                int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out,
+                                int32_t* topk_idx_out, float* topk_w_out, void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream) {
+  if (!router_packed) return fail(MOE_ERR_INVALID_ARG, "NULL router weights");
+  return forward_impl(x, nullptr, router_packed, packed, T, d, E, k, f, renormalize, out, topk_idx_out, topk_w_out,
+                      workspace, workspace_bytes, stream, nullptr);
 }
 
 moe_status_t moe_forward_timed(const void* x, const float* logits, const void* packed, int64_t T, int32_t d,
@@ -435,7 +494,7 @@ moe_status_t moe_forward_timed(const void* x, const float* logits, const void* p
   if (!events) return fail(MOE_ERR_INVALID_ARG, "NULL events");
   for (int i = 0; i <= MOE_FORWARD_STAGES; ++i)
     if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "NULL event handle");
-  return forward_impl(x, logits, packed, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
+  return forward_impl(x, logits, nullptr, packed, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
                       workspace_bytes, stream, events);
 }
 

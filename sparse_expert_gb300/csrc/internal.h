@@ -15,6 +15,14 @@ inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int n_groups, int renormalize,
                               int32_t* topk_idx, float* topk_w, int32_t* counts, int num_sms, cudaStream_t stream);
 
+// ---- stage 1 with the router linear layer fused
+int router_e_pad(int E);  // E rounded up to a multiple of 128
+size_t router_smem_bytes(int E);
+cudaError_t launch_pack_router(const void* w_router, int d, int E, void* packed, cudaStream_t stream);
+cudaError_t launch_router_topk(const void* x, const void* w_packed, int64_t T, int d, int E, int k, int renormalize,
+                               int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* status,
+                               cudaStream_t stream);
+
 // ---- stages 2-3
 constexpr int kDispatchThreads = 256;
 constexpr int kDispatchPairsPerThread = 8;

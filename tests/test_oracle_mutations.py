@@ -105,3 +105,12 @@ def test_grouped_route_ignoring_groups_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "route_topk_grouped", lambda l, k, G, renormalize=True: real(l, k, renormalize))
     _fails(pins.test_grouped_route_balances_the_groups)
     _fails(pins.test_grouped_route_golden, load_golden)
+
+
+def test_router_with_transposed_weights_is_caught(monkeypatch):
+    import oracle
+    real = om.router_topk
+    monkeypatch.setattr(oracle, "router_topk", lambda x, w, k, renormalize=True: real(x, np.asarray(w)[::-1], k,
+                                                                                       renormalize))
+    _fails(pins.test_router_logits_match_per_token_dot_products)
+    _fails(pins.test_router_with_one_hot_tokens_selects_router_rows)

@@ -361,3 +361,45 @@ def test_grouped_route_golden(golden):
                                            case["renormalize"])
         assert list(idx[0]) == case["idx"]
         np.testing.assert_allclose(w[0], case["w"], rtol=1e-15)
+
+
+# -------------------------------------------------------- router + top-k
+def test_router_logits_match_per_token_dot_products():
+    """Brute force: each logit is the plain dot product of the token row and
+    the expert's router column."""
+    rng = _rng(31)
+    T, d, E = 7, 12, 5
+    x = _bf16_values(rng.standard_normal((T, d)))
+    wr = _bf16_values(rng.standard_normal((d, E)))
+    _, _, logits = oracle.router_topk(x, wr, 2)
+    for t in range(T):
+        for e in range(E):
+            assert logits[t, e] == pytest.approx(sum(float(x[t, i]) * float(wr[i, e]) for i in range(d)), rel=1e-13)
+
+
+def test_router_with_one_hot_tokens_selects_router_rows():
+    """x = e_i makes the logits the i-th row of the router matrix (closed form)."""
+    rng = _rng(33)
+    d, E, k = 6, 9, 3
+    wr = rng.standard_normal((d, E))
+    idx, w, logits = oracle.router_topk(np.eye(d), wr, k)
+    assert np.array_equal(logits, wr)
+    for i in range(d):
+        assert list(idx[i]) == _brute_topk(list(wr[i]), k)
+        np.testing.assert_allclose(w[i], scipy.special.softmax(wr[i, idx[i]]), rtol=1e-14)
+
+
+def test_router_topk_equals_routing_of_its_logits():
+    rng = _rng(35)
+    x = _bf16_values(rng.standard_normal((50, 32)))
+    wr = _bf16_values(rng.standard_normal((32, 16)) / np.sqrt(32))
+    for renorm in (True, False):
+        idx, w, logits = oracle.router_topk(x, wr, 4, renorm)
+        # logits here are exactly representable in fp32 for the ranking check
+        order = np.argsort(-logits, axis=1, kind="stable")[:, :4]
+        assert np.array_equal(idx, order)
+        ref = scipy.special.softmax(logits, axis=1)
+        ref = np.take_along_axis(ref, order, axis=1)
+        if renorm:
+            ref = ref / ref.sum(axis=1, keepdims=True)
+        np.testing.assert_allclose(w, ref, rtol=1e-13)

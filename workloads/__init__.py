@@ -142,6 +142,16 @@ def generate(cfg, seed: int = 0, device="cpu", weights: bool = True, x: bool = T
     return out
 
 
+def generate_router(cfg, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Router weights w_router [d, E] bf16, N(0, 1)/sqrt(d), from their own
+    generator (seeded with seed + 1,000,003) so they do not shift the draws
+    of ``generate``.  With x ~ N(0, 1) the router logits are about N(0, 1),
+    like the workloads' logits."""
+    cfg = get(cfg)
+    g = _gen(seed + 1_000_003, torch.device(device))
+    return (torch.randn(cfg.d, cfg.E, generator=g, device=device) / math.sqrt(cfg.d)).to(torch.bfloat16)
+
+
 def generate_logits(cfg, seed: int = 0, device="cpu") -> torch.Tensor:
     """Router logits alone, with the same values ``generate`` returns."""
     return generate(cfg, seed, device, weights=False, x=False)["logits"]
