@@ -306,6 +306,37 @@ def gpu_arm(args):
         e2e = {"value": round(job_throughput(T * args.steps, world, e2e_s), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": x_h.numel() * 2 + l_h.numel() * 4, "d2h_bytes_per_step": o_h.numel() * 2}
 
+    # the layer from the tokens: fused router (router GEMM + top-k) instead of given logits
+    routed = None
+    if not args.no_routed:
+        wr = workloads.generate_router(cfg, seed=args.seed + rank, device="cuda")
+        rp = moe.moe_pack_router_weights(wr)
+        for _ in range(args.warmup):
+            moe.moe_router_topk(x, rp, E, k, cfg.renormalize)
+        r_ms = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            moe.moe_router_topk(x, rp, E, k, cfg.renormalize)
+            b.record(stream)
+            r_ms.append((a, b))
+        for _ in range(args.warmup):
+            moe.moe_forward_routed(x, rp, packed, E, k, f, cfg.renormalize, workspace=ws, out=out)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            moe.moe_forward_routed(x, rp, packed, E, k, f, cfg.renormalize, workspace=ws, out=out)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        router_ms = statistics.mean(a.elapsed_time(b) for a, b in r_ms)
+        routed_s = max_over_ranks(t0.elapsed_time(t1) / 1e3, world, device="cuda")
+        router_tf = 2.0 * T * d * E / (router_ms * 1e-3) / 1e12
+        routed = {"value": round(job_throughput(T * args.steps, world, routed_s), 1), "unit": "tokens/s",
+                  "ms_per_step": round(routed_s * 1e3 / args.steps, 4),
+                  "router_topk_ms": round(router_ms, 4), "router_tflops": round(router_tf, 1),
+                  "note": "whole layer from x and router weights: fused router GEMM + top-k replaces the given logits"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = min(args.cpu_sample_tokens, T)
@@ -329,7 +360,7 @@ def gpu_arm(args):
             "grouped_gemm": {"tflops": round(gemm_tflops, 2), "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
                              "weight_bytes_read": weight_bytes_read(cfg, counts)},
             "permute_gbs": stages["permute"]["gbs"],
-            "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed,
             "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -380,6 +411,7 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-routed", action="store_true", help="skip the fused-router forward measurement")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--ref-sample-tokens", type=int, default=4)
     args = ap.parse_args(argv)
