@@ -114,3 +114,27 @@ def test_router_with_transposed_weights_is_caught(monkeypatch):
                                                                                        renormalize))
     _fails(pins.test_router_logits_match_per_token_dot_products)
     _fails(pins.test_router_with_one_hot_tokens_selects_router_rows)
+
+
+def test_fp8_round_half_up_is_caught(monkeypatch):
+    from oracle import fp8_oracle as f8
+    from tests import test_fp8_oracle as fp8_pins
+    real = f8.e4m3_round
+
+    def half_up(x):
+        x = np.asarray(x, dtype=np.float32).astype(np.float64)
+        a = np.abs(x)
+        _, e2 = np.frexp(a)
+        q = np.exp2(np.maximum(e2 - 1, -6) - 3.0)
+        r = np.minimum(np.floor(a / q + 0.5) * q, 448.0)
+        return np.where(np.signbit(x), -r, r).astype(np.float32)
+    monkeypatch.setattr(f8, "e4m3_round", half_up)
+    _fails(fp8_pins.test_rounding_matches_torch_including_every_tie)
+    monkeypatch.setattr(f8, "e4m3_round", real)
+
+
+def test_fp8_wrong_scale_range_is_caught(monkeypatch):
+    from oracle import fp8_oracle as f8
+    from tests import test_fp8_oracle as fp8_pins
+    monkeypatch.setattr(f8, "E4M3_MAX", 240.0)
+    _fails(fp8_pins.test_blockwise_scale_puts_the_block_maximum_at_448)
