@@ -234,6 +234,24 @@ MOE_API moe_status_t moe_pack_weights(const void* w_gate, const void* w_up, cons
                               moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Blockwise FP8 expert weights ("Training a 1T-Params MoE on EU public
+ * infrastructure", FP8 expert weight all-gather): the n values of a weight
+ * tensor are cut into blocks of 128 consecutive values; each block gets one
+ * fp32 scale = amax / 448 (1 for an all-zero block) and its values become
+ * E4M3 codes of w / scale (fp32 division, round to nearest even, saturating
+ * at +-448).  Dequantisation gives bf16(E4M3 value * scale), the weights
+ * the expert computation then uses (pack them with moe_pack_weights); per
+ * value the error is at most ~6% of its block's maximum.
+ *   w [n] bf16; codes [n] uint8 (E4M3 bit patterns); scales [n/128] fp32.
+ * n must be a multiple of 128.  Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_NO_DEVICE, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_quantize_fp8_blockwise(const void* w, int64_t n, uint8_t* codes, float* scales,
+                                        moe_stream_t stream);
+MOE_API moe_status_t moe_dequantize_fp8_blockwise(const uint8_t* codes, const float* scales, int64_t n,
+                                          void* w_out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Stage 4, expert computation — the grouped gate/up GEMM with
  * Silu(gate)*up and the grouped down GEMM (Algorithm 1, stage 4), over the
  * expert groups given by offsets, on the tensor cores (bf16 operands, fp32

@@ -22,6 +22,8 @@ from ._lib import (  # noqa: F401
     FORWARD_STAGES,
     moe_forward_workspace_bytes,
     moe_grouped_swiglu,
+    moe_quantize_fp8_blockwise,
+    moe_dequantize_fp8_blockwise,
     moe_pack_weights,
     moe_packed_weight_bytes,
     moe_permute,

@@ -60,6 +60,8 @@ SIGNATURES = {
     "moe_permute": (_S, [_P, _I64, _I32, _P, _I32, _P, _P]),
     "moe_packed_weight_bytes": (_SZ, [_I32, _I32, _I32]),
     "moe_pack_weights": (_S, [_P, _P, _P, _I32, _I32, _I32, _P, _P]),
+    "moe_quantize_fp8_blockwise": (_S, [_P, _I64, _P, _P, _P]),
+    "moe_dequantize_fp8_blockwise": (_S, [_P, _P, _I64, _P, _P]),
     "moe_grouped_swiglu_workspace_bytes": (_SZ, []),
     "moe_grouped_swiglu": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_S, [_P, _P, _P, _I64, _I32, _I32, _P, _P]),
@@ -215,6 +217,28 @@ def moe_pack_weights(w_gate, w_up, w_down, stream=None):
     _check(lib.moe_pack_weights(_ptr(w_gate), _ptr(w_up), _ptr(w_down), E, d, f, _ptr(packed), _stream(stream)),
            "moe_pack_weights")
     return packed
+
+
+def moe_quantize_fp8_blockwise(w, stream=None):
+    """(codes uint8 [n], scales fp32 [n/128]) of a bf16 tensor, blocks of 128 in memory order."""
+    _contig(w, torch.bfloat16, "w")
+    n = w.numel()
+    codes = torch.empty(n, dtype=torch.uint8, device=w.device)
+    scales = torch.empty(n // 128, dtype=torch.float32, device=w.device)
+    _check(lib.moe_quantize_fp8_blockwise(_ptr(w), n, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_quantize_fp8_blockwise")
+    return codes, scales
+
+
+def moe_dequantize_fp8_blockwise(codes, scales, shape=None, stream=None):
+    """bf16 weights (of ``shape``, flat by default) from codes and per-block scales."""
+    _contig(codes, torch.uint8, "codes")
+    _contig(scales, torch.float32, "scales")
+    n = codes.numel()
+    out = torch.empty(n, dtype=torch.bfloat16, device=codes.device)
+    _check(lib.moe_dequantize_fp8_blockwise(_ptr(codes), _ptr(scales), n, _ptr(out), _stream(stream)),
+           "moe_dequantize_fp8_blockwise")
+    return out if shape is None else out.view(shape)
 
 
 def moe_grouped_swiglu(x_perm, offsets, E, f, packed, row_scale=None, workspace=None, stream=None):

@@ -314,6 +314,33 @@ moe_status_t moe_pack_weights(const void* w_gate, const void* w_up, const void* 
   return MOE_OK;
 }
 
+moe_status_t moe_quantize_fp8_blockwise(const void* w, int64_t n, uint8_t* codes, float* scales, moe_stream_t stream) {
+  if (n < 0 || n % 128 != 0) return fail(MOE_ERR_INVALID_ARG, "n must be a non-negative multiple of 128");
+  if (n > 0 && (!w || !codes || !scales)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(w, 8) || !aligned(codes, 4)) return fail(MOE_ERR_INVALID_ARG, "w must be 8-byte and codes 4-byte aligned");
+  if (n == 0) return MOE_OK;
+  DeviceInfo dev;
+  moe_status_t s = device_info(&dev);
+  if (s != MOE_OK) return s;
+  MOE_CUDA(launch_quantize_fp8(w, n, codes, scales, dev.num_sms, static_cast<cudaStream_t>(stream)),
+           "fp8 quantize launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_dequantize_fp8_blockwise(const uint8_t* codes, const float* scales, int64_t n, void* w_out,
+                                          moe_stream_t stream) {
+  if (n < 0 || n % 128 != 0) return fail(MOE_ERR_INVALID_ARG, "n must be a non-negative multiple of 128");
+  if (n > 0 && (!w_out || !codes || !scales)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(w_out, 8) || !aligned(codes, 4)) return fail(MOE_ERR_INVALID_ARG, "w_out must be 8-byte and codes 4-byte aligned");
+  if (n == 0) return MOE_OK;
+  DeviceInfo dev;
+  moe_status_t s = device_info(&dev);
+  if (s != MOE_OK) return s;
+  MOE_CUDA(launch_dequantize_fp8(codes, scales, n, w_out, dev.num_sms, static_cast<cudaStream_t>(stream)),
+           "fp8 dequantize launch");
+  return MOE_OK;
+}
+
 size_t moe_grouped_swiglu_workspace_bytes(void) { return sizeof(WsHeader); }
 
 moe_status_t moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, int64_t P, int32_t E, int32_t d,

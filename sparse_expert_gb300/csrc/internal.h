@@ -23,6 +23,12 @@ cudaError_t launch_router_topk(const void* x, const void* w_packed, int64_t T, i
                                int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* status,
                                cudaStream_t stream);
 
+// ---- blockwise FP8 (E4M3) weights
+cudaError_t launch_quantize_fp8(const void* w, int64_t n, uint8_t* codes, float* scales, int num_sms,
+                                cudaStream_t stream);
+cudaError_t launch_dequantize_fp8(const uint8_t* codes, const float* scales, int64_t n, void* out, int num_sms,
+                                  cudaStream_t stream);
+
 // ---- stages 2-3
 constexpr int kDispatchThreads = 256;
 constexpr int kDispatchPairsPerThread = 8;
