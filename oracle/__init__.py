@@ -14,6 +14,8 @@ from .moe_oracle import (  # noqa: F401
     silu,
     expert_mlp,
     combine,
+    combine_backward,
+    route_backward,
     moe_forward,
     moe_forward_tokens,
 )

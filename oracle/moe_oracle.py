@@ -221,6 +221,59 @@ def combine(y, dest_row, w):
     return out
 
 
+# ------------------------------------------------------------- backward
+def combine_backward(dout, mlp_out, dest_row, w):
+    """Output reduction, backward (Algorithm 1, stage 5, backward function):
+    for every routed pair p = (t, j) with row r = dest_row[p],
+      mlp_out_grad[r] = w[t, j] * output_grad[t]
+      weights_grad[t, j] = <mlp_out[r], output_grad[t]>
+    ``mlp_out`` is the expert output before the gate.  Returns
+    (mlp_out_grad [P, d], weights_grad [T, k]) in fp64.
+    """
+    dout = np.asarray(dout, dtype=np.float64)
+    y = np.asarray(mlp_out, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T, k = w.shape
+    rows = np.asarray(dest_row, dtype=np.int64).reshape(T, k)
+    dy = np.zeros_like(y)
+    dw = np.zeros((T, k))
+    for j in range(k):
+        dy[rows[:, j]] = w[:, j:j + 1] * dout
+        dw[:, j] = np.einsum("td,td->t", y[rows[:, j]], dout)
+    return dy, dw
+
+
+def route_backward(logits, idx, dw, renormalize=True):
+    """Gradient of the router logits from the gradient of the gates.
+
+    With the selection fixed, w_j = exp(l_{e_j}) / Z where Z sums exp(l)
+    over all E experts, or over the k selected when renormalised, so
+    dl_e = [e selected as slot j] w_j dw_j - q_e * sum_j w_j dw_j, with
+    q_e = exp(l_e) / Z on the normalisation set and 0 elsewhere.
+    Returns d_logits [T, E] in fp64.
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    idx = np.asarray(idx, dtype=np.int64)
+    dw = np.asarray(dw, dtype=np.float64)
+    T, E = l.shape
+    out = np.zeros((T, E))
+    for t in range(T):
+        sel = idx[t]
+        if renormalize:
+            z = np.exp(l[t, sel] - l[t, sel].max())
+            wt = z / z.sum()
+            q = np.zeros(E)
+            q[sel] = wt
+        else:
+            q = np.exp(l[t] - l[t].max())
+            q = q / q.sum()
+            wt = q[sel]
+        s = np.dot(wt, dw[t])
+        out[t] = -q * s
+        out[t, sel] += wt * dw[t]
+    return out
+
+
 # ------------------------------------------------------------ whole layer
 def moe_forward(x, logits, w_gate, w_up, w_down, k, renormalize=True):
     """Every stage of the layer forward, in order, with all intermediates."""

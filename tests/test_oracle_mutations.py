@@ -8,6 +8,7 @@ order or sign, and a transposed operand.
 import numpy as np
 import pytest
 
+import oracle
 import oracle.moe_oracle as om
 from tests import test_oracle_pins as pins
 from tests.conftest import load_golden
@@ -138,3 +139,36 @@ def test_fp8_wrong_scale_range_is_caught(monkeypatch):
     from tests import test_fp8_oracle as fp8_pins
     monkeypatch.setattr(f8, "E4M3_MAX", 240.0)
     _fails(fp8_pins.test_blockwise_scale_puts_the_block_maximum_at_448)
+
+
+def test_combine_backward_without_gate_is_caught(monkeypatch):
+    real = om.combine_backward
+
+    def no_gate(dout, mlp_out, dest_row, w):
+        dy, dw = real(dout, mlp_out, dest_row, np.ones_like(np.asarray(w, dtype=np.float64)))
+        return dy, dw
+    monkeypatch.setattr(oracle, "combine_backward", no_gate)
+    _fails(pins.test_combine_backward_matches_finite_differences)
+    _fails(pins.test_combine_backward_golden_scalar)
+
+
+def test_route_backward_wrong_sign_is_caught(monkeypatch):
+    real = om.route_backward
+
+    def flipped(logits, idx, dw, renormalize=True):
+        g = real(logits, idx, dw, renormalize)
+        base = real(logits, idx, np.zeros_like(np.asarray(dw, dtype=np.float64)), renormalize)
+        return 2 * base - g          # negates the whole gradient
+    monkeypatch.setattr(oracle, "route_backward", flipped)
+    _fails(pins.test_route_backward_matches_finite_differences, True)
+    _fails(pins.test_route_backward_matches_finite_differences, False)
+
+
+def test_route_backward_softmax_over_wrong_set_is_caught(monkeypatch):
+    real = om.route_backward
+
+    def other_set(logits, idx, dw, renormalize=True):
+        return real(logits, idx, dw, not renormalize)
+    monkeypatch.setattr(oracle, "route_backward", other_set)
+    _fails(pins.test_route_backward_matches_finite_differences, True)
+    _fails(pins.test_route_backward_matches_finite_differences, False)

@@ -403,3 +403,60 @@ def test_router_topk_equals_routing_of_its_logits():
         if renorm:
             ref = ref / ref.sum(axis=1, keepdims=True)
         np.testing.assert_allclose(w, ref, rtol=1e-13)
+
+
+# --------------------------------------------------------------- backward
+def _finite_diff(fn, x, eps=1e-6):
+    """Central differences of a scalar function of an fp64 array."""
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        xp = x.copy(); xp[i] += eps
+        xm = x.copy(); xm[i] -= eps
+        g[i] = (fn(xp) - fn(xm)) / (2 * eps)
+    return g
+
+
+def test_combine_backward_matches_finite_differences():
+    """The output reduction is linear in the expert outputs and the gates;
+    its backward must equal the numerical derivative of
+    L = <G, combine(y, dest_row, w)> for a fixed output gradient G."""
+    rng = _rng(41)
+    T, d, E, k = 6, 5, 4, 2
+    idx, w = oracle.route_topk(_random_logits(rng, T, E), k)
+    _, _, _, dst = oracle.dispatch(idx, E)
+    y = rng.standard_normal((T * k, d))
+    G = rng.standard_normal((T, d))
+    dy, dw = oracle.combine_backward(G, y, dst, w)
+    np.testing.assert_allclose(dy, _finite_diff(lambda yy: np.sum(G * oracle.combine(yy, dst, w)), y), atol=1e-8)
+    np.testing.assert_allclose(dw, _finite_diff(lambda ww: np.sum(G * oracle.combine(y, dst, ww)), w), atol=1e-8)
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_backward_matches_finite_differences(renorm):
+    """With the selection held fixed, the gate gradient w.r.t. the logits is
+    the derivative of the oracle's own gates."""
+    rng = _rng(43)
+    T, E, k = 5, 7, 3
+    l = rng.standard_normal((T, E))
+    idx, _ = oracle.route_topk(l.astype(np.float32), k, renorm)
+    dw = rng.standard_normal((T, k))
+
+    def gates(ll):
+        if renorm:
+            z = np.exp(np.take_along_axis(ll, idx.astype(np.int64), axis=1))
+            return z / z.sum(axis=1, keepdims=True)
+        p = oracle.softmax_rows(ll)
+        return np.take_along_axis(p, idx.astype(np.int64), axis=1)
+    ref = _finite_diff(lambda ll: np.sum(dw * gates(ll)), l)
+    np.testing.assert_allclose(oracle.route_backward(l, idx, dw, renorm), ref, atol=1e-8)
+
+
+def test_combine_backward_golden_scalar():
+    """One token, two slots, d = 1, worked by hand: rows 0 and 1, gates
+    0.25 and 0.75, expert outputs 2 and -4, output gradient 3:
+    mlp_out_grad = (0.75, 2.25) and weights_grad = (6, -12)."""
+    dy, dw = oracle.combine_backward(np.array([[3.0]]), np.array([[2.0], [-4.0]]), np.array([0, 1]),
+                                     np.array([[0.25, 0.75]]))
+    assert dy.ravel().tolist() == [0.75, 2.25] and dw.ravel().tolist() == [6.0, -12.0]
