@@ -290,6 +290,36 @@ MOE_API moe_status_t moe_combine(const void* y, const int32_t* dest_row, const f
                          int64_t T, int32_t k, int32_t d, void* out, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stage 5 backward — output reduction, backward (Algorithm 1, stage 5,
+ * backward function): for every routed pair (t, j) at row
+ * r = dest_row[t*k + j],
+ *   d_mlp_out[r, :] = bf16( topk_w[t, j] * dout[t, :] )
+ *   d_topk_w[t, j]  = sum_h mlp_out[r, h] * dout[t, h]   (fp32)
+ *   dout [T, d] bf16; mlp_out [T*k, d] bf16, the expert outputs BEFORE the
+ *   gate (moe_grouped_swiglu with row_scale = NULL); dest_row [T*k];
+ *   topk_w [T, k] fp32; d_mlp_out [T*k, d] bf16 out; d_topk_w [T, k] out.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_combine_backward(const void* dout, const void* mlp_out, const int32_t* dest_row,
+                                  const float* topk_w, int64_t T, int32_t k, int32_t d,
+                                  void* d_mlp_out, float* d_topk_w, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 1 backward — gradient of the router logits from the gradient of
+ * the gates, with the top-k selection held fixed (Softmax and TopK of
+ * Algorithm 1, stage 1, differentiated): gates w_j = exp(l_{e_j}) / Z with
+ * Z summed over all E experts, or over the k selected when renormalize != 0,
+ * so d_logits[t, e] = [e is slot j] w_j dw_j - q_e * sum_j w_j dw_j with
+ * q_e = exp(l_e) / Z on the normalisation set (0 elsewhere).
+ *   logits [T, E] fp32 (as given to moe_route_topk); topk_idx [T, k];
+ *   d_topk_w [T, k] fp32; d_logits [T, E] fp32 out (every entry written).
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_route_backward(const float* logits, const int32_t* topk_idx, const float* d_topk_w,
+                                int64_t T, int32_t E, int32_t k, int32_t renormalize,
+                                float* d_logits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The whole layer forward (Algorithm 1, stages 1-5) on one stream, with no
  * host synchronisation: route + histogram, look-back index pass, permute,
  * gate/up GEMM with SwiGLU, down GEMM scaled by each row's gate, combine.

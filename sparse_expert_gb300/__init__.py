@@ -9,6 +9,8 @@ from ._lib import (  # noqa: F401
     abi_version,
     forward_intermediates,
     moe_combine,
+    moe_combine_backward,
+    moe_route_backward,
     moe_dispatch_scan,
     moe_dispatch_scan_noalloc,
     moe_dispatch_workspace_bytes,

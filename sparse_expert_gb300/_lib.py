@@ -65,6 +65,8 @@ SIGNATURES = {
     "moe_grouped_swiglu_workspace_bytes": (_SZ, []),
     "moe_grouped_swiglu": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_S, [_P, _P, _P, _I64, _I32, _I32, _P, _P]),
+    "moe_combine_backward": (_S, [_P, _P, _P, _P, _I64, _I32, _I32, _P, _P, _P]),
+    "moe_route_backward": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _P, _P]),
     "moe_forward_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
     "moe_forward_layout": (_S, [_I64, _I32, _I32, _I32, _I32, ctypes.POINTER(ForwardLayout)]),
     "moe_forward": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -269,6 +271,34 @@ def moe_combine(y, dest_row, T, k, topk_w=None, stream=None):
     out = torch.empty(T, d, dtype=torch.bfloat16, device=y.device)
     _check(lib.moe_combine(_ptr(y), _ptr(dest_row), _ptr(topk_w), T, k, d, _ptr(out), _stream(stream)),
            "moe_combine")
+    return out
+
+
+def moe_combine_backward(dout, mlp_out, dest_row, topk_w, stream=None):
+    """(d_mlp_out [T*k, d] bf16, d_topk_w [T, k] fp32) of the output reduction."""
+    _contig(dout, torch.bfloat16, "dout")
+    _contig(mlp_out, torch.bfloat16, "mlp_out")
+    _contig(dest_row, torch.int32, "dest_row")
+    _contig(topk_w, torch.float32, "topk_w")
+    T, d = dout.shape
+    k = topk_w.shape[1]
+    dy = torch.empty(T * k, d, dtype=torch.bfloat16, device=dout.device)
+    dw = torch.empty(T, k, dtype=torch.float32, device=dout.device)
+    _check(lib.moe_combine_backward(_ptr(dout), _ptr(mlp_out), _ptr(dest_row), _ptr(topk_w), T, k, d, _ptr(dy),
+                                    _ptr(dw), _stream(stream)), "moe_combine_backward")
+    return dy, dw
+
+
+def moe_route_backward(logits, topk_idx, d_topk_w, renormalize=True, stream=None):
+    """d_logits [T, E] fp32 from the gates' gradient (selection held fixed)."""
+    _contig(logits, torch.float32, "logits")
+    _contig(topk_idx, torch.int32, "topk_idx")
+    _contig(d_topk_w, torch.float32, "d_topk_w")
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    out = torch.empty(T, E, dtype=torch.float32, device=logits.device)
+    _check(lib.moe_route_backward(_ptr(logits), _ptr(topk_idx), _ptr(d_topk_w), T, E, k, int(bool(renormalize)),
+                                  _ptr(out), _stream(stream)), "moe_route_backward")
     return out
 
 

@@ -388,6 +388,40 @@ moe_status_t moe_combine(const void* y, const int32_t* dest_row, const float* to
   return MOE_OK;
 }
 
+moe_status_t moe_combine_backward(const void* dout, const void* mlp_out, const int32_t* dest_row, const float* topk_w,
+                                  int64_t T, int32_t k, int32_t d, void* d_mlp_out, float* d_topk_w,
+                                  moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > MOE_MAX_TOPK) return fail(MOE_ERR_INVALID_ARG, "bad T or k");
+  if (T * static_cast<int64_t>(k) >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  moe_status_t s = check_row(d, "d");
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!dout || !mlp_out || !dest_row || !topk_w || !d_mlp_out || !d_topk_w)
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(dout, 16) || !aligned(mlp_out, 16) || !aligned(d_mlp_out, 16))
+    return fail(MOE_ERR_INVALID_ARG, "dout, mlp_out and d_mlp_out must be 16-byte aligned");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  MOE_CUDA(launch_combine_backward(dout, mlp_out, dest_row, topk_w, T, k, d, d_mlp_out, d_topk_w, dev.num_sms,
+                                   static_cast<cudaStream_t>(stream)),
+           "combine backward launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_route_backward(const float* logits, const int32_t* topk_idx, const float* d_topk_w, int64_t T,
+                                int32_t E, int32_t k, int32_t renormalize, float* d_logits, moe_stream_t stream) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_idx || !d_topk_w || !d_logits) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  MOE_CUDA(launch_route_backward(logits, topk_idx, d_topk_w, T, E, k, renormalize, d_logits, dev.num_sms,
+                                 static_cast<cudaStream_t>(stream)),
+           "route backward launch");
+  return MOE_OK;
+}
+
 size_t moe_forward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f) {
   if (T < 0 || E < 1 || k < 1 || d < 1 || f < 1) return 0;
   return forward_layout(T, E, k, d, f).total;

@@ -1,0 +1,155 @@
+// Backward of the routing ends of the layer.
+//
+// combine_backward: "Scalable Pretraining of Large MoE LMs on Aurora Super
+// Computer", §3.1, Algorithm 1, stage 5 (output reduction, backward): for
+// every routed pair (t, j) at row r, mlp_out_grad[r] = w[t, j] *
+// output_grad[t] and weights_grad[t, j] = <mlp_out[r], output_grad[t]>.
+// One warp per token; the k rows are visited in slot order.
+//
+// route_backward: the gates' gradient taken back to the router logits
+// (Algorithm 1, stage 1, Softmax and TopK, with the selection held fixed):
+// dl_e = [e is slot j] w_j dw_j - q_e * sum_j w_j dw_j, q the softmax over
+// all E (or over the k selected when the gates are renormalised).  One warp
+// per token holding the row's logits in registers.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32)
+combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ mlp_out,
+                        const int32_t* __restrict__ dest_row, const float* __restrict__ w, int64_t T, int k, int dvec,
+                        uint4* __restrict__ d_mlp_out, float* __restrict__ d_w) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < T; t += warps_total) {
+    const uint4* g = dout + t * dvec;
+    for (int j = 0; j < k; ++j) {
+      const int64_t row = __ldg(dest_row + t * k + j);
+      const float wj = __ldg(w + t * k + j);
+      const uint4* y = mlp_out + row * dvec;
+      uint4* dy = d_mlp_out + row * dvec;
+      float dot = 0.f;
+      for (int v = lane; v < dvec; v += 32) {
+        const uint4 gv = __ldg(g + v);
+        const uint4 yv = __ldg(y + v);
+        const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&gv);
+        const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yv);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 gf = __bfloat1622float2(gh[i]);
+          const float2 yf = __bfloat1622float2(yh[i]);
+          dot = fmaf(yf.x, gf.x, dot);
+          dot = fmaf(yf.y, gf.y, dot);
+          o[i] = pack_bf16x2(wj * gf.x, wj * gf.y);
+        }
+        dy[v] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
+      if (lane == 0) d_w[t * k + j] = dot;
+    }
+  }
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kWarps * 32)
+route_backward_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx,
+                      const float* __restrict__ d_w, int64_t T, int E, int k, int renormalize,
+                      float* __restrict__ d_logits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < T; t += warps_total) {
+    const float* row = logits + t * E;
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = (lane + 32 * i < E) ? __ldg(row + lane + 32 * i) : -INFINITY;
+    // lane j < k: slot j's expert, logit and gate gradient
+    const int e_j = lane < k ? __ldg(idx + t * k + lane) : 0;
+    const float l_j = lane < k ? __ldg(row + e_j) : -INFINITY;
+    const float dw_j = lane < k ? __ldg(d_w + t * k + lane) : 0.f;
+    // the normalisation set: all E experts, or the k selected
+    float mx = renormalize ? l_j : -INFINITY;
+    if (!renormalize) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) mx = fmaxf(mx, v[i]);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    float z = 0.f;
+    if (renormalize) {
+      z = lane < k ? expf(l_j - mx) : 0.f;
+    } else {
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i < E) z += expf(v[i] - mx);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) z += __shfl_xor_sync(0xffffffffu, z, s);
+    const float inv_z = 1.0f / __shfl_sync(0xffffffffu, z, 0);
+    const float w_j = lane < k ? expf(l_j - mx) * inv_z : 0.f;
+    float s_sum = w_j * dw_j;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) s_sum += __shfl_xor_sync(0xffffffffu, s_sum, s);
+    s_sum = __shfl_sync(0xffffffffu, s_sum, 0);
+    float g[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) g[i] = renormalize ? 0.f : -expf(v[i] - mx) * inv_z * s_sum;
+    // slot j adds w_j dw_j (and, renormalised, its own -q s term) at its expert
+    for (int j = 0; j < k; ++j) {
+      const int e = __shfl_sync(0xffffffffu, e_j, j);
+      const float add = __shfl_sync(0xffffffffu, renormalize ? w_j * (dw_j - s_sum) : w_j * dw_j, j);
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i == e) g[i] += add;
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (lane + 32 * i < E) d_logits[t * E + lane + 32 * i] = g[i];
+  }
+}
+
+int token_grid(int64_t T, int num_sms) {
+  const int64_t want = (T + kWarps - 1) / kWarps;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  return static_cast<int>(want < cap ? want : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_combine_backward(const void* dout, const void* mlp_out, const int32_t* dest_row, const float* w,
+                                    int64_t T, int k, int d, void* d_mlp_out, float* d_w, int num_sms,
+                                    cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  combine_backward_kernel<<<token_grid(T, num_sms), kWarps * 32, 0, stream>>>(
+      static_cast<const uint4*>(dout), static_cast<const uint4*>(mlp_out), dest_row, w, T, k, d / 8,
+      static_cast<uint4*>(d_mlp_out), d_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_backward(const float* logits, const int32_t* idx, const float* d_w, int64_t T, int E, int k,
+                                  int renormalize, float* d_logits, int num_sms, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const int grid = token_grid(T, num_sms);
+  const int nv = (E + 31) / 32;
+#define MOE_RB_CASE(NV)                                                                                           \
+  route_backward_kernel<NV><<<grid, kWarps * 32, 0, stream>>>(logits, idx, d_w, T, E, k, renormalize, d_logits); \
+  break;
+  switch (nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : nv <= 12 ? 12 : nv <= 16 ? 16 : 32) {
+    case 1: MOE_RB_CASE(1)
+    case 2: MOE_RB_CASE(2)
+    case 4: MOE_RB_CASE(4)
+    case 8: MOE_RB_CASE(8)
+    case 12: MOE_RB_CASE(12)
+    case 16: MOE_RB_CASE(16)
+    default: MOE_RB_CASE(32)
+  }
+#undef MOE_RB_CASE
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -23,6 +23,13 @@ cudaError_t launch_router_topk(const void* x, const void* w_packed, int64_t T, i
                                int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* status,
                                cudaStream_t stream);
 
+// ---- backward of stage 5 and of the routing
+cudaError_t launch_combine_backward(const void* dout, const void* mlp_out, const int32_t* dest_row, const float* w,
+                                    int64_t T, int k, int d, void* d_mlp_out, float* d_w, int num_sms,
+                                    cudaStream_t stream);
+cudaError_t launch_route_backward(const float* logits, const int32_t* idx, const float* d_w, int64_t T, int E, int k,
+                                  int renormalize, float* d_logits, int num_sms, cudaStream_t stream);
+
 // ---- blockwise FP8 (E4M3) weights
 cudaError_t launch_quantize_fp8(const void* w, int64_t n, uint8_t* codes, float* scales, int num_sms,
                                 cudaStream_t stream);
