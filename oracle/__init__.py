@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the MoE-layer forward (test infrastructure only).
+"""fp64 CPU oracle for the MoE layer, forward and backward (test infrastructure only).
 
 This package is the checker, not the product.  Only the tests, the smoke
 check of ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` use it.
@@ -12,10 +12,13 @@ from .moe_oracle import (  # noqa: F401
     dispatch,
     permute,
     silu,
+    silu_grad,
     expert_mlp,
+    expert_mlp_backward,
     combine,
     combine_backward,
     route_backward,
     moe_forward,
     moe_forward_tokens,
+    moe_backward,
 )

@@ -206,6 +206,52 @@ def expert_mlp(x_perm, offsets, w_gate, w_up, w_down, experts=None):
     return h, y
 
 
+def silu_grad(z: np.ndarray) -> np.ndarray:
+    """d/dz SiLU(z) = sigmoid(z) * (1 + z * (1 - sigmoid(z)))."""
+    z = np.asarray(z, dtype=np.float64)
+    s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * (1.0 - s))
+
+
+def expert_mlp_backward(x_perm, offsets, w_gate, w_up, w_down, dy):
+    """Backward of the grouped SwiGLU expert MLP (Algorithm 1, stage 4,
+    differentiated), expert by expert on its rows [offsets[e], offsets[e+1]):
+      dH  = dY @ Wd[e]^T
+      dG  = dH * up * Silu'(gate)        dU = dH * Silu(gate)
+      dX  = dG @ Wg[e]^T + dU @ Wu[e]^T
+      dWd[e] = h^T @ dY     dWg[e] = X^T @ dG     dWu[e] = X^T @ dU
+    ``dy`` is the gradient of the expert outputs (rows of mlp_out).  Returns
+    (dx_perm [P,d], dw_gate [E,d,f], dw_up [E,d,f], dw_down [E,f,d]) in fp64;
+    experts without rows get zero weight gradients.
+    """
+    x_perm = np.asarray(x_perm, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    E = len(offsets) - 1
+    d, f = w_gate.shape[1], w_gate.shape[2]
+    dx = np.zeros_like(x_perm)
+    dwg = np.zeros((E, d, f))
+    dwu = np.zeros((E, d, f))
+    dwd = np.zeros((E, f, d))
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a == b:
+            continue
+        X, dY = x_perm[a:b], dy[a:b]
+        Wg = np.asarray(w_gate[e], dtype=np.float64)
+        Wu = np.asarray(w_up[e], dtype=np.float64)
+        Wd = np.asarray(w_down[e], dtype=np.float64)
+        gate, up = X @ Wg, X @ Wu
+        h = silu(gate) * up
+        dH = dY @ Wd.T
+        dG = dH * up * silu_grad(gate)
+        dU = dH * silu(gate)
+        dx[a:b] = dG @ Wg.T + dU @ Wu.T
+        dwd[e] = h.T @ dY
+        dwg[e] = X.T @ dG
+        dwu[e] = X.T @ dU
+    return dx, dwg, dwu, dwd
+
+
 # ---------------------------------------------------------------- stage 5
 def combine(y, dest_row, w):
     """Output reduction (Algorithm 1, stage 5, forward):
@@ -318,3 +364,27 @@ def moe_forward_tokens(x_rows, logits_rows, w_gate, w_up, w_down, k, renormalize
         y[sel] = he @ np.asarray(w_down[e], dtype=np.float64)
     out = np.einsum("nk,nkd->nd", w, y)
     return dict(idx=idx, w=w, h=h, y=y, out=out)
+
+
+def moe_backward(x, logits, w_gate, w_up, w_down, dout, k, renormalize=True):
+    """Gradients of one layer's output (moe_forward) with respect to its
+    inputs, for an output gradient ``dout`` [T,d], the top-k selection held
+    fixed.  Runs the forward of Algorithm 1, then its stages backwards:
+    output reduction backward (stage 5), the expert MLP backward (stage 4),
+    the un-permute of the row gradients to their tokens (the transpose of
+    mlp_in = input[input_indices]: every row adds into its token), and the
+    gate gradient taken back to the router logits (stage 1).
+    Returns a dict with dx [T,d], d_logits [T,E], dw_gate, dw_up [E,d,f],
+    dw_down [E,f,d] (fp64)."""
+    x = np.asarray(x, dtype=np.float64)
+    E = np.asarray(logits).shape[1]
+    idx, w = route_topk(logits, k, renormalize)
+    counts, offsets, src, dst = dispatch(idx, E)
+    xp = permute(x, src)
+    _, y = expert_mlp(xp, offsets, w_gate, w_up, w_down)
+    dy, dw = combine_backward(dout, y, dst, w)
+    dxp, dwg, dwu, dwd = expert_mlp_backward(xp, offsets, w_gate, w_up, w_down, dy)
+    dx = np.zeros_like(x)
+    np.add.at(dx, src, dxp)
+    d_logits = route_backward(np.asarray(logits, dtype=np.float64), idx, dw, renormalize)
+    return {"dx": dx, "d_logits": d_logits, "dw_gate": dwg, "dw_up": dwu, "dw_down": dwd}

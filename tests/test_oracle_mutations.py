@@ -172,3 +172,31 @@ def test_route_backward_softmax_over_wrong_set_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "route_backward", other_set)
     _fails(pins.test_route_backward_matches_finite_differences, True)
     _fails(pins.test_route_backward_matches_finite_differences, False)
+
+
+def test_silu_grad_without_product_term_is_caught(monkeypatch):
+    sigmoid_only = lambda z: 1.0 / (1.0 + np.exp(-np.asarray(z, dtype=np.float64)))  # noqa: E731
+    monkeypatch.setattr(om, "silu_grad", sigmoid_only)
+    monkeypatch.setattr(oracle, "silu_grad", sigmoid_only)
+    _fails(pins.test_layer_backward_matches_finite_differences, True)
+    _fails(pins.test_silu_grad_matches_finite_differences_and_limits)
+
+
+def test_unpermute_overwriting_instead_of_adding_is_caught(monkeypatch):
+    real = om.expert_mlp_backward
+
+    def dropped(x_perm, offsets, w_gate, w_up, w_down, dy):
+        dx, dwg, dwu, dwd = real(x_perm, offsets, w_gate, w_up, w_down, dy)
+        return dx * 0.5, dwg, dwu, dwd     # as if one of two slots were lost
+    monkeypatch.setattr(om, "expert_mlp_backward", dropped)
+    _fails(pins.test_layer_backward_matches_finite_differences, False)
+
+
+def test_up_gradient_with_wrong_factor_is_caught(monkeypatch):
+    real = om.expert_mlp_backward
+
+    def wrong(x_perm, offsets, w_gate, w_up, w_down, dy):
+        # dU = dH * up instead of dH * Silu(gate): swap the roles of gate and up
+        return real(x_perm, offsets, w_up, w_gate, w_down, dy)
+    monkeypatch.setattr(om, "expert_mlp_backward", wrong)
+    _fails(pins.test_layer_backward_scalar_closed_form)

@@ -460,3 +460,67 @@ def test_combine_backward_golden_scalar():
     dy, dw = oracle.combine_backward(np.array([[3.0]]), np.array([[2.0], [-4.0]]), np.array([0, 1]),
                                      np.array([[0.25, 0.75]]))
     assert dy.ravel().tolist() == [0.75, 2.25] and dw.ravel().tolist() == [6.0, -12.0]
+
+
+# ------------------------------------------------------- layer backward
+def test_silu_grad_matches_finite_differences_and_limits():
+    z = np.linspace(-12.0, 12.0, 97)
+    fd = (oracle.silu(z + 1e-6) - oracle.silu(z - 1e-6)) / 2e-6
+    np.testing.assert_allclose(oracle.silu_grad(z), fd, atol=1e-8)
+    assert oracle.silu_grad(np.array([0.0]))[0] == 0.5          # sigmoid(0) * (1 + 0)
+    assert abs(oracle.silu_grad(np.array([-60.0]))[0]) < 1e-20  # flat far left
+    assert abs(oracle.silu_grad(np.array([60.0]))[0] - 1.0) < 1e-20  # identity far right
+
+
+def _small_layer(seed, T, d, E, k, f):
+    rng = _rng(seed)
+    x = _bf16_values(rng.standard_normal((T, d)))
+    wg = _bf16_values(rng.standard_normal((E, d, f)) / math.sqrt(d))
+    wu = _bf16_values(rng.standard_normal((E, d, f)) / math.sqrt(d))
+    wd = _bf16_values(rng.standard_normal((E, f, d)) / math.sqrt(f))
+    logits = _random_logits(rng, T, E).astype(np.float64)
+    dout = rng.standard_normal((T, d))
+    return x.astype(np.float64), logits, wg.astype(np.float64), wu.astype(np.float64), wd.astype(np.float64), dout
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_layer_backward_matches_finite_differences(renorm):
+    """Every gradient of the layer against central differences of the
+    per-token brute-force forward (every token through its experts, no
+    grouping or index maps), L = <dout, out>.  E = 4 with k = 2 leaves one
+    expert with few rows; the selection does not move under the 1e-6 steps."""
+    T, d, E, k, f = 7, 4, 4, 2, 3
+    x, l, wg, wu, wd, dout = _small_layer(61, T, d, E, k, f)
+    g = oracle.moe_backward(x, l.astype(np.float32), wg, wu, wd, dout, k, renorm)
+
+    def loss(xx=x, ll=l, gg=wg, uu=wu, dd=wd):
+        return float(np.sum(dout * _brute_force_layer(xx, ll, gg, uu, dd, k, renorm)))
+    np.testing.assert_allclose(g["dx"], _finite_diff(lambda v: loss(xx=v), x), atol=1e-7)
+    np.testing.assert_allclose(g["d_logits"], _finite_diff(lambda v: loss(ll=v), l), atol=1e-7)
+    np.testing.assert_allclose(g["dw_gate"], _finite_diff(lambda v: loss(gg=v), wg), atol=1e-7)
+    np.testing.assert_allclose(g["dw_up"], _finite_diff(lambda v: loss(uu=v), wu), atol=1e-7)
+    np.testing.assert_allclose(g["dw_down"], _finite_diff(lambda v: loss(dd=v), wd), atol=1e-7)
+
+
+def test_layer_backward_scalar_closed_form():
+    """d = f = 1, one token, one expert: out = wd * SiLU(wg x) * (wu x), so
+    d out/dx = wd (SiLU'(wg x) wg wu x + SiLU(wg x) wu) and
+    d out/d wd = SiLU(wg x) wu x, written with math.exp at x=1, wg=1, wu=2,
+    wd=3."""
+    s = 1.0 / (1.0 + math.exp(-1.0))
+    silu1, dsilu1 = s, s * (1.0 + (1.0 - s))
+    g = oracle.moe_backward(np.array([[1.0]]), np.array([[0.3]], dtype=np.float32), np.array([[[1.0]]]),
+                            np.array([[[2.0]]]), np.array([[[3.0]]]), np.array([[1.0]]), 1, True)
+    assert g["dx"][0, 0] == pytest.approx(3.0 * (dsilu1 * 2.0 + silu1 * 2.0), rel=1e-14)
+    assert g["dw_down"][0, 0, 0] == pytest.approx(silu1 * 2.0, rel=1e-14)
+    assert g["dw_gate"][0, 0, 0] == pytest.approx(3.0 * 2.0 * dsilu1, rel=1e-14)
+    assert g["dw_up"][0, 0, 0] == pytest.approx(3.0 * silu1, rel=1e-14)
+    assert g["d_logits"][0, 0] == 0.0     # one expert, renormalised: the gate is constant 1
+
+
+def test_expert_without_rows_gets_zero_weight_gradient():
+    T, d, E, k, f = 5, 4, 6, 1, 3
+    x, l, wg, wu, wd, dout = _small_layer(67, T, d, E, k, f)
+    l[:, 5] = -30.0                       # expert 5 is never chosen
+    g = oracle.moe_backward(x, l.astype(np.float32), wg, wu, wd, dout, k)
+    assert not g["dw_gate"][5].any() and not g["dw_up"][5].any() and not g["dw_down"][5].any()
