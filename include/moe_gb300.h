@@ -290,6 +290,47 @@ MOE_API moe_status_t moe_combine(const void* y, const int32_t* dest_row, const f
                          int64_t T, int32_t k, int32_t d, void* out, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stage 4 for training — the grouped gate/up GEMM of moe_grouped_swiglu
+ * that also keeps the gate and up pre-activations G = x_perm Wg[e] and
+ * U = x_perm Wu[e] (bf16), which the backward reads:
+ *   h  [P, f] bf16 out, Silu(G)*U as moe_grouped_swiglu writes it;
+ *   gu [P, 2f] bf16 out, interleaved like the packed gate/up weights: for
+ *      gate/up tile t (h_t = 128 if f % 128 == 0, else 64 columns),
+ *      gu[r, 2*h_t*t + i] = G[r, h_t*t + i] and gu[r, 2*h_t*t + h_t + i] =
+ *      U[r, h_t*t + i], 0 <= i < h_t.
+ * Other arguments and errors as moe_grouped_swiglu; workspace
+ * moe_grouped_swiglu_workspace_bytes().
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_grouped_gate_up_save(const void* x_perm, const int32_t* offsets, int64_t P,
+                                      int32_t E, int32_t d, int32_t f, const void* packed,
+                                      void* h, void* gu, void* workspace, size_t workspace_bytes,
+                                      moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 4 backward — the grouped SwiGLU expert MLP (Algorithm 1, stage 4)
+ * differentiated, as four grouped GEMMs on the tensor cores.  For expert e
+ * and its rows (G, U from moe_grouped_gate_up_save, H = Silu(G)*U, dY the
+ * gradient of the expert outputs):
+ *   dH = dY Wd[e]^T;  dG = dH U Silu'(G);  dU = dH Silu(G)
+ *   dx_perm = dG Wg[e]^T + dU Wu[e]^T
+ *   dw_down[e] = H^T dY;  dw_gate[e] = X^T dG;  dw_up[e] = X^T dU
+ * with fp32 accumulation and bf16 results.
+ *   x_perm, dy, dx_perm [P, d] bf16; h [P, f]; gu, dgu [P, 2f] (dgu is
+ *   written: dG and dU interleaved like gu); packed from moe_pack_weights
+ *   (the same weights as the forward); dw_gate, dw_up [E, d, f] and
+ *   dw_down [E, f, d] bf16 out, in moe_pack_weights' input layout (every
+ *   expert written, zero for an expert without rows).
+ * Workspace moe_grouped_swiglu_workspace_bytes().  Errors as
+ * moe_grouped_swiglu.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_grouped_swiglu_backward(const void* x_perm, const void* h, const void* gu,
+                                         const void* dy, const int32_t* offsets, int64_t P,
+                                         int32_t E, int32_t d, int32_t f, const void* packed,
+                                         void* dgu, void* dx_perm, void* dw_gate, void* dw_up,
+                                         void* dw_down, void* workspace, size_t workspace_bytes,
+                                         moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Stage 5 backward — output reduction, backward (Algorithm 1, stage 5,
  * backward function): for every routed pair (t, j) at row
  * r = dest_row[t*k + j],
@@ -356,6 +397,37 @@ MOE_API moe_status_t moe_forward_routed(const void* x, const void* router_packed
                                 int32_t renormalize, void* out,
                                 int32_t* topk_idx_out, float* topk_w_out,
                                 void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The whole layer backward: the gradients of moe_forward's output with
+ * respect to x, the router logits and the three expert weight tensors, for
+ * an output gradient dout, the top-k selection held fixed.  The forward is
+ * recomputed first (full activation recomputation: route, index, permute,
+ * gate/up GEMM keeping G and U, down GEMM with ungated rows), then:
+ * output reduction backward (Algorithm 1, stage 5), gate gradient to the
+ * logits, the four backward GEMMs of moe_grouped_swiglu_backward, and the
+ * un-permute of the row gradients (each token sums its k rows).
+ *   x [T, d] bf16; logits [T, E] fp32; packed from moe_pack_weights;
+ *   dout [T, d] bf16; dx [T, d] bf16 out; d_logits [T, E] fp32 out;
+ *   dw_gate, dw_up [E, d, f], dw_down [E, f, d] bf16 out.
+ * Workspace moe_backward_workspace_bytes(T, E, k, d, f).  Errors as the
+ * forward.  moe_backward_timed records events[i] (MOE_BACKWARD_STAGES + 1
+ * caller-created cudaEvent_t) at the boundaries
+ *   0 route+index+permute 1 gate/up 2 down 3 output-reduction and logit
+ *   backward 4 dgrad down 5 dgrad gate/up 6 wgrad down 7 wgrad gate/up 8
+ *   un-permute 9.
+ * ---------------------------------------------------------------------- */
+#define MOE_BACKWARD_STAGES 9
+MOE_API size_t moe_backward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f);
+MOE_API moe_status_t moe_backward(const void* x, const float* logits, const void* packed, const void* dout,
+                          int64_t T, int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize,
+                          void* dx, float* d_logits, void* dw_gate, void* dw_up, void* dw_down,
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_backward_timed(const void* x, const float* logits, const void* packed,
+                                const void* dout, int64_t T, int32_t d, int32_t E, int32_t k,
+                                int32_t f, int32_t renormalize, void* dx, float* d_logits,
+                                void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+                                size_t workspace_bytes, moe_stream_t stream, void* const* events);
 
 /* ------------------------------------------------------------------------
  * moe_forward with stage timing: identical work, plus cudaEventRecord of

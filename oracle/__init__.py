@@ -15,6 +15,7 @@ from .moe_oracle import (  # noqa: F401
     silu_grad,
     expert_mlp,
     expert_mlp_backward,
+    expert_gate_up,
     combine,
     combine_backward,
     route_backward,

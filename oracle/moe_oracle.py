@@ -213,7 +213,22 @@ def silu_grad(z: np.ndarray) -> np.ndarray:
     return s * (1.0 + z * (1.0 - s))
 
 
-def expert_mlp_backward(x_perm, offsets, w_gate, w_up, w_down, dy):
+def expert_gate_up(x_perm, offsets, w_gate, w_up):
+    """The gate and up pre-activations of every row (Algorithm 1, stage 4:
+    gate_out = X_e @ Wg[e], up_out = X_e @ Wu[e]), [P, f] each, fp64."""
+    x_perm = np.asarray(x_perm, dtype=np.float64)
+    f = w_gate.shape[2]
+    gate = np.zeros((x_perm.shape[0], f))
+    up = np.zeros((x_perm.shape[0], f))
+    for e in range(len(offsets) - 1):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a < b:
+            gate[a:b] = x_perm[a:b] @ np.asarray(w_gate[e], dtype=np.float64)
+            up[a:b] = x_perm[a:b] @ np.asarray(w_up[e], dtype=np.float64)
+    return gate, up
+
+
+def expert_mlp_backward(x_perm, offsets, w_gate, w_up, w_down, dy, return_preact_grads=False):
     """Backward of the grouped SwiGLU expert MLP (Algorithm 1, stage 4,
     differentiated), expert by expert on its rows [offsets[e], offsets[e+1]):
       dH  = dY @ Wd[e]^T
@@ -222,7 +237,8 @@ def expert_mlp_backward(x_perm, offsets, w_gate, w_up, w_down, dy):
       dWd[e] = h^T @ dY     dWg[e] = X^T @ dG     dWu[e] = X^T @ dU
     ``dy`` is the gradient of the expert outputs (rows of mlp_out).  Returns
     (dx_perm [P,d], dw_gate [E,d,f], dw_up [E,d,f], dw_down [E,f,d]) in fp64;
-    experts without rows get zero weight gradients.
+    experts without rows get zero weight gradients.  With
+    ``return_preact_grads`` the tuple ends with dgate, dup [P,f].
     """
     x_perm = np.asarray(x_perm, dtype=np.float64)
     dy = np.asarray(dy, dtype=np.float64)
@@ -232,6 +248,8 @@ def expert_mlp_backward(x_perm, offsets, w_gate, w_up, w_down, dy):
     dwg = np.zeros((E, d, f))
     dwu = np.zeros((E, d, f))
     dwd = np.zeros((E, f, d))
+    dgate = np.zeros((x_perm.shape[0], f))
+    dup = np.zeros((x_perm.shape[0], f))
     for e in range(E):
         a, b = int(offsets[e]), int(offsets[e + 1])
         if a == b:
@@ -249,6 +267,10 @@ def expert_mlp_backward(x_perm, offsets, w_gate, w_up, w_down, dy):
         dwd[e] = h.T @ dY
         dwg[e] = X.T @ dG
         dwu[e] = X.T @ dU
+        dgate[a:b] = dG
+        dup[a:b] = dU
+    if return_preact_grads:
+        return dx, dwg, dwu, dwd, dgate, dup
     return dx, dwg, dwu, dwd
 
 

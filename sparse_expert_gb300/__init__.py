@@ -1,4 +1,4 @@
-"""Single-GPU Mixture-of-Experts layer forward for GB300 (sm_103a).
+"""Single-GPU Mixture-of-Experts layer, forward and backward, for GB300 (sm_103a).
 
 The compute lives in libmoe_gb300.so (hand-written CUDA kernels behind a C
 ABI, declared in include/moe_gb300.h); this package is its Python binding.
@@ -24,6 +24,12 @@ from ._lib import (  # noqa: F401
     FORWARD_STAGES,
     moe_forward_workspace_bytes,
     moe_grouped_swiglu,
+    moe_grouped_gate_up_save,
+    moe_grouped_swiglu_backward,
+    gu_split,
+    moe_backward,
+    moe_backward_timed,
+    BACKWARD_STAGES,
     moe_quantize_fp8_blockwise,
     moe_dequantize_fp8_blockwise,
     moe_pack_weights,

@@ -73,6 +73,13 @@ SIGNATURES = {
     "moe_forward_timed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "moe_forward_host": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P]),
     "moe_read_device_status": (_S, [_P, _P, ctypes.POINTER(_I32)]),
+    "moe_grouped_gate_up_save": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_swiglu_backward": (_S, [_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                         _SZ, _P]),
+    "moe_backward_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
+    "moe_backward": (_S, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_backward_timed": (_S, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                _P]),
 }
 for _name, (_res, _args) in SIGNATURES.items():
     _fn = getattr(lib, _name)
@@ -259,6 +266,97 @@ def moe_grouped_swiglu(x_perm, offsets, E, f, packed, row_scale=None, workspace=
                                   _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_grouped_swiglu")
     return h, y
+
+
+def moe_grouped_gate_up_save(x_perm, offsets, E, f, packed, workspace=None, stream=None):
+    """(h [P,f], gu [P,2f]): the gate/up GEMM keeping G and U, interleaved per gate/up tile."""
+    _contig(x_perm, torch.bfloat16, "x_perm")
+    _contig(offsets, torch.int32, "offsets")
+    P, d = x_perm.shape
+    dev = x_perm.device
+    if workspace is None:
+        workspace = torch.empty(lib.moe_grouped_swiglu_workspace_bytes(), dtype=torch.uint8, device=dev)
+    h = torch.empty(P, f, dtype=torch.bfloat16, device=dev)
+    gu = torch.empty(P, 2 * f, dtype=torch.bfloat16, device=dev)
+    _check(lib.moe_grouped_gate_up_save(_ptr(x_perm), _ptr(offsets), P, E, d, f, _ptr(packed), _ptr(h), _ptr(gu),
+                                        _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_grouped_gate_up_save")
+    return h, gu
+
+
+def gu_split(gu, f):
+    """(G [P,f], U [P,f]) from the interleaved [P,2f] layout (a view reshuffle, for checks)."""
+    h_t = 128 if f % 128 == 0 else 64
+    t = gu.reshape(gu.shape[0], f // h_t, 2, h_t)
+    return t[:, :, 0, :].reshape(gu.shape[0], f), t[:, :, 1, :].reshape(gu.shape[0], f)
+
+
+def moe_grouped_swiglu_backward(x_perm, h, gu, dy, offsets, E, f, packed, workspace=None, stream=None):
+    """dict(dgu, dx_perm, dw_gate, dw_up, dw_down) of the expert MLP backward."""
+    for t, name in ((x_perm, "x_perm"), (h, "h"), (gu, "gu"), (dy, "dy")):
+        _contig(t, torch.bfloat16, name)
+    _contig(offsets, torch.int32, "offsets")
+    P, d = x_perm.shape
+    dev = x_perm.device
+    if workspace is None:
+        workspace = torch.empty(lib.moe_grouped_swiglu_workspace_bytes(), dtype=torch.uint8, device=dev)
+    r = dict(dgu=torch.empty(P, 2 * f, dtype=torch.bfloat16, device=dev),
+             dx_perm=torch.empty(P, d, dtype=torch.bfloat16, device=dev),
+             dw_gate=torch.empty(E, d, f, dtype=torch.bfloat16, device=dev),
+             dw_up=torch.empty(E, d, f, dtype=torch.bfloat16, device=dev),
+             dw_down=torch.empty(E, f, d, dtype=torch.bfloat16, device=dev))
+    _check(lib.moe_grouped_swiglu_backward(_ptr(x_perm), _ptr(h), _ptr(gu), _ptr(dy), _ptr(offsets), P, E, d, f,
+                                           _ptr(packed), _ptr(r["dgu"]), _ptr(r["dx_perm"]), _ptr(r["dw_gate"]),
+                                           _ptr(r["dw_up"]), _ptr(r["dw_down"]), _ptr(workspace), workspace.numel(),
+                                           _stream(stream)),
+           "moe_grouped_swiglu_backward")
+    return r
+
+
+def _backward_outputs(T, d, E, f, dev):
+    return dict(dx=torch.empty(T, d, dtype=torch.bfloat16, device=dev),
+                d_logits=torch.empty(T, E, dtype=torch.float32, device=dev),
+                dw_gate=torch.empty(E, d, f, dtype=torch.bfloat16, device=dev),
+                dw_up=torch.empty(E, d, f, dtype=torch.bfloat16, device=dev),
+                dw_down=torch.empty(E, f, d, dtype=torch.bfloat16, device=dev))
+
+
+def moe_backward(x, logits, packed, dout, E, k, f, renormalize=True, workspace=None, grads=None, stream=None):
+    """dict(dx, d_logits, dw_gate, dw_up, dw_down): the layer backward (forward recomputed)."""
+    _contig(x, torch.bfloat16, "x")
+    _contig(logits, torch.float32, "logits")
+    _contig(dout, torch.bfloat16, "dout")
+    T, d = x.shape
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(lib.moe_backward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device=dev)
+    g = grads if grads is not None else _backward_outputs(T, d, E, f, dev)
+    _check(lib.moe_backward(_ptr(x), _ptr(logits), _ptr(packed), _ptr(dout), T, d, E, k, f, int(bool(renormalize)),
+                            _ptr(g["dx"]), _ptr(g["d_logits"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]),
+                            _ptr(g["dw_down"]), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_backward")
+    return g
+
+
+BACKWARD_STAGES = ("recompute_route_index_permute", "recompute_gate_up", "recompute_down", "combine_route_bwd",
+                   "dgrad_down", "dgrad_gate_up", "wgrad_down", "wgrad_gate_up", "unpermute")
+
+
+def moe_backward_timed(x, logits, packed, dout, E, k, f, workspace, grads, events, renormalize=True, stream=None):
+    """moe_backward recording events[0..9] at the stage boundaries (BACKWARD_STAGES)."""
+    T, d = x.shape
+    s = stream if stream is not None else torch.cuda.current_stream()
+    for ev in events:
+        if ev.cuda_event == 0:
+            ev.record(s)
+    handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    g = grads
+    _check(lib.moe_backward_timed(_ptr(x), _ptr(logits), _ptr(packed), _ptr(dout), T, d, E, k, f,
+                                  int(bool(renormalize)), _ptr(g["dx"]), _ptr(g["d_logits"]), _ptr(g["dw_gate"]),
+                                  _ptr(g["dw_up"]), _ptr(g["dw_down"]), _ptr(workspace), workspace.numel(), _stream(s),
+                                  handles),
+           "moe_backward_timed")
+    return g
 
 
 def moe_combine(y, dest_row, T, k, topk_w=None, stream=None):

@@ -116,6 +116,31 @@ ForwardLayout forward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t
   return L;
 }
 
+// ---- moe_backward workspace layout (the forward's buffers, then the
+// backward's; y is reused for dx_perm once the output-reduction backward
+// has read it)
+struct BackwardLayout {
+  ForwardLayout F;
+  size_t gu, dy, dgu, d_topk_w, total;
+};
+
+BackwardLayout backward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f) {
+  const int64_t P = T * k;
+  BackwardLayout L{};
+  L.F = forward_layout(T, E, k, d, f);
+  size_t o = L.F.total;
+  L.gu = o;
+  o += align_up(static_cast<size_t>(P) * 2 * f * 2);
+  L.dy = o;
+  o += align_up(static_cast<size_t>(P) * d * 2);
+  L.dgu = o;
+  o += align_up(static_cast<size_t>(P) * 2 * f * 2);
+  L.d_topk_w = o;
+  o += align_up(static_cast<size_t>(P) * 4);
+  L.total = o;
+  return L;
+}
+
 // Dispatch state inside a workspace: flags right after the header (cleared
 // with it), agg/incl at `state_at` (not cleared).
 DispatchState dispatch_state_split(void* ws, size_t state_at, int64_t P, int E) {
@@ -422,6 +447,90 @@ moe_status_t moe_route_backward(const float* logits, const int32_t* topk_idx, co
   return MOE_OK;
 }
 
+moe_status_t moe_grouped_gate_up_save(const void* x_perm, const int32_t* offsets, int64_t P, int32_t E, int32_t d,
+                                      int32_t f, const void* packed, void* h, void* gu, void* workspace,
+                                      size_t workspace_bytes, moe_stream_t stream) {
+  if (P < 0 || P >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "P must be in [0, 2^31)");
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
+  moe_status_t s = check_gemm_dims(d, f);
+  if (s != MOE_OK) return s;
+  if ((s = check_tile_space(P, E, d, f)) != MOE_OK) return s;
+  if (!offsets || !packed) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (P > 0 && (!x_perm || !h || !gu)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!workspace || workspace_bytes < sizeof(WsHeader) || !aligned(workspace, kAlign))
+    return fail(MOE_ERR_WORKSPACE, "grouped GEMM workspace needs 256 bytes, 256-byte aligned");
+  if (!aligned(x_perm, 16) || !aligned(h, 16) || !aligned(gu, 16) || !aligned(packed, 16))
+    return fail(MOE_ERR_INVALID_ARG, "x_perm, h, gu and packed must be 16-byte aligned");
+  if (P == 0) return MOE_OK;
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* hdr = static_cast<WsHeader*>(workspace);
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st), "workspace clear");
+  BackwardGemmArgs a{};
+  a.P = P;
+  a.E = E;
+  a.d = d;
+  a.f = f;
+  a.offsets = offsets;
+  a.w_gate_up = packed;
+  a.x_perm = x_perm;
+  a.h = h;
+  a.gu = gu;
+  a.counters = hdr->tile_counter;
+  a.status = &hdr->status;
+  MOE_CUDA(launch_gate_up_save(a, dev.num_sms, st), "gate/up GEMM launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_grouped_swiglu_backward(const void* x_perm, const void* h, const void* gu, const void* dy,
+                                         const int32_t* offsets, int64_t P, int32_t E, int32_t d, int32_t f,
+                                         const void* packed, void* dgu, void* dx_perm, void* dw_gate, void* dw_up,
+                                         void* dw_down, void* workspace, size_t workspace_bytes,
+                                         moe_stream_t stream) {
+  if (P < 0 || P >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "P must be in [0, 2^31)");
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
+  moe_status_t s = check_gemm_dims(d, f);
+  if (s != MOE_OK) return s;
+  if ((s = check_tile_space(P, E, d, f)) != MOE_OK) return s;
+  if (static_cast<int64_t>(E) * ((std::max(d, f) + 127) / 128) * (2 * static_cast<int64_t>(f) / 64 + d / 64) >=
+      (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "problem too large for the tile index");
+  if (!offsets || !packed || !dw_gate || !dw_up || !dw_down) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (P > 0 && (!x_perm || !h || !gu || !dy || !dgu || !dx_perm)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!workspace || workspace_bytes < sizeof(WsHeader) || !aligned(workspace, kAlign))
+    return fail(MOE_ERR_WORKSPACE, "grouped GEMM workspace needs 256 bytes, 256-byte aligned");
+  const void* al[] = {x_perm, h, gu, dy, dgu, dx_perm, dw_gate, dw_up, dw_down, packed};
+  for (const void* q : al)
+    if (!aligned(q, 16)) return fail(MOE_ERR_INVALID_ARG, "every matrix must be 16-byte aligned");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* hdr = static_cast<WsHeader*>(workspace);
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st), "workspace clear");
+  BackwardGemmArgs a{};
+  a.P = P;
+  a.E = E;
+  a.d = d;
+  a.f = f;
+  a.offsets = offsets;
+  a.w_gate_up = packed;
+  a.w_down = static_cast<const __nv_bfloat16*>(packed) + static_cast<int64_t>(E) * 2 * f * d;
+  a.x_perm = x_perm;
+  a.dy = dy;
+  a.h = const_cast<void*>(h);
+  a.gu = const_cast<void*>(gu);
+  a.dgu = dgu;
+  a.dx_perm = dx_perm;
+  a.dw_gate = dw_gate;
+  a.dw_up = dw_up;
+  a.dw_down = dw_down;
+  a.counters = hdr->tile_counter;
+  a.status = &hdr->status;
+  MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, nullptr), "backward GEMM launch");
+  return MOE_OK;
+}
+
 size_t moe_forward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f) {
   if (T < 0 || E < 1 || k < 1 || d < 1 || f < 1) return 0;
   return forward_layout(T, E, k, d, f).total;
@@ -579,6 +688,140 @@ moe_status_t moe_forward_host(const void* x_host, const float* logits_host, void
   if (T > 0) MOE_CUDA(cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, st), "out copy to host");
   MOE_CUDA(cudaStreamSynchronize(st), "stream synchronize");
   return MOE_OK;
+}
+
+size_t moe_backward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f) {
+  if (T < 0 || E < 1 || k < 1 || d < 1 || f < 1) return 0;
+  return backward_layout(T, E, k, d, f).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_status_t backward_impl(const void* x, const float* logits, const void* packed, const void* dout, int64_t T,
+                           int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize, void* dx,
+                           float* d_logits, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream, void* const* events) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if ((s = check_gemm_dims(d, f)) != MOE_OK) return s;
+  const int64_t P = T * k;
+  if ((s = check_tile_space(P, E, d, f)) != MOE_OK) return s;
+  if (static_cast<int64_t>(E) * ((std::max(d, f) + 127) / 128) * (2 * static_cast<int64_t>(f) / 64 + d / 64) >=
+      (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "problem too large for the tile index");
+  if (!packed || !dw_gate || !dw_up || !dw_down) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T > 0 && (!x || !logits || !dout || !dx || !d_logits)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  const void* al[] = {x, dout, dx, dw_gate, dw_up, dw_down, packed};
+  for (const void* q : al)
+    if (!aligned(q, 16)) return fail(MOE_ERR_INVALID_ARG, "x, dout, dx, the weight gradients and packed must be "
+                                                          "16-byte aligned");
+  const BackwardLayout L = backward_layout(T, E, k, d, f);
+  if (!workspace || workspace_bytes < L.total || !aligned(workspace, kAlign))
+    return fail(MOE_ERR_WORKSPACE, "backward workspace needs " + std::to_string(L.total) + " bytes, 256-byte aligned");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  auto* hdr = reinterpret_cast<WsHeader*>(ws);
+  const ForwardLayout& F = L.F;
+  auto* counts = reinterpret_cast<int32_t*>(ws + F.counts);
+  auto* offsets = reinterpret_cast<int32_t*>(ws + F.offsets);
+  auto* topk_idx = reinterpret_cast<int32_t*>(ws + F.topk_idx);
+  auto* topk_w = reinterpret_cast<float*>(ws + F.topk_w);
+  auto* src_token = reinterpret_cast<int32_t*>(ws + F.src_token);
+  auto* dest_row = reinterpret_cast<int32_t*>(ws + F.dest_row);
+  auto* row_w = reinterpret_cast<float*>(ws + F.row_w);
+  auto* d_topk_w = reinterpret_cast<float*>(ws + L.d_topk_w);
+  void* x_perm = ws + F.x_perm;
+  void* h = ws + F.h;
+  void* y = ws + F.y;
+  void* dx_perm = ws + F.y;  // y is dead once the output-reduction backward has read it
+  void* gu = ws + L.gu;
+  void* dy = ws + L.dy;
+  void* dgu = ws + L.dgu;
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+  };
+  MOE_CUDA(mark(0), "event record");
+  MOE_CUDA(cudaMemsetAsync(ws, 0, F.clear_bytes, st), "workspace clear");
+  BackwardGemmArgs a{};
+  a.P = P;
+  a.E = E;
+  a.d = d;
+  a.f = f;
+  a.offsets = offsets;
+  a.w_gate_up = packed;
+  a.w_down = static_cast<const __nv_bfloat16*>(packed) + static_cast<int64_t>(E) * 2 * f * d;
+  a.x_perm = x_perm;
+  a.dy = dy;
+  a.h = h;
+  a.gu = gu;
+  a.dgu = dgu;
+  a.dx_perm = dx_perm;
+  a.dw_gate = dw_gate;
+  a.dw_up = dw_up;
+  a.dw_down = dw_down;
+  a.counters = hdr->tile_counter;
+  a.status = &hdr->status;
+  if (T == 0) {
+    // no rows: every weight gradient is zero
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st), "offsets clear");
+    for (int i = 1; i <= 4; ++i) MOE_CUDA(mark(i), "event record");
+    MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 5 : nullptr),
+             "backward GEMM launch");
+    MOE_CUDA(mark(9), "event record");
+    return MOE_OK;
+  }
+  // forward recomputation: stages 1-4 with G and U kept; the down GEMM
+  // leaves its rows ungated (the gates enter in the output reduction)
+  MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, counts, dev.num_sms, st),
+           "route launch");
+  DispatchState dstate = dispatch_state_split(ws, F.dispatch_state, P, E);
+  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, ws, dstate, st),
+           "index launch");
+  MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, dev.num_sms, st), "permute launch");
+  MOE_CUDA(mark(1), "event record");
+  MOE_CUDA(launch_gate_up_save(a, dev.num_sms, st), "gate/up GEMM launch");
+  MOE_CUDA(mark(2), "event record");
+  const auto* wdn = static_cast<const __nv_bfloat16*>(a.w_down);
+  GroupedGemmProblem g2{h, wdn, offsets, nullptr, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
+  MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
+  MOE_CUDA(mark(3), "event record");
+  // stage 5 backward, then the gates back to the logits
+  MOE_CUDA(launch_combine_backward(dout, y, dest_row, topk_w, T, k, d, dy, d_topk_w, dev.num_sms, st),
+           "combine backward launch");
+  MOE_CUDA(launch_route_backward(logits, topk_idx, d_topk_w, T, E, k, renormalize, d_logits, dev.num_sms, st),
+           "route backward launch");
+  MOE_CUDA(mark(4), "event record");
+  // stage 4 backward: dgrad (down, gate/up), wgrad (down, gate/up)
+  MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 5 : nullptr), "backward GEMM launch");
+  // the transpose of the permute: each token sums its k row gradients
+  MOE_CUDA(launch_combine(dx_perm, dest_row, nullptr, T, k, d, dx, dev.num_sms, st), "un-permute launch");
+  MOE_CUDA(mark(9), "event record");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_backward(const void* x, const float* logits, const void* packed, const void* dout, int64_t T,
+                          int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize, void* dx, float* d_logits,
+                          void* dw_gate, void* dw_up, void* dw_down, void* workspace, size_t workspace_bytes,
+                          moe_stream_t stream) {
+  return backward_impl(x, logits, packed, dout, T, d, E, k, f, renormalize, dx, d_logits, dw_gate, dw_up, dw_down,
+                       workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status_t moe_backward_timed(const void* x, const float* logits, const void* packed, const void* dout, int64_t T,
+                                int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize, void* dx,
+                                float* d_logits, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+                                size_t workspace_bytes, moe_stream_t stream, void* const* events) {
+  if (!events) return fail(MOE_ERR_INVALID_ARG, "NULL events");
+  return backward_impl(x, logits, packed, dout, T, d, E, k, f, renormalize, dx, d_logits, dw_gate, dw_up, dw_down,
+                       workspace, workspace_bytes, stream, events);
 }
 
 moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream, int32_t* status) {

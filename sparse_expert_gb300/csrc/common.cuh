@@ -1,4 +1,4 @@
-// Device-side helpers shared by the kernels of the MoE-layer forward.
+// Device-side helpers shared by the kernels of the MoE layer.
 #pragma once
 
 #include <cstdint>
@@ -18,8 +18,9 @@ enum : int32_t {
 struct WsHeader {
   int32_t status;          // first device error, or 0
   int32_t ticket;          // dynamic block ticket of the look-back pass
-  int32_t tile_counter[2]; // persistent-GEMM tile counters (gate/up, down)
-  int32_t reserved[60];
+  int32_t tile_counter[6]; // persistent-GEMM tile counters (forward: gate/up, down;
+                           // backward: dgrad down, dgrad gate/up, wgrad down, wgrad gate/up)
+  int32_t reserved[56];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is one 256-byte line");
 
@@ -225,12 +226,36 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return desc;
 }
 
+// Shared-memory matrix descriptor of an MN-major bf16 operand written by TMA
+// with 128-byte swizzling, as chunks of [K rows][64 MN values]: each K row
+// of a chunk is 128 bytes (64 consecutive M or N indices), 8 K rows make a
+// 1024-byte swizzle atom.  Stride byte offset (bits 32-45) = 1024 >> 4, the
+// step between 8-row groups along K; leading byte offset (bits 16-29) =
+// `chunk_bytes` >> 4, the step between 64-wide chunks along M or N.  Moving
+// 16 rows along K (one MMA) adds 2048 bytes to the start address, so every
+// start stays 1024-byte aligned (base offset 0).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t chunk_bytes) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  desc |= static_cast<uint64_t>((chunk_bytes >> 4) & 0x3FFFu) << 16;
+  desc |= static_cast<uint64_t>(1024 >> 4) << 32;
+  desc |= static_cast<uint64_t>(1) << 46;
+  desc |= static_cast<uint64_t>(2) << 61;
+  return desc;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Same with the operands' major-ness: bit 15 set = A is MN-major (M
+// contiguous), bit 16 set = B is MN-major (N contiguous).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16_f32_major(int M, int N, bool a_mn, bool b_mn) {
+  return umma_idesc_bf16_f32(M, N) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
 }
 
 // ------------------------------------------------------------------ misc

@@ -31,6 +31,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -80,49 +81,6 @@ struct Smem {
   uint32_t tmem_base;
   int abort;
 };
-
-// Expert, M tile and N tile of flat tile t.  s_pre[e] = M tiles of experts
-// before e (s_pre[E] = all).  The largest e with s_pre[e]*nt <= t has a
-// non-empty range containing t.
-__device__ __forceinline__ void decode_tile(int t, const int32_t* s_pre, int E, int n_tiles, int& e, int& mt,
-                                            int& nt) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_pre[mid] * n_tiles <= t)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  e = lo;
-  const int mtiles = s_pre[e + 1] - s_pre[e];
-  const int local = t - s_pre[e] * n_tiles;
-  nt = local / mtiles;
-  mt = local - nt * mtiles;
-}
-
-// Stores one 32-column chunk of the epilogue warp's 32 tile rows.  Thread
-// `lane` holds row `lane` as 16 packed bf16x2 words (64 bytes).  Through a
-// 2 KB shared-memory transpose, each 16-byte global store instruction then
-// covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes.  In
-// the buffer, 16-byte piece j of row r sits at slot j ^ ((r >> 1) & 3),
-// so the row-wise writes and the row-pair reads are free of bank
-// conflicts.  Rows at or past `valid_rows` are not stored.
-__device__ __forceinline__ void store_chunk_coalesced(const uint32_t (&w)[16], uint4* sbuf, int lane,
-                                                      __nv_bfloat16* row0, int64_t ld, int valid_rows) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    sbuf[lane * 4 + (j ^ ((lane >> 1) & 3))] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = i * 8 + (lane >> 2);
-    const int g = lane & 3;
-    const uint4 v = sbuf[r * 4 + (g ^ ((r >> 1) & 3))];
-    if (r < valid_rows) *reinterpret_cast<uint4*>(row0 + r * ld + g * 8) = v;
-  }
-  __syncwarp();
-}
 
 template <int BN, bool kSwiGLU>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -409,60 +367,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 }
 
 // ------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// 2-D bf16 map over a row-major [rows, cols] matrix, box [box_rows, 64],
-// 128-byte swizzle, zero fill outside the matrix.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 3-D bf16 map over tile-major weights: [blocks][bn rows][64], box one
-// block, 128-byte swizzle.
-bool make_weight_map(CUtensorMap* map, const void* ptr, int64_t blocks, int bn) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(bn), static_cast<cuuint64_t>(blocks)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(BK) * 2, static_cast<cuuint64_t>(bn) * BK * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(bn), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BN, bool kSwiGLU>
 cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, pb.a, pb.P, pb.K, BM)) return cudaErrorInvalidValue;
+  if (!make_bf16_map_2d(&ma, pb.a, pb.P, pb.K, BK, BM)) return cudaErrorInvalidValue;
+  // tile-major weights as [blocks][BN rows][64], one block per box
   const int64_t blocks = static_cast<int64_t>(pb.E) * (pb.n_per_expert / BN) * ((pb.K + BK - 1) / BK);
-  if (!make_weight_map(&mb, pb.b, blocks, BN)) return cudaErrorInvalidValue;
+  if (!make_bf16_map_3d(&mb, pb.b, BK, BN, blocks, BK, BN)) return cudaErrorInvalidValue;
   Params prm;
   prm.offsets = pb.offsets;
   prm.row_scale = pb.row_scale;

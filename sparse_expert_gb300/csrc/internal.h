@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <string>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -89,6 +90,40 @@ struct GroupedGemmProblem {
 };
 enum class Epilogue { kSwiGLU, kScale };
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
+
+// ---- stage 4 backward: expert GEMMs of the backward pass
+struct BackwardGemmArgs {
+  int64_t P;
+  int E, d, f;
+  const int32_t* offsets;  // [E+1]
+  const void* w_gate_up;   // packed gate/up weights (first part of moe_pack_weights' output)
+  const void* w_down;      // packed down weights (second part)
+  const void* x_perm;      // [P, d]
+  const void* dy;          // [P, d] gradient of the expert outputs
+  void* h;                 // [P, f]   (written by the gate/up GEMM, read by the down wgrad)
+  void* gu;                // [P, 2f]  gate and up pre-activations, interleaved per gate/up tile
+  void* dgu;               // [P, 2f]  their gradients, same order
+  void* dx_perm;           // [P, d]
+  void* dw_gate;           // [E, d, f] or null (skip both gate/up weight gradients)
+  void* dw_up;             // [E, d, f]
+  void* dw_down;           // [E, f, d] or null
+  int32_t* counters;       // the workspace header's 6 tile counters, zeroed before launch:
+                           // [0] gate/up (save), [2..5] dgrad down, dgrad gate/up,
+                           // wgrad down, wgrad gate/up
+  int32_t* status;
+};
+// Gate/up GEMM that writes H and, for the backward, G and U.
+cudaError_t launch_gate_up_save(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream);
+// dG,dU (from dY, G, U), dX, and the weight gradients, in that order;
+// events[0..3] (optional) are recorded after each of the four GEMMs.
+cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
+                                         void* const* events);
+
+// Tiled bf16 TMA maps, 128-byte swizzle, zero fill outside the tensor.
+// 2-D: row-major [rows, cols], box [box_rows, box_cols].  3-D: dense
+// [d2][d1][d0] (d0 contiguous), box [1][box1][box0].
+bool make_bf16_map_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
+bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int box0, int box1);
 
 // Device properties of the current device (cached per device).
 struct DeviceInfo {

@@ -245,25 +245,6 @@ router_topk_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 // packed[((i / 64) * E_pad + e) * 64 + i % 64] = w[i][e] (0 for e >= E)
 __global__ void pack_router_kernel(const __nv_bfloat16* __restrict__ w, int d, int E, int E_pad,
                                    __nv_bfloat16* __restrict__ packed) {
@@ -299,30 +280,11 @@ cudaError_t launch_router_topk(const void* x, const void* w_packed, int64_t T, i
                                int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* status,
                                cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return cudaErrorInvalidValue;
   const int e_pad = router_e_pad(E);
   CUtensorMap mx, mw;
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[2] = {BK, BM};
-    cuuint32_t estr[2] = {1, 1};
-    if (fn(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    cuuint64_t dims[3] = {BK, static_cast<cuuint64_t>(e_pad), static_cast<cuuint64_t>(d / BK)};
-    cuuint64_t strides[2] = {BK * 2, static_cast<cuuint64_t>(e_pad) * BK * 2};
-    cuuint32_t box[3] = {BK, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    if (fn(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w_packed), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!make_bf16_map_2d(&mx, x, T, d, BK, BM)) return cudaErrorInvalidValue;
+  // packed router weights as [d/64][E_pad rows][64], box 128 rows of one block
+  if (!make_bf16_map_3d(&mw, w_packed, BK, e_pad, d / BK, BK, 128)) return cudaErrorInvalidValue;
   RouterParams prm;
   prm.T = T;
   prm.E = E;

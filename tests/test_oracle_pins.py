@@ -524,3 +524,23 @@ def test_expert_without_rows_gets_zero_weight_gradient():
     l[:, 5] = -30.0                       # expert 5 is never chosen
     g = oracle.moe_backward(x, l.astype(np.float32), wg, wu, wd, dout, k)
     assert not g["dw_gate"][5].any() and not g["dw_up"][5].any() and not g["dw_down"][5].any()
+
+
+def test_gate_up_preactivations_give_the_mlp_hidden_state():
+    """h of the expert MLP is Silu(gate) * up of the pre-activations, and the
+    pre-activation gradients put together give the same dx_perm."""
+    T, d, E, k, f = 9, 6, 3, 2, 5
+    x, l, wg, wu, wd, _ = _small_layer(71, T, d, E, k, f)
+    idx, _ = oracle.route_topk(l.astype(np.float32), k)
+    _, offsets, src, _ = oracle.dispatch(idx, E)
+    xp = oracle.permute(x, src)
+    gate, up = oracle.expert_gate_up(xp, offsets, wg, wu)
+    h, _ = oracle.expert_mlp(xp, offsets, wg, wu, wd)
+    np.testing.assert_allclose(oracle.silu(gate) * up, h, rtol=1e-13, atol=1e-14)
+    dy = _rng(72).standard_normal((T * k, d))
+    dx, _, _, _, dG, dU = oracle.expert_mlp_backward(xp, offsets, wg, wu, wd, dy, return_preact_grads=True)
+    ref = np.zeros_like(dx)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        ref[a:b] = dG[a:b] @ wg[e].T + dU[a:b] @ wu[e].T
+    np.testing.assert_allclose(dx, ref, rtol=1e-12, atol=1e-13)
