@@ -1,5 +1,5 @@
 #!/usr/bin/env python
-"""Throughput of one MoE-layer forward on GB300.
+"""Throughput of one MoE-layer forward on GB300 (and, on the side, of its backward).
 
 A step is one pass of the whole path — route + token counts, look-back
 index, permute, gate/up grouped GEMM with SwiGLU, down grouped GEMM with
@@ -176,6 +176,15 @@ def stage_work(cfg):
     }
 
 
+def backward_gemm_flops(cfg):
+    """Algorithmic FLOPs of the GEMM stages of the layer backward (real rows
+    only): the recomputed forward GEMMs, two dgrad and two wgrad GEMMs."""
+    P = cfg.T * cfg.k
+    pdf = P * cfg.d * cfg.f
+    return {"recompute_gate_up": 4 * pdf, "recompute_down": 2 * pdf, "dgrad_down": 2 * pdf,
+            "dgrad_gate_up": 4 * pdf, "wgrad_down": 2 * pdf, "wgrad_gate_up": 4 * pdf}
+
+
 def weight_bytes_read(cfg, counts):
     nonempty = int((np.asarray(counts) > 0).sum())
     return nonempty * 3 * cfg.d * cfg.f * 2
@@ -337,6 +346,66 @@ def gpu_arm(args):
                   "router_topk_ms": round(router_ms, 4), "router_tflops": round(router_tf, 1),
                   "note": "whole layer from x and router weights: fused router GEMM + top-k replaces the given logits"}
 
+    # training use: the layer backward (forward recomputed inside it)
+    backward = None
+    if not args.no_backward:
+        grads = {"dx": torch.empty(T, d, dtype=torch.bfloat16, device="cuda"),
+                 "d_logits": torch.empty(T, E, dtype=torch.float32, device="cuda"),
+                 "dw_gate": torch.empty(E, d, f, dtype=torch.bfloat16, device="cuda"),
+                 "dw_up": torch.empty(E, d, f, dtype=torch.bfloat16, device="cuda"),
+                 "dw_down": torch.empty(E, f, d, dtype=torch.bfloat16, device="cuda")}
+        bws = torch.empty(moe.moe_backward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device="cuda")
+        dout = (torch.randn(T, d, device="cuda", generator=torch.Generator(device="cuda").manual_seed(args.seed + 5))
+                * 0.1).to(torch.bfloat16)
+        nb = len(moe.BACKWARD_STAGES)
+        bsteps = max(1, min(args.steps, 20))
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)] for _ in range(bsteps)]
+        for _ in range(max(3, min(args.warmup, 5))):
+            moe.moe_backward_timed(x, logits, packed, dout, E, k, f, bws, grads, bev[0], cfg.renormalize, stream)
+        torch.cuda.synchronize()
+        bclocks = ClockSampler(local)
+        bclocks.start()
+        barrier(world)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for s_ in range(bsteps):
+            moe.moe_backward_timed(x, logits, packed, dout, E, k, f, bws, grads, bev[s_], cfg.renormalize, stream)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bclk = bclocks.stop()
+        if moe.moe_read_device_status(bws) != 0:
+            raise SystemExit("device status after the backward steps")
+        bwd_s = max_over_ranks(b0.elapsed_time(b1) / 1e3, world, device="cuda")
+        bstage = {name: statistics.mean(bev[s_][i].elapsed_time(bev[s_][i + 1]) for s_ in range(bsteps))
+                  for i, name in enumerate(moe.BACKWARD_STAGES)}
+        bflops = backward_gemm_flops(cfg)
+        bst = {}
+        for name, ms in bstage.items():
+            e = {"ms": round(ms, 4)}
+            if name in bflops:
+                e["tflops"] = round(bflops[name] / (ms * 1e-3) / 1e12, 1)
+            bst[name] = e
+        gemm_names = [n for n in moe.BACKWARD_STAGES if n in bflops]
+        bgemm_ms = sum(bstage[n] for n in gemm_names)
+        bdom = max(gemm_names, key=lambda n: bstage[n])
+        bach = bflops[bdom] / (bstage[bdom] * 1e-3) / 1e12
+        backward = {
+            "value": round(job_throughput(T * bsteps, world, bwd_s), 1), "unit": "tokens/s",
+            "ms_per_step": round(bwd_s * 1e3 / bsteps, 4), "steps": bsteps,
+            "train_step_tokens_per_s": round(T / (max_s / args.steps + bwd_s / bsteps), 1),
+            "gemm_tflops": round(sum(bflops.values()) / (bgemm_ms * 1e-3) / 1e12, 1),
+            "stages": bst,
+            "roofline": {"bound": "tensor", "kernel": f"grouped_gemm_bwd_kernel ({bdom})", "achieved": round(bach, 1),
+                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": round(bach / peaks["bf16_tflops_sustained"], 4), "traffic": None,
+                         "peak_source": f"bf16 dense sustained, {peaks['source']}"},
+            "clocks": bclk,
+            "note": "gradients of x, the router logits and the three expert weight tensors for a given output "
+                    "gradient; the forward is recomputed inside (route, index, permute, gate/up keeping G and U, "
+                    "ungated down); train_step = forward + backward",
+        }
+        del bws, grads
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = min(args.cpu_sample_tokens, T)
@@ -361,7 +430,7 @@ def gpu_arm(args):
                              "weight_bytes_read": weight_bytes_read(cfg, counts)},
             "permute_gbs": stages["permute"]["gbs"],
             "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed,
-            "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk,
+            "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk, "backward": backward,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -412,6 +481,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-routed", action="store_true", help="skip the fused-router forward measurement")
+    ap.add_argument("--no-backward", action="store_true", help="skip the layer-backward measurement")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--ref-sample-tokens", type=int, default=4)
     args = ap.parse_args(argv)

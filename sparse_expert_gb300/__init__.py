@@ -28,6 +28,7 @@ from ._lib import (  # noqa: F401
     moe_grouped_swiglu_backward,
     gu_split,
     moe_backward,
+    moe_backward_workspace_bytes,
     moe_backward_timed,
     BACKWARD_STAGES,
     moe_quantize_fp8_blockwise,

@@ -405,6 +405,10 @@ def moe_forward_workspace_bytes(T, E, k, d, f) -> int:
     return lib.moe_forward_workspace_bytes(T, E, k, d, f)
 
 
+def moe_backward_workspace_bytes(T, E, k, d, f) -> int:
+    return lib.moe_backward_workspace_bytes(T, E, k, d, f)
+
+
 def moe_forward_layout(T, E, k, d, f) -> ForwardLayout:
     lay = ForwardLayout()
     _check(lib.moe_forward_layout(T, E, k, d, f, ctypes.byref(lay)), "moe_forward_layout")

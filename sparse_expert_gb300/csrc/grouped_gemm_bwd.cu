@@ -309,13 +309,13 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
             // rows valid..63 of every chunk belong to the next expert (or lie
             // past the matrix): a whole 128-byte row is zero whatever the
             // swizzle does inside it
-            constexpr int kChunks = (BM + BN) / 64;
-            const int per_chunk = (BK - valid) * 8;
-            for (int i = lane; i < per_chunk * kChunks; i += 32) {
-              const int c = i / per_chunk;
-              const int rem = i - c * per_chunk;
+            // lane: 16-byte piece lane % 8 of rows valid + lane / 8, +4, ...
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            const int piece = lane & 7;
+#pragma unroll
+            for (int c = 0; c < (BM + BN) / 64; ++c) {
               uint8_t* cb = c < BM / 64 ? a_st + c * kChunk : b_st + (c - BM / 64) * kChunk;
-              reinterpret_cast<uint4*>(cb + valid * 128)[rem] = make_uint4(0, 0, 0, 0);
+              for (int r = valid + (lane >> 3); r < BK; r += 4) reinterpret_cast<uint4*>(cb + r * 128)[piece] = zero;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();

@@ -75,3 +75,24 @@ def test_reference_arm_prints_one_json_line():
     assert rec["impl"] == "reference" and rec["unit"] == "tokens/s" and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
     assert rec["warmup"] >= 3
+
+
+def test_backward_gemm_work_of_the_1t_layer():
+    """Recomputed forward (6 P d f) + two dgrad (6 P d f) + two wgrad (6 P d f)."""
+    cfg = workloads.get("t1")
+    fl = bench.backward_gemm_flops(cfg)
+    P = 16384 * 8
+    assert sum(fl.values()) == 18 * P * 6144 * 1792
+    assert fl["dgrad_gate_up"] == fl["wgrad_gate_up"] == fl["recompute_gate_up"] == 4 * P * 6144 * 1792
+
+
+def test_bench_uses_only_names_the_binding_exports():
+    """Every moe.<name> that bench.py calls exists in the package (caught here,
+    on the CPU, rather than after a GPU run)."""
+    import re
+    moe = pytest.importorskip("sparse_expert_gb300")
+    entry = os.path.join(os.path.dirname(bench.__file__), "__graft_entry__.py")
+    names = set(re.findall(r"\bmoe\.(\w+)", open(bench.__file__).read() + open(entry).read()))
+    assert names, "no binding calls found"
+    missing = sorted(n for n in names if not hasattr(moe, n))
+    assert not missing, missing

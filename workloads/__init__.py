@@ -56,6 +56,10 @@ CONFIGS = {
     "t1": MoEConfig("t1", T=16384, d=6144, E=384, k=8, f=1792, routing="normal"),
     # same layer, router biased by a Zipf law over the experts
     "skew": MoEConfig("skew", T=16384, d=6144, E=384, k=8, f=1792, routing="zipf"),
+    # the t1 routing shape (16,384 tokens, 384 experts, top-8: ~341 rows per
+    # expert) on narrow experts: the profiling case of the per-tile behaviour
+    # of the t1 GEMMs with a few GB on the device
+    "t1_narrow": MoEConfig("t1_narrow", T=16384, d=1024, E=384, k=8, f=512, routing="normal"),
     # one 64k-token sequence with forced-uniform routing
     "long": MoEConfig("long", T=65536, d=6144, E=384, k=8, f=1792, routing="fur"),
 }
