@@ -4,7 +4,8 @@
 // Computer", §3.1, Algorithm 1, stage 5 (output reduction, backward): for
 // every routed pair (t, j) at row r, mlp_out_grad[r] = w[t, j] *
 // output_grad[t] and weights_grad[t, j] = <mlp_out[r], output_grad[t]>.
-// One warp per token; the k rows are visited in slot order.
+// One warp per token; each row's dot product sums in slot-independent
+// lane order (the lane's pieces in order, then a butterfly over lanes).
 //
 // route_backward: the gates' gradient taken back to the router logits
 // (Algorithm 1, stage 1, Softmax and TopK, with the selection held fixed):
@@ -19,6 +20,11 @@ namespace {
 
 constexpr int kWarps = 8;
 
+// The token's output-gradient row is read once: each lane walks its 16-byte
+// pieces of that row and, for every piece, visits the k expert rows (their
+// row index and gate broadcast from lane j), so a token's k rows are read
+// and written once and dout is not re-read per slot.
+template <int KMAX>
 __global__ void __launch_bounds__(kWarps * 32)
 combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ mlp_out,
                         const int32_t* __restrict__ dest_row, const float* __restrict__ w, int64_t T, int k, int dvec,
@@ -26,32 +32,45 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarps;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < T; t += warps_total) {
+    const int64_t my_row = lane < k ? __ldg(dest_row + t * k + lane) : 0;
+    const float my_w = lane < k ? __ldg(w + t * k + lane) : 0.f;
     const uint4* g = dout + t * dvec;
-    for (int j = 0; j < k; ++j) {
-      const int64_t row = __ldg(dest_row + t * k + j);
-      const float wj = __ldg(w + t * k + j);
-      const uint4* y = mlp_out + row * dvec;
-      uint4* dy = d_mlp_out + row * dvec;
-      float dot = 0.f;
-      for (int v = lane; v < dvec; v += 32) {
-        const uint4 gv = __ldg(g + v);
-        const uint4 yv = __ldg(y + v);
-        const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&gv);
-        const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yv);
-        uint32_t o[4];
+    float dot[KMAX];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 gf = __bfloat1622float2(gh[i]);
-          const float2 yf = __bfloat1622float2(yh[i]);
-          dot = fmaf(yf.x, gf.x, dot);
-          dot = fmaf(yf.y, gf.y, dot);
-          o[i] = pack_bf16x2(wj * gf.x, wj * gf.y);
+    for (int j = 0; j < KMAX; ++j) dot[j] = 0.f;
+    for (int v = lane; v < dvec; v += 32) {
+      const uint4 gv = __ldg(g + v);
+      const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&gv);
+      float2 gf[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) gf[i] = __bfloat1622float2(gh[i]);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
+          const float wj = __shfl_sync(0xffffffffu, my_w, j);
+          const uint4 yv = __ldg(mlp_out + row * dvec + v);
+          const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yv);
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 yf = __bfloat1622float2(yh[i]);
+            dot[j] = fmaf(yf.x, gf[i].x, dot[j]);
+            dot[j] = fmaf(yf.y, gf[i].y, dot[j]);
+            o[i] = pack_bf16x2(wj * gf[i].x, wj * gf[i].y);
+          }
+          d_mlp_out[row * dvec + v] = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        dy[v] = make_uint4(o[0], o[1], o[2], o[3]);
       }
+    }
 #pragma unroll
-      for (int s = 16; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
-      if (lane == 0) d_w[t * k + j] = dot;
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        float s = dot[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) d_w[t * k + j] = s;
+      }
     }
   }
 }
@@ -125,9 +144,15 @@ cudaError_t launch_combine_backward(const void* dout, const void* mlp_out, const
                                     int64_t T, int k, int d, void* d_mlp_out, float* d_w, int num_sms,
                                     cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  combine_backward_kernel<<<token_grid(T, num_sms), kWarps * 32, 0, stream>>>(
-      static_cast<const uint4*>(dout), static_cast<const uint4*>(mlp_out), dest_row, w, T, k, d / 8,
-      static_cast<uint4*>(d_mlp_out), d_w);
+  const auto* g = static_cast<const uint4*>(dout);
+  const auto* y = static_cast<const uint4*>(mlp_out);
+  auto* dy = static_cast<uint4*>(d_mlp_out);
+  if (k <= 8)
+    combine_backward_kernel<8><<<token_grid(T, num_sms), kWarps * 32, 0, stream>>>(g, y, dest_row, w, T, k, d / 8, dy,
+                                                                                    d_w);
+  else
+    combine_backward_kernel<32><<<token_grid(T, num_sms), kWarps * 32, 0, stream>>>(g, y, dest_row, w, T, k, d / 8,
+                                                                                     dy, d_w);
   return cudaGetLastError();
 }
 
