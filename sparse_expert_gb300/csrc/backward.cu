@@ -38,8 +38,12 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
     float dot[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) dot[j] = 0.f;
-    for (int v = lane; v < dvec; v += 32) {
-      const uint4 gv = __ldg(g + v);
+    // the loop runs warp-uniformly (the shuffles need every lane); lanes past
+    // the row's end take no load or store
+    for (int v0 = 0; v0 < dvec; v0 += 32) {
+      const int v = v0 + lane;
+      const bool active = v < dvec;
+      const uint4 gv = active ? __ldg(g + v) : make_uint4(0, 0, 0, 0);
       const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&gv);
       float2 gf[4];
 #pragma unroll
@@ -49,17 +53,19 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
         if (j < k) {
           const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
           const float wj = __shfl_sync(0xffffffffu, my_w, j);
-          const uint4 yv = __ldg(mlp_out + row * dvec + v);
-          const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yv);
-          uint32_t o[4];
+          if (active) {
+            const uint4 yv = __ldg(mlp_out + row * dvec + v);
+            const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yv);
+            uint32_t o[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 yf = __bfloat1622float2(yh[i]);
-            dot[j] = fmaf(yf.x, gf[i].x, dot[j]);
-            dot[j] = fmaf(yf.y, gf[i].y, dot[j]);
-            o[i] = pack_bf16x2(wj * gf[i].x, wj * gf[i].y);
+            for (int i = 0; i < 4; ++i) {
+              const float2 yf = __bfloat1622float2(yh[i]);
+              dot[j] = fmaf(yf.x, gf[i].x, dot[j]);
+              dot[j] = fmaf(yf.y, gf[i].y, dot[j]);
+              o[i] = pack_bf16x2(wj * gf[i].x, wj * gf[i].y);
+            }
+            d_mlp_out[row * dvec + v] = make_uint4(o[0], o[1], o[2], o[3]);
           }
-          d_mlp_out[row * dvec + v] = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
     }
