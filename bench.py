@@ -298,6 +298,32 @@ def gpu_arm(args):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "traffic": traffic, "peak_source": f"bf16 dense burst, {peaks['source']}"}
 
+    # the same layer with the permute fused into the gate/up GEMM (TMA gathers of x[src_token])
+    gathered = None
+    if not args.no_gathered:
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)] for _ in range(args.steps)]
+        for _ in range(args.warmup):
+            moe.moe_forward_gathered_timed(x, logits, packed, E, k, f, ws, out, warm_events, cfg.renormalize, stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for s_ in range(args.steps):
+            moe.moe_forward_gathered_timed(x, logits, packed, E, k, f, ws, out, gev[s_], cfg.renormalize, stream)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        if moe.moe_read_device_status(ws) != 0:
+            raise SystemExit("device status after the gathered forward")
+        gat_s = max_over_ranks(g0.elapsed_time(g1) / 1e3, world, device="cuda")
+        gstage = {name: round(statistics.mean(gev[s_][i].elapsed_time(gev[s_][i + 1]) for s_ in range(args.steps)), 4)
+                  for i, name in enumerate(moe.FORWARD_STAGES) if name != "permute"}
+        gathered = {"value": round(job_throughput(T * args.steps, world, gat_s), 1), "unit": "tokens/s",
+                    "ms_per_step": round(gat_s * 1e3 / args.steps, 4), "stages_ms": gstage,
+                    "gate_up_tflops": round(work["gate_up"]["flops"] / (gstage["gate_up"] * 1e-3) / 1e12, 1),
+                    "note": "the same layer without x_perm: four warps of the gate/up GEMM gather its A rows "
+                            "x[src_token[r]] with 16-byte cp.async copies; outputs bit-identical to the permuted "
+                            "path"}
+
     # end to end: host buffers through the C ABI, copies inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -429,7 +455,7 @@ def gpu_arm(args):
             "grouped_gemm": {"tflops": round(gemm_tflops, 2), "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
                              "weight_bytes_read": weight_bytes_read(cfg, counts)},
             "permute_gbs": stages["permute"]["gbs"],
-            "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed,
+            "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed, "gathered_forward": gathered,
             "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk, "backward": backward,
         }
         print(json.dumps(line), flush=True)
@@ -482,6 +508,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-routed", action="store_true", help="skip the fused-router forward measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the layer-backward measurement")
+    ap.add_argument("--no-gathered", action="store_true", help="skip the gathered (no x_perm) forward measurement")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--ref-sample-tokens", type=int, default=4)
     args = ap.parse_args(argv)

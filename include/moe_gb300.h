@@ -430,6 +430,27 @@ MOE_API moe_status_t moe_backward_timed(const void* x, const float* logits, cons
                                 size_t workspace_bytes, moe_stream_t stream, void* const* events);
 
 /* ------------------------------------------------------------------------
+ * moe_forward without the permuted copy of the tokens: the gate/up GEMM
+ * fetches each A row x[src_token[r]] itself (four warps of 16-byte
+ * asynchronous copies into the swizzled A stage) — the SonicMoE kernel's way
+ * of running the expert GEMMs on the token-dispatch layout ("Training a
+ * 1T-Params MoE on EU public infrastructure", SonicMoE).  Same arguments, results, workspace and
+ * layout as moe_forward, except that the layout's x_perm region is left
+ * unwritten.  moe_forward_gathered_timed records events as
+ * moe_forward_timed does (the permute stage is empty).
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_forward_gathered(const void* x, const float* logits, const void* packed,
+                                  int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
+                                  int32_t renormalize, void* out,
+                                  int32_t* topk_idx_out, float* topk_w_out,
+                                  void* workspace, size_t workspace_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_forward_gathered_timed(const void* x, const float* logits, const void* packed,
+                                        int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
+                                        int32_t renormalize, void* out, void* workspace,
+                                        size_t workspace_bytes, moe_stream_t stream,
+                                        void* const* events);
+
+/* ------------------------------------------------------------------------
  * moe_forward with stage timing: identical work, plus cudaEventRecord of
  * events[i] (caller-created cudaEvent_t handles, MOE_FORWARD_STAGES + 1 of
  * them) on `stream` at the stage boundaries

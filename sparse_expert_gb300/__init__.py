@@ -19,6 +19,8 @@ from ._lib import (  # noqa: F401
     moe_forward_layout,
     moe_forward_timed,
     moe_forward_routed,
+    moe_forward_gathered,
+    moe_forward_gathered_timed,
     moe_pack_router_weights,
     moe_router_topk,
     FORWARD_STAGES,

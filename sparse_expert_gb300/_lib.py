@@ -71,6 +71,8 @@ SIGNATURES = {
     "moe_forward_layout": (_S, [_I64, _I32, _I32, _I32, _I32, ctypes.POINTER(ForwardLayout)]),
     "moe_forward": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_timed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
+    "moe_forward_gathered": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_gathered_timed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "moe_forward_host": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P]),
     "moe_read_device_status": (_S, [_P, _P, ctypes.POINTER(_I32)]),
     "moe_grouped_gate_up_save": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -433,6 +435,38 @@ def moe_forward(x, logits, packed, E, k, f, renormalize=True, workspace=None, ou
 
 
 FORWARD_STAGES = ("route", "index", "permute", "gate_up", "down", "combine")
+
+
+def moe_forward_gathered(x, logits, packed, E, k, f, renormalize=True, workspace=None, out=None, topk_idx=None,
+                         topk_w=None, stream=None):
+    """moe_forward with the gate/up GEMM gathering its rows from x (no x_perm)."""
+    _contig(x, torch.bfloat16, "x")
+    _contig(logits, torch.float32, "logits")
+    T, d = x.shape
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(lib.moe_forward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    _check(lib.moe_forward_gathered(_ptr(x), _ptr(logits), _ptr(packed), T, d, E, k, f, int(bool(renormalize)),
+                                    _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(),
+                                    _stream(stream)),
+           "moe_forward_gathered")
+    return out
+
+
+def moe_forward_gathered_timed(x, logits, packed, E, k, f, workspace, out, events, renormalize=True, stream=None):
+    """moe_forward_gathered recording events[0..6] at the stage boundaries."""
+    T, d = x.shape
+    s = stream if stream is not None else torch.cuda.current_stream()
+    for ev in events:
+        if ev.cuda_event == 0:
+            ev.record(s)
+    handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    _check(lib.moe_forward_gathered_timed(_ptr(x), _ptr(logits), _ptr(packed), T, d, E, k, f, int(bool(renormalize)),
+                                          _ptr(out), _ptr(workspace), workspace.numel(), _stream(s), handles),
+           "moe_forward_gathered_timed")
+    return out
 
 
 def moe_forward_routed(x, router_packed, packed, E, k, f, renormalize=True, workspace=None, out=None, stream=None):

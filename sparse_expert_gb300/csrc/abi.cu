@@ -563,10 +563,12 @@ namespace {
 
 // Stage 1 reads `logits` when router_packed is null, else computes the
 // logits from x and the packed router weights inside the route kernel.
+// With `gathered`, the gate/up GEMM reads its A rows from x through
+// src_token (TMA gathers) and no permuted copy is made.
 moe_status_t forward_impl(const void* x, const float* logits, const void* router_packed, const void* packed,
                           int64_t T, int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out,
                           int32_t* topk_idx_out, float* topk_w_out, void* workspace, size_t workspace_bytes,
-                          moe_stream_t stream, void* const* events) {
+                          moe_stream_t stream, void* const* events, bool gathered = false) {
   moe_status_t s = check_routing(T, E, k);
   if (s != MOE_OK) return s;
   if ((s = check_gemm_dims(d, f)) != MOE_OK) return s;
@@ -622,11 +624,16 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* router
            "index launch");
   MOE_CUDA(mark(2), "event record");
   // stage 4
-  MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, dev.num_sms, st), "permute launch");
+  if (!gathered) MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, dev.num_sms, st), "permute launch");
   MOE_CUDA(mark(3), "event record");
   const auto* wgu = static_cast<const __nv_bfloat16*>(packed);
   const auto* wdn = wgu + static_cast<int64_t>(E) * 2 * f * d;
   GroupedGemmProblem g1{x_perm, wgu, offsets, nullptr, h, P, E, d, 2 * f, f, &hdr->tile_counter[0], &hdr->status};
+  if (gathered) {
+    g1.a = x;
+    g1.gather_rows = src_token;
+    g1.a_rows = T;
+  }
   MOE_CUDA(launch_grouped_gemm(g1, Epilogue::kSwiGLU, dev.num_sms, st), "gate/up GEMM launch");
   MOE_CUDA(mark(4), "event record");
   GroupedGemmProblem g2{h, wdn, offsets, row_w, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
@@ -666,6 +673,23 @@ moe_status_t moe_forward_timed(const void* x, const float* logits, const void* p
     if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "NULL event handle");
   return forward_impl(x, logits, nullptr, packed, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
                       workspace_bytes, stream, events);
+}
+
+moe_status_t moe_forward_gathered(const void* x, const float* logits, const void* packed, int64_t T, int32_t d,
+                                  int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out,
+                                  int32_t* topk_idx_out, float* topk_w_out, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream) {
+  return forward_impl(x, logits, nullptr, packed, T, d, E, k, f, renormalize, out, topk_idx_out, topk_w_out,
+                      workspace, workspace_bytes, stream, nullptr, true);
+}
+
+moe_status_t moe_forward_gathered_timed(const void* x, const float* logits, const void* packed, int64_t T, int32_t d,
+                                        int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out,
+                                        void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                        void* const* events) {
+  if (!events) return fail(MOE_ERR_INVALID_ARG, "NULL events");
+  return forward_impl(x, logits, nullptr, packed, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
+                      workspace_bytes, stream, events, true);
 }
 
 moe_status_t moe_forward_host(const void* x_host, const float* logits_host, void* out_host, void* x_dev,

@@ -23,6 +23,14 @@
 //   warps 2-9 epilogue: tcgen05.ld of the accumulator, fp32 math, bf16
 //            stores; TMEM lane quadrant = warp % 4, and the two warps of a
 //            quadrant take one half of the tile's columns each.
+// Gathered A ("Training a 1T-Params MoE on EU public infrastructure", the
+// SonicMoE kernel that runs the expert GEMMs on the token-dispatch layout
+// without a permuted copy): the gate/up GEMM can take its A rows straight
+// from the token matrix, row r of the grouped problem being token
+// gather_rows[r] (src_token): four warps copy each tile row's 128 bytes per
+// K block with 16-byte cp.async into the swizzled stage, signal the stage
+// barrier on completion, and the MMA thread fences the generic-proxy writes
+// before the tensor cores read them (the epilogue then has four warps).
 // Tiles: BM=128 rows of one expert's group (the last tile of a group is
 // partial; rows past the group are computed and not stored), BN columns of
 // that expert's weights.  Tile t of the flat order walks experts in order,
@@ -61,6 +69,10 @@ struct Cfg {
 
 struct Params {
   const int32_t* offsets;
+  const int32_t* gather_rows;  // gathered A: source row of every row, or null
+  int64_t P;                   // rows of the grouped problem
+  int64_t a_rows;              // rows of the gathered source matrix
+  const void* gather_src;      // the gathered source matrix [a_rows, K]
   const float* row_scale;
   __nv_bfloat16* out;
   int32_t* tile_counter;
@@ -82,11 +94,29 @@ struct Smem {
   int abort;
 };
 
-template <int BN, bool kSwiGLU>
+// Gathered A: one 16-byte piece of a row, 16 bytes from src or zeros when
+// src_bytes is 0 (a row past the problem).
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// One arrival on `bar` once every cp.async issued so far by this thread has
+// landed (the arrival is expected in the barrier's count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+template <int BN, bool kSwiGLU, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const Params p) {
   using C = Cfg<BN>;
+  // gathered A: warps 2-5 are the epilogue and warps 6-9 fetch the A rows
+  // (one thread per tile row); otherwise warps 2-9 are the epilogue
+  constexpr int kEpi = kGather ? 4 : kEpiWarps;
+  constexpr int kGatherThreads = kGather ? 128 : 0;
+  const __nv_bfloat16* x_src = reinterpret_cast<const __nv_bfloat16*>(p.gather_src);
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   // stage buffers need 1024-byte alignment for the 128-byte swizzle
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -129,16 +159,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     tmem_relinquish();
   } else if (warp == 2 && lane == 0) {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&S->full[i], 1);
+      mbar_init(&S->full[i], 1 + kGatherThreads);
       mbar_init(&S->empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S->tfull[i], 1);
-      mbar_init(&S->tempty[i], kEpiWarps);
+      mbar_init(&S->tempty[i], kEpi);
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&S->rfull[i], 1);
-      mbar_init(&S->rempty[i], 1 + kEpiWarps);
+      mbar_init(&S->rempty[i], 1 + kEpi + kGatherThreads / 32);
     }
     mbar_init(&S->drain, 1);
     S->abort = 0;
@@ -188,8 +218,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&S->full[stage], C::kStageBytes);
-          tma_load_2d(sA + stage * C::kABytes, &tm_a, &S->full[stage], kb * BK, row0);
+          if constexpr (kGather) {
+            mbar_arrive_expect_tx(&S->full[stage], C::kBBytes);
+          } else {
+            mbar_arrive_expect_tx(&S->full[stage], C::kStageBytes);
+            tma_load_2d(sA + stage * C::kABytes, &tm_a, &S->full[stage], kb * BK, row0);
+          }
           tma_load_3d(sB + stage * C::kBBytes, &tm_b, &S->full[stage], 0, 0, bblk + kb);
           last_stage = stage;
           last_phase = phase;
@@ -243,6 +277,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             ok = false;
             break;
           }
+          // gathered A rows were written by the gather threads' copies
+          // (generic proxy); order them before the tensor cores read them
+          if constexpr (kGather) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_after_sync();
           const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
           const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
@@ -272,10 +309,62 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       volatile int never = 0;
       mbar_wait(&S->drain, 0, &never);
     }
+  } else if (kGather && warp >= 2 + kEpi) {
+    // ------------------------------------------- gathered A rows (4 warps)
+    // thread g fetches row g of every A tile: token gather_rows[row], its 64
+    // columns of this K block as 8 copies of 16 bytes into the swizzled row
+    // (piece j at slot j ^ (g % 8)); rows past the problem read as zeros
+    const int g = threadIdx.x - 32 * (2 + kEpi);
+    int stage = 0;
+    uint32_t phase = 0;
+    int rs = 0;
+    uint32_t rphase = 0;
+    bool ok = true;
+    for (;;) {
+      if (!mbar_wait_warp(&S->rfull[rs], rphase, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int t = S->ring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S->rempty[rs]);
+      if (++rs == kRing) {
+        rs = 0;
+        rphase ^= 1u;
+      }
+      if (t < 0) break;
+      int e, mt, nt;
+      decode_tile(t, s_pre, p.E, p.n_tiles, e, mt, nt);
+      const int64_t row = static_cast<int64_t>(s_off[e]) + mt * BM + g;
+      const int src_bytes = row < p.P ? 16 : 0;
+      const __nv_bfloat16* src_row = x_src + (row < p.P ? static_cast<int64_t>(__ldg(p.gather_rows + row)) * p.K : 0);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait_warp(&S->empty[stage], phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = sA + stage * C::kABytes + g * 128;
+        const __nv_bfloat16* src = src_row + kb * BK;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cp_async_16(dst + ((j ^ (g & 7)) << 4), src + j * 8, src_bytes);
+        cp_async_arrive(&S->full[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    // no copy of this thread may still be in flight when the block exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!ok && lane == 0) {
+      record_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
   } else {
     // ---------------------------------------------------------- epilogue
     const int quad = warp & 3;         // TMEM lanes 32*quad .. 32*quad+31
-    const int half = (warp - 2) >> 2;  // which half of the tile's columns
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns (0 with 4 epilogue warps)
     uint4* sbuf = s_stage + (warp - 2) * 32 * 4;
     int rs = 0;
     uint32_t rphase = 0;
@@ -315,7 +404,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       };
       if constexpr (kSwiGLU) {
         constexpr int H = BN / 2;  // gate columns [0, H), up columns [H, 2H)
-        constexpr int kCols = H / 2;
+        constexpr int kCols = H / (kEpi / 4);
         const int c0 = half * kCols;
         __nv_bfloat16* dst = p.out + wrow0 * p.out_cols + static_cast<int64_t>(nt) * H + c0;
 #pragma unroll 1
@@ -335,7 +424,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
           store_chunk_coalesced(packed, sbuf, lane, dst + c, p.out_cols, valid_rows);
         }
       } else {
-        constexpr int kCols = BN / 2;
+        constexpr int kCols = BN / (kEpi / 4);
         const int c0 = half * kCols;
         const float scale = (lane < valid_rows && p.row_scale != nullptr) ? __ldg(p.row_scale + wrow0 + lane) : 1.0f;
         __nv_bfloat16* dst = p.out + wrow0 * p.out_cols + static_cast<int64_t>(nt) * BN + c0;
@@ -367,16 +456,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 }
 
 // ------------------------------------------------------------ host side
-template <int BN, bool kSwiGLU>
+template <int BN, bool kSwiGLU, bool kGather>
 cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap ma, mb;
-  if (!make_bf16_map_2d(&ma, pb.a, pb.P, pb.K, BK, BM)) return cudaErrorInvalidValue;
+  // the gathered variant reads A with plain copies; its map is unused (built over the same matrix)
+  if (!make_bf16_map_2d(&ma, pb.a, kGather ? pb.a_rows : pb.P, pb.K, BK, kGather ? 1 : BM))
+    return cudaErrorInvalidValue;
   // tile-major weights as [blocks][BN rows][64], one block per box
   const int64_t blocks = static_cast<int64_t>(pb.E) * (pb.n_per_expert / BN) * ((pb.K + BK - 1) / BK);
   if (!make_bf16_map_3d(&mb, pb.b, BK, BN, blocks, BK, BN)) return cudaErrorInvalidValue;
   Params prm;
   prm.offsets = pb.offsets;
+  prm.gather_rows = pb.gather_rows;
+  prm.P = pb.P;
+  prm.a_rows = pb.a_rows;
+  prm.gather_src = pb.a;
   prm.row_scale = pb.row_scale;
   prm.out = static_cast<__nv_bfloat16*>(pb.out);
   prm.tile_counter = pb.tile_counter;
@@ -388,7 +483,7 @@ cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t st
   prm.out_cols = pb.out_cols;
   const size_t smem = 1024 + static_cast<size_t>(C::kStages) * C::kStageBytes + sizeof(Smem) +
                       2 * static_cast<size_t>(pb.E + 1) * sizeof(int32_t) + 16 + kStoreStageBytes;
-  auto kernel = grouped_gemm_kernel<BN, kSwiGLU>;
+  auto kernel = grouped_gemm_kernel<BN, kSwiGLU, kGather>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   // persistent: one block per SM, never more blocks than an upper bound on tiles
@@ -404,14 +499,17 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int 
   if (pb.P == 0) return cudaSuccess;
   if (epi == Epilogue::kSwiGLU) {
     // N tile = matching gate and up halves of gate_up_half_tile(f) columns
-    return gate_up_tile_n(pb.out_cols) == 256 ? launch_bn<256, true>(pb, num_sms, stream)
-                                              : launch_bn<128, true>(pb, num_sms, stream);
+    const bool wide = gate_up_tile_n(pb.out_cols) == 256;
+    if (pb.gather_rows != nullptr)
+      return wide ? launch_bn<256, true, true>(pb, num_sms, stream) : launch_bn<128, true, true>(pb, num_sms, stream);
+    return wide ? launch_bn<256, true, false>(pb, num_sms, stream) : launch_bn<128, true, false>(pb, num_sms, stream);
   }
+  if (pb.gather_rows != nullptr) return cudaErrorNotSupported;
   // N tile of the packed down weights
   switch (down_tile_n(pb.out_cols)) {
-    case 256: return launch_bn<256, false>(pb, num_sms, stream);
-    case 128: return launch_bn<128, false>(pb, num_sms, stream);
-    default: return launch_bn<64, false>(pb, num_sms, stream);
+    case 256: return launch_bn<256, false, false>(pb, num_sms, stream);
+    case 128: return launch_bn<128, false, false>(pb, num_sms, stream);
+    default: return launch_bn<64, false, false>(pb, num_sms, stream);
   }
 }
 

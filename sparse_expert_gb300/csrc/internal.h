@@ -75,7 +75,7 @@ cudaError_t launch_pack_weights(const void* w_gate, const void* w_up, const void
 
 // ---- stage 4 expert GEMMs
 struct GroupedGemmProblem {
-  const void* a;           // [P, K] bf16 (x_perm or h)
+  const void* a;           // [P, K] bf16 (x_perm or h); with gather_rows: [a_rows, K] (x)
   const void* b;           // packed weights of this projection, [E * n_per_expert, K] bf16
   const int32_t* offsets;  // [E+1]
   const float* row_scale;  // [P] or null (down projection only)
@@ -87,6 +87,8 @@ struct GroupedGemmProblem {
   int out_cols;            // f or d
   int32_t* tile_counter;   // zeroed before launch
   int32_t* status;
+  const int32_t* gather_rows = nullptr;  // gate/up only: A row r is a[gather_rows[r]] (src_token)
+  int64_t a_rows = 0;                    // rows of a when gathering (T)
 };
 enum class Epilogue { kSwiGLU, kScale };
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
