@@ -25,7 +25,8 @@
  *     bit patterns (2 bytes each); they are typed void* here.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream) and returns without waiting for it.  Only
- *     moe_read_device_status and moe_forward_host synchronise.
+ *     moe_read_device_status, moe_forward_host and moe_forward_host_stream
+ *     synchronise.
  *   - Argument errors are found on the host and returned at once with no
  *     work enqueued.  Errors found by a kernel (a bounded wait that ran out,
  *     an out-of-range expert index) are written to a status word at the
@@ -479,6 +480,30 @@ MOE_API moe_status_t moe_forward_host(const void* x_host, const float* logits_ho
                               const void* packed, int64_t T, int32_t d, int32_t E, int32_t k,
                               int32_t f, int32_t renormalize,
                               void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_forward over a sequence of batches in HOST memory with the copies
+ * overlapped with compute: batch b+1's inputs are copied in on copy_in and
+ * batch b-1's output is copied out on copy_out while batch b runs on
+ * `stream`, through two device staging slots.
+ *   x_host[b] [T, d] bf16, logits_host[b] [T, E] fp32, out_host[b] [T, d]
+ *   bf16: host pointers of batch b, 0 <= b < n_batches (pinned for full
+ *   copy speed; a pointer may repeat);
+ *   x_dev[2], logits_dev[2], out_dev[2]: the two device slots, each sized
+ *   for one batch; workspace as moe_forward (shared by the batches, which
+ *   run in order on `stream`).
+ * stream, copy_in and copy_out must be three different streams.  Returns
+ * once every copy has completed.  Errors: as moe_forward, and
+ * MOE_ERR_INVALID_ARG for NULL arrays or pointers.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_forward_host_stream(const void* const* x_host, const float* const* logits_host,
+                                     void* const* out_host, int32_t n_batches,
+                                     void* const* x_dev, float* const* logits_dev,
+                                     void* const* out_dev, const void* packed, int64_t T,
+                                     int32_t d, int32_t E, int32_t k, int32_t f,
+                                     int32_t renormalize, void* workspace,
+                                     size_t workspace_bytes, moe_stream_t stream,
+                                     moe_stream_t copy_in, moe_stream_t copy_out);
 
 /* ------------------------------------------------------------------------
  * Reads the device status word at the start of a workspace used by

@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     moe_dispatch_workspace_bytes,
     moe_forward,
     moe_forward_host,
+    moe_forward_host_stream,
     moe_forward_layout,
     moe_forward_timed,
     moe_forward_routed,

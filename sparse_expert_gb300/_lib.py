@@ -75,6 +75,8 @@ SIGNATURES = {
     "moe_forward_gathered_timed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "moe_forward_host": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P]),
     "moe_read_device_status": (_S, [_P, _P, ctypes.POINTER(_I32)]),
+    "moe_forward_host_stream": (_S, [_P, _P, _P, _I32, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
+                                     _P, _P, _P]),
     "moe_grouped_gate_up_save": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_grouped_swiglu_backward": (_S, [_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                          _SZ, _P]),
@@ -508,6 +510,25 @@ def moe_forward_host(x_host, logits_host, out_host, x_dev, logits_dev, out_dev, 
                                 _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_forward_host")
     return out_host
+
+
+def moe_forward_host_stream(x_hosts, logits_hosts, out_hosts, x_dev, logits_dev, out_dev, packed, E, k, f,
+                            workspace, renormalize=True, stream=None, copy_in=None, copy_out=None):
+    """moe_forward over host batches with overlapped copies; *_dev are pairs of device slots."""
+    n = len(x_hosts)
+    T, d = x_hosts[0].shape
+    stream = stream if stream is not None else torch.cuda.current_stream()
+    copy_in = copy_in if copy_in is not None else torch.cuda.Stream()
+    copy_out = copy_out if copy_out is not None else torch.cuda.Stream()
+
+    def arr(ts):
+        return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    _check(lib.moe_forward_host_stream(arr(x_hosts), arr(logits_hosts), arr(out_hosts), n, arr(x_dev),
+                                       arr(logits_dev), arr(out_dev), _ptr(packed), T, d, E, k, f,
+                                       int(bool(renormalize)), _ptr(workspace), workspace.numel(), _stream(stream),
+                                       _stream(copy_in), _stream(copy_out)),
+           "moe_forward_host_stream")
+    return out_hosts
 
 
 def forward_intermediates(workspace, T, E, k, d, f):

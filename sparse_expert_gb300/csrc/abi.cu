@@ -714,6 +714,64 @@ moe_status_t moe_forward_host(const void* x_host, const float* logits_host, void
   return MOE_OK;
 }
 
+moe_status_t moe_forward_host_stream(const void* const* x_host, const float* const* logits_host,
+                                     void* const* out_host, int32_t n_batches, void* const* x_dev,
+                                     float* const* logits_dev, void* const* out_dev, const void* packed, int64_t T,
+                                     int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize,
+                                     void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                     moe_stream_t copy_in, moe_stream_t copy_out) {
+  moe_status_t s = check_routing(T, E, k);
+  if (s != MOE_OK) return s;
+  if (n_batches < 0) return fail(MOE_ERR_INVALID_ARG, "n_batches must be >= 0");
+  if (n_batches == 0 || T == 0) return MOE_OK;
+  if (!x_host || !logits_host || !out_host || !x_dev || !logits_dev || !out_dev)
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer array");
+  for (int b = 0; b < n_batches; ++b)
+    if (!x_host[b] || !logits_host[b] || !out_host[b]) return fail(MOE_ERR_INVALID_ARG, "NULL host pointer");
+  for (int i = 0; i < 2; ++i)
+    if (!x_dev[i] || !logits_dev[i] || !out_dev[i]) return fail(MOE_ERR_INVALID_ARG, "NULL device slot");
+  if (copy_in == stream || copy_out == stream || copy_in == copy_out)
+    return fail(MOE_ERR_INVALID_ARG, "stream, copy_in and copy_out must be three different streams");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStream_t ci = static_cast<cudaStream_t>(copy_in);
+  cudaStream_t co = static_cast<cudaStream_t>(copy_out);
+  const size_t xb = static_cast<size_t>(T) * d * 2, lb = static_cast<size_t>(T) * E * 4;
+  // per slot: inputs landed, compute done (slot inputs free, output ready), output copied (slot output free)
+  cudaEvent_t ev[3][2] = {};
+  moe_status_t result = MOE_OK;
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+    for (int j = 0; j < 2 && e == cudaSuccess; ++j) e = cudaEventCreateWithFlags(&ev[i][j], cudaEventDisableTiming);
+  for (int b = 0; b < n_batches && e == cudaSuccess && result == MOE_OK; ++b) {
+    const int sl = b & 1;
+    if (b >= 2) e = cudaStreamWaitEvent(ci, ev[1][sl], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(x_dev[sl], x_host[b], xb, cudaMemcpyHostToDevice, ci);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(logits_dev[sl], logits_host[b], lb, cudaMemcpyHostToDevice, ci);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[0][sl], ci);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[0][sl], 0);
+    if (e == cudaSuccess && b >= 2) e = cudaStreamWaitEvent(cs, ev[2][sl], 0);
+    if (e != cudaSuccess) break;
+    result = moe_forward(x_dev[sl], logits_dev[sl], packed, T, d, E, k, f, renormalize, out_dev[sl], nullptr, nullptr,
+                         workspace, workspace_bytes, stream);
+    if (result != MOE_OK) break;
+    e = cudaEventRecord(ev[1][sl], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(co, ev[1][sl], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(out_host[b], out_dev[sl], xb, cudaMemcpyDeviceToHost, co);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[2][sl], co);
+  }
+  // whatever was enqueued completes before the events go away
+  cudaError_t e2 = cudaStreamSynchronize(co);
+  if (e2 == cudaSuccess) e2 = cudaStreamSynchronize(cs);
+  if (e2 == cudaSuccess) e2 = cudaStreamSynchronize(ci);
+  for (int i = 0; i < 3; ++i)
+    for (int j = 0; j < 2; ++j)
+      if (ev[i][j]) cudaEventDestroy(ev[i][j]);
+  if (result != MOE_OK) return result;
+  if (e != cudaSuccess) return cuda_fail(e, "pipelined host forward");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "stream synchronize");
+  return MOE_OK;
+}
+
 size_t moe_backward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f) {
   if (T < 0 || E < 1 || k < 1 || d < 1 || f < 1) return 0;
   return backward_layout(T, E, k, d, f).total;

@@ -177,3 +177,25 @@ def test_gathered_forward_zero_tokens(moe):
     out = moe.moe_forward_gathered(torch.empty(0, d, dtype=torch.bfloat16, device="cuda"),
                                    torch.empty(0, E, device="cuda"), packed, E, k, f)
     assert out.shape == (0, d)
+
+
+def test_forward_host_stream_matches_device_forward(moe):
+    """Five batches from pinned host memory through the pipelined entry point
+    (copies on their own streams, two device slots) give, batch by batch,
+    the bit-identical outputs of moe_forward on device copies."""
+    cfg = workloads.get("small")
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
+    w = workloads.generate(cfg, seed=11, device="cuda")
+    packed = moe.moe_pack_weights(w["w_gate"], w["w_up"], w["w_down"])
+    batches = [workloads.generate(cfg, seed=20 + b, weights=False) for b in range(5)]
+    xh = [b["x"].pin_memory() for b in batches]
+    lh = [b["logits"].pin_memory() for b in batches]
+    oh = [torch.empty(T, d, dtype=torch.bfloat16).pin_memory() for _ in batches]
+    xd = [torch.empty(T, d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    ld = [torch.empty(T, E, dtype=torch.float32, device="cuda") for _ in range(2)]
+    od = [torch.empty(T, d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    ws = torch.empty(moe.moe_forward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device="cuda")
+    moe.moe_forward_host_stream(xh, lh, oh, xd, ld, od, packed, E, k, f, ws, cfg.renormalize)
+    for b in range(5):
+        ref = moe.moe_forward(batches[b]["x"].cuda(), batches[b]["logits"].cuda(), packed, E, k, f, cfg.renormalize)
+        assert torch.equal(oh[b], ref.cpu()), b
