@@ -510,6 +510,18 @@ MOE_API moe_status_t moe_forward_host_stream(const void* const* x_host, const fl
  * moe_dispatch_scan, moe_grouped_swiglu or moe_forward, after waiting for
  * `stream`.  *status receives MOE_OK or the first device error.
  * ---------------------------------------------------------------------- */
+/* ------------------------------------------------------------------------
+ * Check of the failure path every kernel shares: one block waits, with the
+ * same bounded helpers the kernels use, on an mbarrier phase that never
+ * completes, gives up after limit_ns (1 .. 2e9 ns, the kernels' own bound
+ * being 2 s) and writes MOE_ERR_TIMEOUT into the workspace status word
+ * (read it with moe_read_device_status); the context stays usable.
+ * Workspace: 256 bytes, 256-byte aligned.  Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_WORKSPACE, MOE_ERR_NO_DEVICE, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_ns,
+                                       moe_stream_t stream);
+
 MOE_API moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream,
                                     int32_t* status);
 

@@ -75,6 +75,7 @@ SIGNATURES = {
     "moe_forward_gathered_timed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "moe_forward_host": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P]),
     "moe_read_device_status": (_S, [_P, _P, ctypes.POINTER(_I32)]),
+    "moe_selftest_wait_timeout": (_S, [_P, _SZ, _I64, _P]),
     "moe_forward_host_stream": (_S, [_P, _P, _P, _I32, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
                                      _P, _P, _P]),
     "moe_grouped_gate_up_save": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -529,6 +530,12 @@ def moe_forward_host_stream(x_hosts, logits_hosts, out_hosts, x_dev, logits_dev,
                                        _stream(copy_in), _stream(copy_out)),
            "moe_forward_host_stream")
     return out_hosts
+
+
+def moe_selftest_wait_timeout(workspace, limit_ns, stream=None):
+    """Runs the bounded-wait check; read the status with moe_read_device_status."""
+    _check(lib.moe_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(limit_ns), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def forward_intermediates(workspace, T, E, k, d, f):

@@ -906,6 +906,22 @@ moe_status_t moe_backward_timed(const void* x, const float* logits, const void* 
                        workspace, workspace_bytes, stream, events);
 }
 
+moe_status_t moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_ns,
+                                       moe_stream_t stream) {
+  if (limit_ns < 1 || limit_ns > static_cast<int64_t>(kWaitLimitNs))
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns must be in [1, 2e9]");
+  if (!workspace || workspace_bytes < sizeof(WsHeader) || !aligned(workspace, kAlign))
+    return fail(MOE_ERR_WORKSPACE, "workspace needs 256 bytes, 256-byte aligned");
+  DeviceInfo dev;
+  moe_status_t s = device_info(&dev);
+  if (s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st), "workspace clear");
+  MOE_CUDA(launch_wait_timeout(&static_cast<WsHeader*>(workspace)->status, static_cast<uint64_t>(limit_ns), st),
+           "wait check launch");
+  return MOE_OK;
+}
+
 moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream, int32_t* status) {
   if (!workspace || !status) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   MOE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");

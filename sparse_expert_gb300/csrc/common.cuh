@@ -75,7 +75,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete.  Returns false when
 // the wait ran out or another role of the block has given up (*abort != 0).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -83,13 +84,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(a, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
 // Same, taken by a whole warp with a warp-uniform outcome (needed before
 // .sync.aligned instructions).
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_addr(bar);
   uint64_t t0 = 0;
   const int lane = threadIdx.x & 31;
@@ -99,7 +101,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
     if (__all_sync(0xffffffffu, ok)) return true;
     if ((it & 31u) == 31u) {
       int give_up = 0;
-      if (lane == 0) give_up = (*abort != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
+      if (lane == 0) give_up = (*abort != 0) || (global_timer_ns() - t0 > limit_ns);
       if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
     }
   }

@@ -127,6 +127,10 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
 bool make_bf16_map_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
 bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int box0, int box1);
 
+// Bounded-wait check: one block waits on a phase that never completes and
+// records a timeout in *status after limit_ns.
+cudaError_t launch_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
 // Device properties of the current device (cached per device).
 struct DeviceInfo {
   int device;

@@ -148,3 +148,10 @@ def test_gemm_and_forward_argument_errors():
 def test_valid_call_without_a_device_reports_no_device():
     assert lib.moe_route_topk(FAKE, 10, 8, 2, 1, FAKE, FAKE, NULL) == NO_DEVICE
     assert "device" in _last()
+
+
+def test_wait_check_argument_errors():
+    assert lib.moe_selftest_wait_timeout(FAKE, 256, 0, NULL) == INVALID
+    assert lib.moe_selftest_wait_timeout(FAKE, 256, 3_000_000_000, NULL) == INVALID
+    assert lib.moe_selftest_wait_timeout(NULL, 256, 1000, NULL) == WORKSPACE
+    assert lib.moe_selftest_wait_timeout(FAKE, 255, 1000, NULL) == WORKSPACE
