@@ -1,6 +1,6 @@
 /*
- * moe_gb300.h — C ABI of the single-GPU Mixture-of-Experts layer forward
- * (GB300, sm_103a).
+ * moe_gb300.h — C ABI of the single-GPU Mixture-of-Experts layer, forward
+ * and backward (GB300, sm_103a).
  *
  * The layer follows "Scalable Pretraining of Large MoE LMs on Aurora Super
  * Computer", §3.1 FastSparseMoE, Algorithm 1 (FastSparseMoEBlock), on one
@@ -12,9 +12,15 @@
  *            grouped gate/up GEMMs, Silu(gate)*up, grouped
  *            down GEMM                                    -> moe_grouped_swiglu
  *   stage 5  output reduction weighted by the TopK weights -> moe_combine
- * and moe_forward runs all of them.  Sizes follow the problem statement of
- * that section: T tokens of hidden size d, E routed experts, top-k, expert
- * hidden size f; P = T*k routed (token, slot) pairs.
+ * and moe_forward runs all of them (moe_forward_gathered without the
+ * permuted copy; moe_forward_routed from the tokens and the router weights;
+ * moe_forward_host / moe_forward_host_stream from host buffers).  The
+ * backward: stage 5 -> moe_combine_backward, stage 1 -> moe_route_backward,
+ * stage 4 -> moe_grouped_gate_up_save + moe_grouped_swiglu_backward, and
+ * moe_backward runs the whole layer backward with the forward recomputed.
+ * Sizes follow the problem statement of that section: T tokens of hidden
+ * size d, E routed experts, top-k, expert hidden size f; P = T*k routed
+ * (token, slot) pairs.
  *
  * Conventions shared by every entry point
  *   - Pointers are DEVICE memory owned by the caller unless a parameter says
