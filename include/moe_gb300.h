@@ -229,10 +229,10 @@ MOE_API moe_status_t moe_permute(const void* x, int64_t T, int32_t d, const int3
  *                projection with N tile BN and K = 64 * nkb sits at
  *                (((e * N/BN + n/BN) * nkb + k/64) * BN + n%BN) * 64 + k%64,
  *                so that one GEMM stage's weights are one contiguous block.
- *                Gate/up: N = 2f, K = d, BN = 2h (h = 128 if f % 128 == 0,
- *                else 64) and N tile t holds gate columns t*h .. t*h+h-1
- *                then the same up columns.  Down: N = d, K = f, BN = 256,
- *                128 or 64, the largest dividing d.
+ *                Gate/up: N = 2f, K = d, BN = 128, and N tile t holds
+ *                gate columns 64t .. 64t+63 then the same up columns.
+ *                Down: N = d, K = f, BN = 256, 128 or 64, the largest
+ *                dividing d.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 MOE_API size_t moe_packed_weight_bytes(int32_t E, int32_t d, int32_t f);
@@ -302,9 +302,8 @@ MOE_API moe_status_t moe_combine(const void* y, const int32_t* dest_row, const f
  * U = x_perm Wu[e] (bf16), which the backward reads:
  *   h  [P, f] bf16 out, Silu(G)*U as moe_grouped_swiglu writes it;
  *   gu [P, 2f] bf16 out, interleaved like the packed gate/up weights: for
- *      gate/up tile t (h_t = 128 if f % 128 == 0, else 64 columns),
- *      gu[r, 2*h_t*t + i] = G[r, h_t*t + i] and gu[r, 2*h_t*t + h_t + i] =
- *      U[r, h_t*t + i], 0 <= i < h_t.
+ *      gate/up tile t, gu[r, 128t + i] = G[r, 64t + i] and
+ *      gu[r, 128t + 64 + i] = U[r, 64t + i], 0 <= i < 64.
  * Other arguments and errors as moe_grouped_swiglu; workspace
  * moe_grouped_swiglu_workspace_bytes().
  * ---------------------------------------------------------------------- */

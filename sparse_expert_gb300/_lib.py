@@ -291,7 +291,7 @@ def moe_grouped_gate_up_save(x_perm, offsets, E, f, packed, workspace=None, stre
 
 def gu_split(gu, f):
     """(G [P,f], U [P,f]) from the interleaved [P,2f] layout (a view reshuffle, for checks)."""
-    h_t = 128 if f % 128 == 0 else 64
+    h_t = 64
     t = gu.reshape(gu.shape[0], f // h_t, 2, h_t)
     return t[:, :, 0, :].reshape(gu.shape[0], f), t[:, :, 1, :].reshape(gu.shape[0], f)
 

@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build", platform.machine())
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 SOURCES = ["abi.cu", "route.cu", "router.cu", "dispatch.cu", "dispatch_noalloc.cu", "permute_combine.cu", "pack.cu",
            "grouped_gemm.cu", "fp8.cu", "backward.cu", "tensor_map.cu", "grouped_gemm_bwd.cu",
-           "selftest.cu"]
+           "selftest.cu", "grouped_gemm_2sm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3,-Wall,-fvisibility=hidden", "--expt-relaxed-constexpr",
           "-I", os.path.join(ROOT, "include"), "-I", CSRC]

@@ -497,6 +497,10 @@ cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t st
 
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream) {
   if (pb.P == 0) return cudaSuccess;
+  // SM pairs with the weights as the 256-row operand where the weight rows
+  // per expert are a multiple of 256 (grouped_gemm_2sm.cu)
+  if (pb.gather_rows == nullptr && grouped_gemm_2sm_supported(pb, epi))
+    return launch_grouped_gemm_2sm(pb, epi, num_sms, stream);
   if (epi == Epilogue::kSwiGLU) {
     // N tile = matching gate and up halves of gate_up_half_tile(f) columns
     const bool wide = gate_up_tile_n(pb.out_cols) == 256;

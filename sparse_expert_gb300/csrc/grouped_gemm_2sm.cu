@@ -1,0 +1,694 @@
+// Grouped expert GEMMs of the forward on SM pairs (tcgen05 cta_group::2,
+// sm_103a), with the weights as the 256-row operand and the tokens as N.
+//
+// "Scalable Pretraining of Large MoE LMs on Aurora Super Computer", §3.1,
+// Algorithm 1, stage 4: gate_out/up_out = Grouped_mm(mlp_in, weight);
+// mul_out = Silu(gate_out) * up_out; mlp_out = Grouped_mm(mul_out,
+// down_weight), over expert-contiguous rows bounded by the cumulative
+// token counts.
+//
+// Each tile computes D^T = W_e[256 rows, K] x X_e[N tokens, K]^T on a pair
+// of SMs (a 2-CTA cluster) for up to 512 of the expert's tokens at once
+// (all of them at the 1T layer's ~341 per expert), so every weight tile is
+// read once per expert.  Per K step the leader issues tcgen05.mma M=256 with
+// N1 = min(N, 256) tokens and, when N > 256, a second one with the other
+// N2 = N - 256 into the next TMEM columns; N is the tile's token count
+// rounded up to 16.  CTA r holds 128 weight rows and, of each part, the
+// token rows r*N_part/2 .. +N_part/2 (128-row boxes).  The accumulator lands
+// in each CTA's TMEM as its 128 weight rows x N token columns.  Per SM this
+// takes in 8.3 KB of operands per MFLOP (a one-SM 128 x 256 tile: 11.4).
+// One accumulator: the epilogue drains a tile before the next one starts.
+//
+// Gate/up: a tile's 256 weight rows are two packed gate/up tiles of 64 gate
+// then the same 64 up columns, one per CTA, so TMEM lanes 0-63 of a CTA hold
+// gate features j..j+63 and lanes 64-127 the up features of the same j.  The
+// epilogue warps of lanes 0-31 and 64-95 (and 32-63 with 96-127) swap half
+// of their token columns through shared memory, form Silu(gate)*up in fp32,
+// and store H[token, j] in bf16.  Down: D^T rows are output features; the
+// epilogue scales each token column by its gate and stores Y[token, i].
+// Both transpose 32 x 32 chunks through shared memory so every global store
+// writes whole token-row segments.
+//
+// Roles in each CTA of the pair (320 threads): warp 0 TMA producer (both
+// CTAs load their halves; every copy signals the leader's stage barrier),
+// warp 1 MMA issuer (leader only; its commits are multicast to both CTAs),
+// warps 2-9 epilogue.  Tiles come from a shared atomic counter (dynamic
+// scheduling): the leader claims each tile and writes its id into both
+// CTAs' rings, over a flat order expert -> weight tile -> token tile
+// (consecutive tiles share a weight tile in L2; an expert's tokens stay in
+// L2 across its weight tiles).  Every wait is bounded; a CTA that gives up records a timeout,
+// and both CTAs meet at a cluster barrier before TMEM is released.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "gemm_common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int kTileN = 512;       // tokens per tile (both CTAs): up to two MMAs of N <= 256
+constexpr int kPartN = 256;       // N of one MMA
+constexpr int kHalfRows = 128;    // weight rows and token rows (per part) staged per CTA
+constexpr int kStages = 4;
+constexpr int kABytes = kHalfRows * BK * 2;
+constexpr int kBBytes = kHalfRows * BK * 2;          // one token part
+constexpr int kStageBytes = kABytes + 2 * kBBytes;   // A | B part 1 | B part 2
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kTmemCols = 512;    // one accumulator: the tile's weight rows x up to 512 tokens
+constexpr int kEpiBytes = kEpiWarps * 32 * 64;   // per epilogue warp 2 KB: SwiGLU exchange, then transpose
+constexpr int kRing = 4;                          // tile ids published ahead
+// readers of a ring slot, counted on the leader's rempty: the leader's MMA
+// thread and epilogue warps, the peer's producer and epilogue warps
+constexpr int kRingReaders = 2 + 2 * kEpiWarps;
+
+struct Params {
+  const int32_t* offsets;
+  const float* row_scale;  // down: gate of each row, or null
+  __nv_bfloat16* out;      // H [P, f] or Y [P, d]
+  __nv_bfloat16* gu;       // gate/up: also G, U [P, 2f] in the packed interleave, or null
+  int32_t* status;
+  int32_t* tile_counter;   // zeroed before launch
+  int E;
+  int K;
+  int m_tiles;         // 256-row weight tiles per expert
+  int a_tile_rows;     // rows of one packed weight tile (128 gate/up, 256 down)
+  int a_tiles;         // packed weight tiles per expert
+  int out_cols;        // f or d
+  int swiglu;
+};
+
+struct Smem {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t tfull[2], tempty[2];
+  uint64_t xsync[4];  // SwiGLU: one per pair of partner epilogue warps
+  uint64_t rfull[kRing], rempty[kRing];
+  int32_t ring[kRing];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the pair.
+__device__ __forceinline__ uint32_t pair_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t leader_addr(const void* p) { return pair_addr(p, 0); }
+
+__device__ __forceinline__ void st_cluster(uint32_t addr, int32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Waits on a barrier that the other CTA of the pair arrives on (acquire at
+// cluster scope), bounded like mbar_wait / mbar_wait_warp.
+__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t a = smem_addr(bar);
+  if (try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (try_wait_cluster(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ bool wait_cluster_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t a = smem_addr(bar);
+  uint64_t t0 = 0;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    const bool ok = try_wait_cluster(a, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((it & 31u) == 31u) {
+      int give_up = 0;
+      if (lane == 0) give_up = (*abort_flag != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory whose completion is counted
+// on a stage barrier of the leader CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* map, uint32_t bar, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* map, uint32_t bar, int32_t c0, int32_t c1,
+                                                 int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` in both CTAs of the pair once every MMA issued so far by
+// this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// Both partner warps arrive, then wait (bounded) for the phase to complete.
+__device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t& parity, volatile int* abort_flag) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait_warp(bar, parity, abort_flag);
+  parity ^= 1u;
+  return ok;
+}
+
+// Tile t: expert, weight tile, token tile.  s_pre[e] = tiles of experts
+// before e; an expert has m_tiles x ceil(rows / 256) tiles, token tile
+// fastest.
+struct Tile {
+  int e, mt, nt, tok0, valid, n;
+};
+
+// An expert's rows are split into ceil(rows / 256) near-equal token tiles
+// of S rows (a multiple of 16); returns the tile count and sets S.
+__host__ __device__ __forceinline__ int token_tiles(int rows, int& S) {
+  if (rows <= 0) {
+    S = 0;
+    return 0;
+  }
+  const int n0 = (rows + kTileN - 1) / kTileN;
+  S = (((rows + n0 - 1) / n0) + 15) & ~15;
+  return (rows + S - 1) / S;  // every tile holds at least one row
+}
+
+__device__ __forceinline__ Tile decode(int t, const int32_t* s_off, const int32_t* s_pre, int E, int m_tiles) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pre[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  Tile x;
+  x.e = lo;
+  const int rows = s_off[lo + 1] - s_off[lo];
+  int S;
+  const int ntt = token_tiles(rows, S);
+  const int local = t - s_pre[lo];
+  x.mt = local / ntt;
+  x.nt = local - x.mt * ntt;
+  x.tok0 = s_off[lo] + x.nt * S;
+  x.valid = min(S, rows - x.nt * S);
+  x.n = (x.valid + 15) & ~15;
+  (void)m_tiles;
+  return x;
+}
+
+// bf16 element (row t, column c) of a 32 x 32 chunk in a 2 KB buffer whose
+// 64-byte rows have their 16-byte pieces swizzled by (t >> 1) & 3.
+__device__ __forceinline__ int trans_off(int t, int c) {
+  return t * 64 + (((c >> 3) ^ ((t >> 1) & 3)) << 4) + ((c & 7) << 1);
+}
+
+// The warp holds column block j0 .. j0+31 (lane = column) of `rows` token
+// rows (vals[r] for token row r, bf16).  Writes them to out rows
+// row0 .. row0+rows-1 (row stride ld), rows >= valid skipped.
+template <int ROWS>
+__device__ __forceinline__ void store_transposed(const __nv_bfloat16 (&vals)[ROWS], uint8_t* buf, int lane,
+                                                 __nv_bfloat16* out, int64_t ld, int valid) {
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) *reinterpret_cast<__nv_bfloat16*>(buf + trans_off(r, lane)) = vals[r];
+  __syncwarp();
+  // ROWS rows of 64 bytes = ROWS * 4 pieces of 16 bytes over 32 lanes
+  constexpr int kPer = ROWS * 4 / 32;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int idx = i * 32 + lane;
+    const int r = idx >> 2;
+    const int p = idx & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 64 + ((p ^ ((r >> 1) & 3)) << 4));
+    if (r < valid) *reinterpret_cast<uint4*>(out + r * ld + p * 8) = v;
+  }
+  __syncwarp();
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                        const Params p) {
+  extern __shared__ __align__(1024) uint8_t dyn_smem[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_stage0 = base;  // stage s at s_stage0 + s * kStageBytes: A | B part 1 | B part 2
+  uint8_t* s_epi = s_stage0 + kStages * kStageBytes;
+  Smem* S = reinterpret_cast<Smem*>(s_epi + kEpiBytes);
+  int32_t* s_off = reinterpret_cast<int32_t*>(S + 1);
+  int32_t* s_pre = s_off + (p.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  volatile int* abort_flag = &S->abort;
+
+  if (warp == 0) {
+    int carry = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      int lo = 0, hi = 0;
+      if (e < p.E) {
+        lo = __ldg(p.offsets + e);
+        hi = __ldg(p.offsets + e + 1);
+        s_off[e] = lo;
+        if (e == p.E - 1) s_off[p.E] = hi;
+      }
+      int S;
+      int v = p.m_tiles * token_tiles(hi - lo, S);
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, s);
+        if (lane >= s) v += o;
+      }
+      if (e < p.E) s_pre[e + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_pre[0] = 0;
+  } else if (warp == 1) {
+    tmem_alloc_pair(&S->tmem_base, kTmemCols);
+  } else if (warp == 2 && lane == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&S->full[i], 1);
+      mbar_init(&S->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S->tfull[i], 1);
+      mbar_init(&S->tempty[i], 2 * kEpiWarps);  // both CTAs' epilogue warps (leader's copy is used)
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&S->xsync[i], 2);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&S->rfull[i], 1);
+      mbar_init(&S->rempty[i], kRingReaders);  // the leader's copy is used
+    }
+    mbar_init(&S->drain, 1);
+    S->abort = 0;
+    fence_barrier_init();
+  }
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+
+  const int total = s_pre[p.E];
+  const uint32_t tmem_base = S->tmem_base;
+  bool failed = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_w);
+      tma_prefetch_desc(&tm_x);
+      const int num_kb = p.K / BK;
+      int stage = 0;
+      uint32_t phase = 0;
+      int rs = 0;
+      uint32_t rphase = 0;
+      for (;;) {
+        // tiles come from a shared counter (dynamic scheduling): the leader
+        // claims one and publishes it in both CTAs' rings
+        int t;
+        if (rank == 0) {
+          if (!wait_cluster(&S->rempty[rs], rphase ^ 1u, abort_flag)) {
+            failed = true;
+            break;
+          }
+          t = atomicAdd(p.tile_counter, 1);
+          if (t >= total) t = -1;
+          S->ring[rs] = t;
+          st_cluster(pair_addr(&S->ring[rs], 1), t);
+          mbar_arrive(&S->rfull[rs]);
+          arrive_remote(pair_addr(&S->rfull[rs], 1));
+        } else {
+          if (!wait_cluster(&S->rfull[rs], rphase, abort_flag)) {
+            failed = true;
+            break;
+          }
+          t = S->ring[rs];
+          arrive_remote(leader_addr(&S->rempty[rs]));
+        }
+        if (++rs == kRing) {
+          rs = 0;
+          rphase ^= 1u;
+        }
+        if (t < 0) break;
+        const Tile x = decode(t, s_off, s_pre, p.E, p.m_tiles);
+        // this CTA's 128 weight rows: packed tile and row inside it
+        const int w0 = x.mt * 2 * kHalfRows + static_cast<int>(rank) * kHalfRows;
+        const int wblk = (x.e * p.a_tiles + w0 / p.a_tile_rows) * num_kb;
+        const int wrow = w0 % p.a_tile_rows;
+        // this CTA's token rows of each part
+        const int n1 = min(x.n, kPartN), n2 = x.n - n1;
+        const int xrow1 = x.tok0 + static_cast<int>(rank) * (n1 >> 1);
+        const int xrow2 = x.tok0 + n1 + static_cast<int>(rank) * (n2 >> 1);
+        const uint32_t bytes = 2 * (kABytes + kBBytes + (n2 > 0 ? kBBytes : 0));  // both CTAs
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&S->empty[stage], phase ^ 1u, abort_flag)) {
+            failed = true;
+            break;
+          }
+          const uint32_t lead_full = leader_addr(&S->full[stage]);
+          uint8_t* st = s_stage0 + stage * kStageBytes;
+          if (rank == 0) mbar_arrive_expect_tx(&S->full[stage], bytes);
+          tma_load_3d_pair(st, &tm_w, lead_full, 0, wrow, wblk + kb);
+          tma_load_2d_pair(st + kABytes, &tm_x, lead_full, kb * BK, xrow1);
+          if (n2 > 0) tma_load_2d_pair(st + kABytes + kBBytes, &tm_x, lead_full, kb * BK, xrow2);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (failed) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (rank == 0 && lane == 0) {
+      const int num_kb = p.K / BK;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t aphase = 0;
+      const uint32_t idesc0 = umma_idesc_bf16_f32(2 * kHalfRows, 16) & ~(0x3Fu << 17);
+      int rs = 0;
+      uint32_t rphase = 0;
+      for (;;) {
+        if (!wait_cluster(&S->rfull[rs], rphase, abort_flag)) {
+          failed = true;
+          break;
+        }
+        const int t = S->ring[rs];
+        arrive_remote(leader_addr(&S->rempty[rs]));
+        if (++rs == kRing) {
+          rs = 0;
+          rphase ^= 1u;
+        }
+        if (t < 0) break;
+        const Tile x = decode(t, s_off, s_pre, p.E, p.m_tiles);
+        const int n1 = min(x.n, kPartN), n2 = x.n - n1;
+        const uint32_t idesc1 = idesc0 | (static_cast<uint32_t>(n1 >> 3) << 17);
+        const uint32_t idesc2 = idesc0 | (static_cast<uint32_t>(max(n2, 16) >> 3) << 17);
+        // the epilogue has drained the previous tile
+        if (!wait_cluster(&S->tempty[0], aphase ^ 1u, abort_flag)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&S->full[stage], phase, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_addr(s_stage0 + stage * kStageBytes);
+          const uint32_t b1 = a0 + kABytes;
+          const uint32_t b2 = b1 + kBBytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t da = sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
+            const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
+            umma_pair(d_tmem, da, sw128_kmajor_desc(b1 + kk * UMMA_K * 2), idesc1, accumulate);
+            if (n2 > 0)
+              umma_pair(d_tmem + kPartN, da, sw128_kmajor_desc(b2 + kk * UMMA_K * 2), idesc2, accumulate);
+          }
+          umma_commit_pair(&S->empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (failed) break;
+        umma_commit_pair(&S->tfull[0]);
+        aphase ^= 1u;
+      }
+      umma_commit_pair(&S->drain);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quad = warp & 3;            // TMEM lanes 32*quad .. +31
+    const int half = (warp - 2) >> 2;     // first or second half of the tile's 32-token chunks
+    const int ew = warp - 2;
+    // one 2 KB buffer per warp: the SwiGLU exchange with the partner warp,
+    // then (the partner having read it) the transpose of the warp's stores
+    uint8_t* xbuf = s_epi + ew * 2048;
+    uint8_t* tbuf = xbuf;
+    const uint32_t lead_tempty = leader_addr(&S->tempty[0]);
+    uint32_t aphase = 0;
+    uint32_t xparity = 0;
+    int rs = 0;
+    uint32_t rphase = 0;
+    const uint32_t lead_rempty0 = leader_addr(&S->rempty[0]);
+    for (;;) {
+      if (!wait_cluster_warp(&S->rfull[rs], rphase, abort_flag)) {
+        failed = true;
+        break;
+      }
+      const int t = S->ring[rs];
+      __syncwarp();
+      if (lane == 0) arrive_remote(lead_rempty0 + rs * static_cast<uint32_t>(sizeof(uint64_t)));
+      if (++rs == kRing) {
+        rs = 0;
+        rphase ^= 1u;
+      }
+      if (t < 0) break;
+      const Tile x = decode(t, s_off, s_pre, p.E, p.m_tiles);
+      if (!mbar_wait_warp(&S->tfull[0], aphase, abort_flag)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+      // token columns 0 .. n-1 (TMEM columns 0..255 hold part 1, 256.. part 2)
+      const int chunks = (x.n + 31) >> 5;
+      const int c_begin = half == 0 ? 0 : ((chunks + 1) >> 1) * 32;
+      const int c_end = half == 0 ? min(((chunks + 1) >> 1) * 32, x.n) : x.n;
+      if (p.swiglu) {
+        // lanes of quads 0/1: gate features j0 + 32*(quad&1) + lane; quads
+        // 2/3: the up features of the same j.  The gate warp keeps token
+        // columns 0-15 of each chunk, the up warp 16-31.
+        const bool is_gate = quad < 2;
+        const int j = (x.mt * 2 + static_cast<int>(rank)) * 64 + (quad & 1) * 32 + lane;
+        // packed gate/up tile t = 2*mt + rank: TMEM lane l is interleaved
+        // column 128t + l of G,U (gate 64t.. then up 64t..)
+        __nv_bfloat16* gucol =
+            p.gu ? p.gu + static_cast<int64_t>(x.tok0) * 2 * p.out_cols + (x.mt * 2 + static_cast<int>(rank)) * 128 +
+                       quad * 32
+                 : nullptr;
+        uint64_t* xsync = &S->xsync[(quad & 1) + 2 * half];    // shared with the partner warp
+        uint8_t* my_x = xbuf;
+        uint8_t* partner_x = s_epi + (ew ^ 2) * 2048;           // quad ^ 2, same half
+        __nv_bfloat16* hcol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + (j - lane);
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32(taddr + c, v);
+          tmem_ld_wait();
+          if (gucol != nullptr) {  // the raw pre-activations, for the backward
+            __nv_bfloat16 gv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) gv[i] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            store_transposed<32>(gv, tbuf, lane, gucol + static_cast<int64_t>(c) * 2 * p.out_cols, 2 * p.out_cols,
+                                 x.valid - c);
+          }
+          // send the 16 columns the partner keeps
+          // (static indices on both sides of the select keep v in registers)
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 lo4 = make_uint4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            const uint4 hi4 = make_uint4(v[16 + 4 * q4], v[16 + 4 * q4 + 1], v[16 + 4 * q4 + 2], v[16 + 4 * q4 + 3]);
+            *reinterpret_cast<uint4*>(my_x + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4)) = is_gate ? hi4 : lo4;
+          }
+          if (!pair_sync(xsync, xparity, abort_flag)) {
+            failed = true;
+            break;
+          }
+          const int keep0 = is_gate ? 0 : 16;
+          float g[16], u[16];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 r = *reinterpret_cast<const uint4*>(partner_x + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4));
+            const float o[4] = {__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float mine = __uint_as_float(is_gate ? v[4 * q4 + i] : v[16 + 4 * q4 + i]);
+              g[4 * q4 + i] = is_gate ? mine : o[i];
+              u[4 * q4 + i] = is_gate ? o[i] : mine;
+            }
+          }
+          if (!pair_sync(xsync, xparity, abort_flag)) {  // the partner has read my buffer
+            failed = true;
+            break;
+          }
+          __nv_bfloat16 hv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hv[i] = __float2bfloat16_rn(silu_f32(g[i]) * u[i]);
+          const int r0 = c + keep0;  // first token column of my 16
+          store_transposed<16>(hv, tbuf, lane, hcol + static_cast<int64_t>(r0) * p.out_cols, p.out_cols,
+                               x.valid - r0);
+        }
+      } else {
+        // lanes: output features i0 + lane; columns: tokens
+        const int i0 = x.mt * 2 * kHalfRows + static_cast<int>(rank) * kHalfRows + quad * 32;
+        __nv_bfloat16* ycol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + i0;
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32(taddr + c, v);
+          tmem_ld_wait();
+          __nv_bfloat16 yv[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int tok = c + i;
+            const float s =
+                (p.row_scale != nullptr && tok < x.valid) ? __ldg(p.row_scale + x.tok0 + tok) : 1.0f;
+            yv[i] = __float2bfloat16_rn(s * __uint_as_float(v[i]));
+          }
+          store_transposed<32>(yv, tbuf, lane, ycol + static_cast<int64_t>(c) * p.out_cols, p.out_cols,
+                               x.valid - c);
+        }
+      }
+      if (failed) break;
+      // this warp is done with the accumulator: tell the leader
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) arrive_remote(lead_tempty);
+      aphase ^= 1u;
+    }
+  }
+
+  if (failed && lane == 0) {
+    record_status(p.status, kStatusTimeout);
+    *abort_flag = 1;
+  }
+  // every MMA of the pair has completed once drain flips (the leader issued
+  // them all); then let copies that a failed peer may still have in flight
+  // land before the pair meets and frees its TMEM
+  if (warp == 1) {
+    if (lane == 0) {
+      volatile int never = 0;
+      mbar_wait(&S->drain, 0, &never);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (*abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 10000000ull) __nanosleep(1000);
+  }
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+bool grouped_gemm_2sm_supported(const GroupedGemmProblem& pb, Epilogue epi) {
+  if (epi == Epilogue::kSwiGLU) return pb.out_cols % 128 == 0 && gate_up_half_tile(pb.out_cols) == 64;
+  return pb.out_cols % 256 == 0 && down_tile_n(pb.out_cols) == 256;
+}
+
+size_t grouped_gemm_2sm_smem(int E) {
+  return 1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiBytes + sizeof(Smem) +
+         2 * static_cast<size_t>(E + 1) * sizeof(int32_t);
+}
+
+cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream) {
+  if (pb.P == 0) return cudaSuccess;
+  if (!grouped_gemm_2sm_supported(pb, epi)) return cudaErrorNotSupported;
+  const bool swiglu = epi == Epilogue::kSwiGLU;
+  const int a_tile_rows = swiglu ? gate_up_tile_n(pb.out_cols) : down_tile_n(pb.out_cols);
+  const int n_rows = pb.n_per_expert;  // weight rows per expert (2f or d)
+  const int num_kb = pb.K / BK;
+  CUtensorMap mw, mx;
+  const int64_t blocks = static_cast<int64_t>(pb.E) * (n_rows / a_tile_rows) * num_kb;
+  if (!make_bf16_map_3d(&mw, pb.b, BK, a_tile_rows, blocks, BK, kHalfRows)) return cudaErrorInvalidValue;
+  if (!make_bf16_map_2d(&mx, pb.a, pb.P, pb.K, BK, kHalfRows)) return cudaErrorInvalidValue;
+  Params prm;
+  prm.offsets = pb.offsets;
+  prm.row_scale = swiglu ? nullptr : pb.row_scale;
+  prm.out = static_cast<__nv_bfloat16*>(pb.out);
+  prm.gu = swiglu ? static_cast<__nv_bfloat16*>(pb.gu_out) : nullptr;
+  prm.status = pb.status;
+  prm.tile_counter = pb.tile_counter;
+  prm.E = pb.E;
+  prm.K = pb.K;
+  prm.m_tiles = n_rows / (2 * kHalfRows);
+  prm.a_tile_rows = a_tile_rows;
+  prm.a_tiles = n_rows / a_tile_rows;
+  prm.out_cols = pb.out_cols;
+  prm.swiglu = swiglu ? 1 : 0;
+  const size_t smem = grouped_gemm_2sm_smem(pb.E);
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  // persistent: one pair per two SMs, never more pairs than an upper bound on tiles
+  const int64_t max_tiles = (pb.P / kTileN + pb.E) * static_cast<int64_t>(prm.m_tiles);
+  int pairs = num_sms / 2;
+  if (max_tiles < pairs) pairs = static_cast<int>(max_tiles);
+  grouped_gemm_2sm_kernel<<<2 * pairs, kThreads, smem, stream>>>(mw, mx, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

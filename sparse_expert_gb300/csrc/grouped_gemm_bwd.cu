@@ -552,6 +552,14 @@ Params base_params(const int32_t* offsets, int E, int32_t* counter, int32_t* sta
 
 cudaError_t launch_gate_up_save(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream) {
   if (a.P == 0) return cudaSuccess;
+  {
+    // the forward's paired-SM GEMM writes G and U beside H where it applies
+    GroupedGemmProblem g{a.x_perm, a.w_gate_up, a.offsets, nullptr, a.h, a.P, a.E, a.d, 2 * a.f, a.f,
+                         a.counters + 0, a.status};
+    g.gu_out = a.gu;
+    if (grouped_gemm_2sm_supported(g, Epilogue::kSwiGLU)) return launch_grouped_gemm_2sm(g, Epilogue::kSwiGLU, num_sms,
+                                                                                           stream);
+  }
   const int bn = gate_up_tile_n(a.f);
   CUtensorMap ma, mb;
   if (!make_bf16_map_2d(&ma, a.x_perm, a.P, a.d, BK, BM)) return cudaErrorInvalidValue;
@@ -645,7 +653,7 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
   if ((err = mark(2)) != cudaSuccess) return err;
   // dWg[e] = X_e^T dG_e, dWu[e] = X_e^T dU_e: M = d, N = 2f interleaved
   if (a.dw_gate) {
-    const int bn = bn_gu;
+    const int bn = tile_n_for(2 * a.f);  // may span two interleaved gate/up tiles
     CUtensorMap ma, mb;
     const int64_t rows = a.P > 0 ? a.P : 1;
     if (!make_bf16_map_2d(&ma, a.P > 0 ? a.x_perm : a.dw_gate, rows, a.d, 64, BK)) return cudaErrorInvalidValue;

@@ -88,10 +88,16 @@ struct GroupedGemmProblem {
   int32_t* tile_counter;   // zeroed before launch
   int32_t* status;
   const int32_t* gather_rows = nullptr;  // gate/up only: A row r is a[gather_rows[r]] (src_token)
+  void* gu_out = nullptr;                // gate/up, paired form only: also store G, U [P, 2f]
   int64_t a_rows = 0;                    // rows of a when gathering (T)
 };
 enum class Epilogue { kSwiGLU, kScale };
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
+// The paired-SM form (weights as the 256-row operand, up to 512 of an
+// expert's tokens as N): used by launch_grouped_gemm when the weight rows
+// per expert (2f, or d) are a multiple of 256.
+bool grouped_gemm_2sm_supported(const GroupedGemmProblem& pb, Epilogue epi);
+cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
 
 // ---- stage 4 backward: expert GEMMs of the backward pass
 struct BackwardGemmArgs {

@@ -21,7 +21,9 @@
 
 namespace moe {
 
-int gate_up_half_tile(int f) { return (f % 128 == 0) ? 128 : 64; }
+// 64 gate then 64 up columns per packed tile: a 256-row tile of the paired
+// GEMM is two packed tiles, one per SM, each holding matching gate and up rows
+int gate_up_half_tile(int f) { (void)f; return 64; }
 int gate_up_tile_n(int f) { return 2 * gate_up_half_tile(f); }
 int down_tile_n(int d) { return d % 256 == 0 ? 256 : d % 128 == 0 ? 128 : 64; }
 

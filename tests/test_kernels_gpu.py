@@ -172,7 +172,7 @@ def test_pack_layout(moe, E, d, f):
     wu = torch.randn(E, d, f, generator=g).to(torch.bfloat16)
     wd = torch.randn(E, f, d, generator=g).to(torch.bfloat16)
     packed = moe.moe_pack_weights(wg.cuda(), wu.cuda(), wd.cuda()).cpu()
-    h = 128 if f % 128 == 0 else 64
+    h = 64
     # gate/up: N tiles of [h gate columns | the same h up columns], each a row of K = d weights
     gt = wg.transpose(1, 2).reshape(E, f // h, h, d)
     ut = wu.transpose(1, 2).reshape(E, f // h, h, d)
