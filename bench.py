@@ -37,7 +37,7 @@ METRIC = "MoE-layer fwd tokens/s and grouped-GEMM TFLOP/s (% bf16 peak); permute
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS_PER_STEP = 6  # route, index, permute, gate/up GEMM, down GEMM, combine
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
-GEMM_SOURCE = os.path.join(ROOT, "sparse_expert_gb300", "csrc", "grouped_gemm.cu")
+GEMM_SOURCE = os.path.join(ROOT, "sparse_expert_gb300", "csrc", "grouped_gemm_2sm.cu")
 
 
 # ----------------------------------------------------------- distributed
@@ -294,7 +294,7 @@ def gpu_arm(args):
     dominant = max(("gate_up", "down"), key=lambda n: stage_ms[n])
     achieved = work[dominant]["flops"] / (stage_ms[dominant] * 1e-3) / 1e12
     traffic = recorded_traffic(args.workload) if dominant == "gate_up" else None
-    roofline = {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({dominant})", "achieved": round(achieved, 2),
+    roofline = {"bound": "tensor", "kernel": f"grouped_gemm_2sm_kernel ({dominant})", "achieved": round(achieved, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "traffic": traffic, "peak_source": f"bf16 dense burst, {peaks['source']}"}
 
