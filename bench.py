@@ -172,7 +172,7 @@ def stage_work(cfg):
         "permute": {"bytes": T * d * 2 + P * d * 2 + P * 4},
         "gate_up": {"flops": 4 * P * d * f},
         "down": {"flops": 2 * P * d * f},
-        "combine": {"bytes": P * d * 2 + T * d * 2 + P * 4},
+        "combine": {"bytes": P * d * 2 + T * d * 2 + P * 4 + P * 4},   # rows, out, dest_row, gates
     }
 
 

@@ -369,7 +369,9 @@ MOE_API moe_status_t moe_route_backward(const float* logits, const int32_t* topk
 /* ------------------------------------------------------------------------
  * The whole layer forward (Algorithm 1, stages 1-5) on one stream, with no
  * host synchronisation: route + histogram, look-back index pass, permute,
- * gate/up GEMM with SwiGLU, down GEMM scaled by each row's gate, combine.
+ * gate/up GEMM with SwiGLU, down GEMM (rows left ungated), combine weighted
+ * by the TopK weights.  The layout's y therefore holds each routed row's
+ * expert output before its gate; row_w still holds the gate of every row.
  *   x [T, d] bf16; logits [T, E] fp32; packed from moe_pack_weights;
  *   out [T, d] bf16 out; topk_idx_out [T, k] int32 and topk_w_out [T, k]
  *   fp32 out, optional (the workspace keeps its own copy).

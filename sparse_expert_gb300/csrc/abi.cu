@@ -636,11 +636,13 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* router
   }
   MOE_CUDA(launch_grouped_gemm(g1, Epilogue::kSwiGLU, dev.num_sms, st), "gate/up GEMM launch");
   MOE_CUDA(mark(4), "event record");
-  GroupedGemmProblem g2{h, wdn, offsets, row_w, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
+  // the down GEMM leaves its rows ungated: the gates enter in the output
+  // reduction, where they cost no extra memory traffic
+  GroupedGemmProblem g2{h, wdn, offsets, nullptr, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
   MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
   MOE_CUDA(mark(5), "event record");
-  // stage 5 (rows already carry their gate)
-  MOE_CUDA(launch_combine(y, dest_row, nullptr, T, k, d, out, dev.num_sms, st), "combine launch");
+  // stage 5: each token sums its k rows weighted by its TopK weights
+  MOE_CUDA(launch_combine(y, dest_row, topk_w, T, k, d, out, dev.num_sms, st), "combine launch");
   MOE_CUDA(mark(6), "event record");
   return MOE_OK;
 }

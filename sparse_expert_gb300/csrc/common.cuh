@@ -266,6 +266,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+// z * sigmoid(z) with the hardware reciprocal (__fdividef, 2 ulp): for
+// z < -87 the denominator overflows the divide's range and the result is 0,
+// which is also the bf16 value of the true product there.
+__device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 }  // namespace moe

@@ -32,7 +32,8 @@
 // Roles in each CTA of the pair (320 threads): warp 0 TMA producer (both
 // CTAs load their halves; every copy signals the leader's stage barrier),
 // warp 1 MMA issuer (leader only; its commits are multicast to both CTAs),
-// warps 2-9 epilogue.  Tiles come from a shared atomic counter (dynamic
+// warps 2-9 epilogue, two per TMEM lane quadrant, each draining half of the
+// tile's token chunks.  Tiles come from a shared atomic counter (dynamic
 // scheduling): the leader claims each tile and writes its id into both
 // CTAs' rings, over a flat order expert -> weight tile -> token tile
 // (consecutive tiles share a weight tile in L2; an expert's tokens stay in
@@ -43,6 +44,7 @@
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "internal.h"
+#include "moe_gb300.h"
 
 namespace moe {
 namespace {
@@ -56,7 +58,8 @@ constexpr int kStages = 4;
 constexpr int kABytes = kHalfRows * BK * 2;
 constexpr int kBBytes = kHalfRows * BK * 2;          // one token part
 constexpr int kStageBytes = kABytes + 2 * kBBytes;   // A | B part 1 | B part 2
-constexpr int kEpiWarps = 8;
+constexpr int kEpiParts = 2;     // epilogue warps per TMEM lane quadrant, each a share of the token chunks
+constexpr int kEpiWarps = 4 * kEpiParts;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;    // one accumulator: the tile's weight rows x up to 512 tokens
 constexpr int kEpiBytes = kEpiWarps * 32 * 64;   // per epilogue warp 2 KB: SwiGLU exchange, then transpose
@@ -84,7 +87,7 @@ struct Params {
 struct Smem {
   uint64_t full[kStages], empty[kStages];
   uint64_t tfull[2], tempty[2];
-  uint64_t xsync[4];  // SwiGLU: one per pair of partner epilogue warps
+  uint64_t xsync[2 * kEpiParts];  // SwiGLU: one per pair of partner epilogue warps
   uint64_t rfull[kRing], rempty[kRing];
   int32_t ring[kRing];
   uint64_t drain;
@@ -338,7 +341,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       mbar_init(&S->tfull[i], 1);
       mbar_init(&S->tempty[i], 2 * kEpiWarps);  // both CTAs' epilogue warps (leader's copy is used)
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&S->xsync[i], 2);
+    for (int i = 0; i < 2 * kEpiParts; ++i) mbar_init(&S->xsync[i], 2);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&S->rfull[i], 1);
       mbar_init(&S->rempty[i], kRingReaders);  // the leader's copy is used
@@ -487,7 +490,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
   } else {
     // ---------------------------------------------------------- epilogue
     const int quad = warp & 3;            // TMEM lanes 32*quad .. +31
-    const int half = (warp - 2) >> 2;     // first or second half of the tile's 32-token chunks
+    const int part = (warp - 2) >> 2;     // which share of the tile's 32-token chunks
     const int ew = warp - 2;
     // one 2 KB buffer per warp: the SwiGLU exchange with the partner warp,
     // then (the partner having read it) the transpose of the warp's stores
@@ -521,8 +524,16 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
       // token columns 0 .. n-1 (TMEM columns 0..255 hold part 1, 256.. part 2)
       const int chunks = (x.n + 31) >> 5;
-      const int c_begin = half == 0 ? 0 : ((chunks + 1) >> 1) * 32;
-      const int c_end = half == 0 ? min(((chunks + 1) >> 1) * 32, x.n) : x.n;
+      const int per = (chunks + kEpiParts - 1) / kEpiParts;
+      const int c_begin = part * per * 32;
+      const int c_end = min((part + 1) * per * 32, x.n);
+      // v holds chunk c; the load of chunk c + 32 is issued as soon as v has
+      // been consumed, so it overlaps the stores of chunk c
+      uint32_t v[32];
+      if (c_begin < c_end) {
+        tmem_ld_32x32(taddr + c_begin, v);
+        tmem_ld_wait();
+      }
       if (p.swiglu) {
         // lanes of quads 0/1: gate features j0 + 32*(quad&1) + lane; quads
         // 2/3: the up features of the same j.  The gate warp keeps token
@@ -535,15 +546,12 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             p.gu ? p.gu + static_cast<int64_t>(x.tok0) * 2 * p.out_cols + (x.mt * 2 + static_cast<int>(rank)) * 128 +
                        quad * 32
                  : nullptr;
-        uint64_t* xsync = &S->xsync[(quad & 1) + 2 * half];    // shared with the partner warp
+        uint64_t* xsync = &S->xsync[(quad & 1) + 2 * part];    // shared with the partner warp
         uint8_t* my_x = xbuf;
-        uint8_t* partner_x = s_epi + (ew ^ 2) * 2048;           // quad ^ 2, same half
+        uint8_t* partner_x = s_epi + (ew ^ 2) * 2048;           // quad ^ 2, same part
         __nv_bfloat16* hcol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + (j - lane);
 #pragma unroll 1
         for (int c = c_begin; c < c_end; c += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32(taddr + c, v);
-          tmem_ld_wait();
           if (gucol != nullptr) {  // the raw pre-activations, for the backward
             __nv_bfloat16 gv[32];
 #pragma unroll
@@ -576,7 +584,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
               u[4 * q4 + i] = is_gate ? o[i] : mine;
             }
           }
+          if (c + 32 < c_end) tmem_ld_32x32(taddr + c + 32, v);
           if (!pair_sync(xsync, xparity, abort_flag)) {  // the partner has read my buffer
+            tmem_ld_wait();
             failed = true;
             break;
           }
@@ -586,6 +596,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           const int r0 = c + keep0;  // first token column of my 16
           store_transposed<16>(hv, tbuf, lane, hcol + static_cast<int64_t>(r0) * p.out_cols, p.out_cols,
                                x.valid - r0);
+          if (c + 32 < c_end) tmem_ld_wait();
         }
       } else {
         // lanes: output features i0 + lane; columns: tokens
@@ -593,19 +604,21 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         __nv_bfloat16* ycol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + i0;
 #pragma unroll 1
         for (int c = c_begin; c < c_end; c += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32(taddr + c, v);
-          tmem_ld_wait();
           __nv_bfloat16 yv[32];
+          if (p.row_scale != nullptr) {
+            // lane i loads the gate of token column c + i; every lane takes all 32
+            const float s_l = c + lane < x.valid ? __ldg(p.row_scale + x.tok0 + c + lane) : 1.0f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int tok = c + i;
-            const float s =
-                (p.row_scale != nullptr && tok < x.valid) ? __ldg(p.row_scale + x.tok0 + tok) : 1.0f;
-            yv[i] = __float2bfloat16_rn(s * __uint_as_float(v[i]));
+            for (int i = 0; i < 32; ++i)
+              yv[i] = __float2bfloat16_rn(__shfl_sync(0xffffffffu, s_l, i) * __uint_as_float(v[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) yv[i] = __float2bfloat16_rn(__uint_as_float(v[i]));
           }
+          if (c + 32 < c_end) tmem_ld_32x32(taddr + c + 32, v);
           store_transposed<32>(yv, tbuf, lane, ycol + static_cast<int64_t>(c) * p.out_cols, p.out_cols,
                                x.valid - c);
+          if (c + 32 < c_end) tmem_ld_wait();
         }
       }
       if (failed) break;
@@ -648,6 +661,11 @@ bool grouped_gemm_2sm_supported(const GroupedGemmProblem& pb, Epilogue epi) {
   if (epi == Epilogue::kSwiGLU) return pb.out_cols % 128 == 0 && gate_up_half_tile(pb.out_cols) == 64;
   return pb.out_cols % 256 == 0 && down_tile_n(pb.out_cols) == 256;
 }
+
+// the largest expert count the library takes still fits the opt-in 227 KB
+static_assert(1024 + kStages * kStageBytes + kEpiBytes + sizeof(Smem) + 2 * (MOE_MAX_EXPERTS + 1) * sizeof(int32_t) <=
+                  227 * 1024,
+              "shared memory of the paired GEMM at MOE_MAX_EXPERTS");
 
 size_t grouped_gemm_2sm_smem(int E) {
   return 1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiBytes + sizeof(Smem) +

@@ -55,7 +55,7 @@ def test_stage_work_of_the_1t_layer():
     assert w["gate_up"]["flops"] == 4 * P * 6144 * 1792 == 5_772_436_045_824
     assert w["down"]["flops"] == 2 * P * 6144 * 1792
     assert w["permute"]["bytes"] == 16384 * 6144 * 2 + P * 6144 * 2 + P * 4
-    assert w["combine"]["bytes"] == P * 6144 * 2 + 16384 * 6144 * 2 + P * 4
+    assert w["combine"]["bytes"] == P * 6144 * 2 + 16384 * 6144 * 2 + P * 8   # rows, out, dest_row, gates
     assert bench.weight_bytes_read(cfg, [1] * 384) == 384 * 3 * 6144 * 1792 * 2
 
 
