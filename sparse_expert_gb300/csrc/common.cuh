@@ -210,6 +210,30 @@ __device__ __forceinline__ void tmem_ld_32x32(uint32_t taddr, uint32_t (&r)[32])
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 16 TMEM lanes x 32 consecutive 32-bit columns (four 16x256b blocks).
+// Thread i gets lanes base + i/4 and base + 8 + i/4: r[4g] and r[4g + 1] are
+// columns 8g + 2(i%4) and 8g + 2(i%4) + 1 of the first lane, r[4g + 2] and
+// r[4g + 3] the same columns of the second.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Four 8 x 8 bf16 matrices stored transposed: thread i holds in p_m the
+// elements (row i/4, columns 2(i%4) and 2(i%4) + 1, low half first) of
+// matrix m and gives the shared address of stored row i%8 of matrix i/8;
+// stored row j of a matrix is its column j (16 bytes).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t p0, uint32_t p1, uint32_t p2,
+                                                  uint32_t p3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(p0),
+               "r"(p1), "r"(p2), "r"(p3)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
 // 128-byte swizzling: rows of 128 bytes, 8-row swizzle atoms of 1024 bytes
 // stacked along M/N.  Fields: start address >> 4 (bits 0-13), leading byte

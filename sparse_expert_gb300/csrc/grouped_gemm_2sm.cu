@@ -163,6 +163,14 @@ __device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Same without release semantics: the arrive does not wait for this
+// thread's earlier global stores to become visible.  Used where the waiter
+// consumes no memory this thread wrote (the accumulator hand-back: the TMEM
+// loads have completed at tcgen05.wait::ld).
+__device__ __forceinline__ void arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // 2-D tiled load into this CTA's shared memory whose completion is counted
 // on a stage barrier of the leader CTA (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* map, uint32_t bar, int32_t c0, int32_t c1) {
@@ -264,32 +272,51 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* s_off, const int32_
   return x;
 }
 
-// bf16 element (row t, column c) of a 32 x 32 chunk in a 2 KB buffer whose
-// 64-byte rows have their 16-byte pieces swizzled by (t >> 1) & 3.
-__device__ __forceinline__ int trans_off(int t, int c) {
-  return t * 64 + (((c >> 3) ^ ((t >> 1) & 3)) << 4) + ((c & 7) << 1);
+// A warp's token-row staging buffer: up to 32 token rows of 64 bytes (the
+// warp's 32 bf16 features), the 16-byte pieces of row t swizzled by
+// (t >> 1) & 3 so that the stmatrix writes and the 16-byte row reads are
+// both free of bank conflicts.
+//
+// p[4g + m] holds features 8m .. 8m+7 of tokens 8g .. 8g+7 as an stmatrix
+// fragment: thread i has feature 8m + i/4 of tokens 8g + 2(i%4) and +1,
+// packed low/high -- which is what packing the columns of a 16x256b TMEM
+// load (features = TMEM lanes, tokens = TMEM columns) pairwise gives.
+template <int G>
+__device__ __forceinline__ void stage_rows(const uint32_t (&p)[4 * G], uint8_t* buf, int lane) {
+  const uint32_t a0 = smem_addr(buf) + (lane & 7) * 64 + ((((lane >> 3) ^ (lane >> 1)) & 3) << 4);
+#pragma unroll
+  for (int g = 0; g < G; ++g) stmatrix_x4_trans(a0 + g * 512, p[4 * g], p[4 * g + 1], p[4 * g + 2], p[4 * g + 3]);
+  __syncwarp();
 }
 
-// The warp holds column block j0 .. j0+31 (lane = column) of `rows` token
-// rows (vals[r] for token row r, bf16).  Writes them to out rows
-// row0 .. row0+rows-1 (row stride ld), rows >= valid skipped.
+// Rows 0 .. ROWS-1 of the staging buffer to out rows 0 .. ROWS-1 (row
+// stride ld), rows >= valid skipped: each 16-byte store instruction covers
+// 8 rows x 64 contiguous bytes.
 template <int ROWS>
-__device__ __forceinline__ void store_transposed(const __nv_bfloat16 (&vals)[ROWS], uint8_t* buf, int lane,
-                                                 __nv_bfloat16* out, int64_t ld, int valid) {
-#pragma unroll
-  for (int r = 0; r < ROWS; ++r) *reinterpret_cast<__nv_bfloat16*>(buf + trans_off(r, lane)) = vals[r];
-  __syncwarp();
-  // ROWS rows of 64 bytes = ROWS * 4 pieces of 16 bytes over 32 lanes
+__device__ __forceinline__ void rows_to_global(const uint8_t* buf, int lane, __nv_bfloat16* out, int64_t ld,
+                                               int valid) {
   constexpr int kPer = ROWS * 4 / 32;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int idx = i * 32 + lane;
     const int r = idx >> 2;
-    const int p = idx & 3;
-    const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 64 + ((p ^ ((r >> 1) & 3)) << 4));
-    if (r < valid) *reinterpret_cast<uint4*>(out + r * ld + p * 8) = v;
+    const int q = idx & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+    if (r < valid) *reinterpret_cast<uint4*>(out + r * ld + q * 8) = v;
   }
   __syncwarp();
+}
+
+// The fragment of a 32-feature x 32-token chunk from its two 16x256b loads
+// (a: features 0-15, b: 16-31), rounded to bf16.
+__device__ __forceinline__ void pack_chunk(const uint32_t (&a)[16], const uint32_t (&b)[16], uint32_t (&p)[16]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    p[4 * g] = pack_bf16x2(__uint_as_float(a[4 * g]), __uint_as_float(a[4 * g + 1]));
+    p[4 * g + 1] = pack_bf16x2(__uint_as_float(a[4 * g + 2]), __uint_as_float(a[4 * g + 3]));
+    p[4 * g + 2] = pack_bf16x2(__uint_as_float(b[4 * g]), __uint_as_float(b[4 * g + 1]));
+    p[4 * g + 3] = pack_bf16x2(__uint_as_float(b[4 * g + 2]), __uint_as_float(b[4 * g + 3]));
+  }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -527,11 +554,23 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       const int per = (chunks + kEpiParts - 1) / kEpiParts;
       const int c_begin = part * per * 32;
       const int c_end = min((part + 1) * per * 32, x.n);
-      // v holds chunk c; the load of chunk c + 32 is issued as soon as v has
-      // been consumed, so it overlaps the stores of chunk c
-      uint32_t v[32];
+      // a, b hold chunk c (TMEM lanes 0-15 and 16-31 of the warp); the load
+      // of chunk c + 32 is issued as soon as they have been consumed, so it
+      // overlaps the stores of chunk c
+      const uint32_t taddr_b = taddr + (16u << 16);
+      // the accumulator goes back to the MMA as soon as the warp's last TMEM
+      // load has landed, before that chunk's math and stores
+      bool released = false;
+      auto release = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) arrive_remote_relaxed(lead_tempty);
+        released = true;
+      };
+      uint32_t a[16], b[16];
       if (c_begin < c_end) {
-        tmem_ld_32x32(taddr + c_begin, v);
+        tmem_ld_16x256b_x4(taddr + c_begin, a);
+        tmem_ld_16x256b_x4(taddr_b + c_begin, b);
         tmem_ld_wait();
       }
       if (p.swiglu) {
@@ -552,26 +591,32 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         __nv_bfloat16* hcol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + (j - lane);
 #pragma unroll 1
         for (int c = c_begin; c < c_end; c += 32) {
+          if (c + 32 >= c_end) release();
           if (gucol != nullptr) {  // the raw pre-activations, for the backward
-            __nv_bfloat16 gv[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) gv[i] = __float2bfloat16_rn(__uint_as_float(v[i]));
-            store_transposed<32>(gv, tbuf, lane, gucol + static_cast<int64_t>(c) * 2 * p.out_cols, 2 * p.out_cols,
-                                 x.valid - c);
+            uint32_t pk[16];
+            pack_chunk(a, b, pk);
+            stage_rows<4>(pk, tbuf, lane);
+            rows_to_global<32>(tbuf, lane, gucol + static_cast<int64_t>(c) * 2 * p.out_cols, 2 * p.out_cols,
+                               x.valid - c);
           }
-          // send the 16 columns the partner keeps
-          // (static indices on both sides of the select keep v in registers)
+          // token groups 0-1 (columns c .. c+15) stay with the gate warp, 2-3
+          // with the up warp; each sends the other half, 16 words per thread
+          // (static indices on both sides of the selects keep a, b in registers)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            const uint4 lo4 = make_uint4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-            const uint4 hi4 = make_uint4(v[16 + 4 * q4], v[16 + 4 * q4 + 1], v[16 + 4 * q4 + 2], v[16 + 4 * q4 + 3]);
-            *reinterpret_cast<uint4*>(my_x + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4)) = is_gate ? hi4 : lo4;
+            const uint32_t* src_up = q4 < 2 ? &a[4 * q4] : &b[4 * (q4 - 2)];
+            const uint32_t* src_gate = q4 < 2 ? &a[8 + 4 * q4] : &b[8 + 4 * (q4 - 2)];
+            const uint4 w_up = make_uint4(src_up[0], src_up[1], src_up[2], src_up[3]);
+            const uint4 w_gate = make_uint4(src_gate[0], src_gate[1], src_gate[2], src_gate[3]);
+            *reinterpret_cast<uint4*>(my_x + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4)) = is_gate ? w_gate : w_up;
           }
           if (!pair_sync(xsync, xparity, abort_flag)) {
             failed = true;
             break;
           }
           const int keep0 = is_gate ? 0 : 16;
+          // k = 0..7: features 0-15 (a), k = 8..15: features 16-31 (b) of the
+          // two kept token groups, in fragment order
           float g[16], u[16];
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -579,23 +624,37 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             const float o[4] = {__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w)};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float mine = __uint_as_float(is_gate ? v[4 * q4 + i] : v[16 + 4 * q4 + i]);
-              g[4 * q4 + i] = is_gate ? mine : o[i];
-              u[4 * q4 + i] = is_gate ? o[i] : mine;
+              const int k = 4 * q4 + i;
+              const uint32_t mine_gate = k < 8 ? a[k] : b[k - 8];
+              const uint32_t mine_up = k < 8 ? a[8 + k] : b[k];
+              const float mine = __uint_as_float(is_gate ? mine_gate : mine_up);
+              g[k] = is_gate ? mine : o[i];
+              u[k] = is_gate ? o[i] : mine;
             }
           }
-          if (c + 32 < c_end) tmem_ld_32x32(taddr + c + 32, v);
+          if (c + 32 < c_end) {
+            tmem_ld_16x256b_x4(taddr + c + 32, a);
+            tmem_ld_16x256b_x4(taddr_b + c + 32, b);
+          }
           if (!pair_sync(xsync, xparity, abort_flag)) {  // the partner has read my buffer
             tmem_ld_wait();
             failed = true;
             break;
           }
-          __nv_bfloat16 hv[16];
+          float h[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) hv[i] = __float2bfloat16_rn(silu_f32(g[i]) * u[i]);
+          for (int k = 0; k < 16; ++k) h[k] = silu_f32(g[k]) * u[k];
+          uint32_t ph[8];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            ph[4 * t] = pack_bf16x2(h[4 * t], h[4 * t + 1]);
+            ph[4 * t + 1] = pack_bf16x2(h[4 * t + 2], h[4 * t + 3]);
+            ph[4 * t + 2] = pack_bf16x2(h[8 + 4 * t], h[8 + 4 * t + 1]);
+            ph[4 * t + 3] = pack_bf16x2(h[8 + 4 * t + 2], h[8 + 4 * t + 3]);
+          }
           const int r0 = c + keep0;  // first token column of my 16
-          store_transposed<16>(hv, tbuf, lane, hcol + static_cast<int64_t>(r0) * p.out_cols, p.out_cols,
-                               x.valid - r0);
+          stage_rows<2>(ph, tbuf, lane);
+          rows_to_global<16>(tbuf, lane, hcol + static_cast<int64_t>(r0) * p.out_cols, p.out_cols, x.valid - r0);
           if (c + 32 < c_end) tmem_ld_wait();
         }
       } else {
@@ -604,28 +663,38 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         __nv_bfloat16* ycol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + i0;
 #pragma unroll 1
         for (int c = c_begin; c < c_end; c += 32) {
-          __nv_bfloat16 yv[32];
+          if (c + 32 >= c_end) release();
           if (p.row_scale != nullptr) {
-            // lane i loads the gate of token column c + i; every lane takes all 32
+            // lane i loads the gate of token column c + i; thread i's columns
+            // are 8g + 2(i%4) and +1
             const float s_l = c + lane < x.valid ? __ldg(p.row_scale + x.tok0 + c + lane) : 1.0f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              yv[i] = __float2bfloat16_rn(__shfl_sync(0xffffffffu, s_l, i) * __uint_as_float(v[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) yv[i] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            for (int g = 0; g < 4; ++g) {
+              const float s0 = __shfl_sync(0xffffffffu, s_l, 8 * g + 2 * (lane & 3));
+              const float s1 = __shfl_sync(0xffffffffu, s_l, 8 * g + 2 * (lane & 3) + 1);
+              a[4 * g] = __float_as_uint(s0 * __uint_as_float(a[4 * g]));
+              a[4 * g + 1] = __float_as_uint(s1 * __uint_as_float(a[4 * g + 1]));
+              a[4 * g + 2] = __float_as_uint(s0 * __uint_as_float(a[4 * g + 2]));
+              a[4 * g + 3] = __float_as_uint(s1 * __uint_as_float(a[4 * g + 3]));
+              b[4 * g] = __float_as_uint(s0 * __uint_as_float(b[4 * g]));
+              b[4 * g + 1] = __float_as_uint(s1 * __uint_as_float(b[4 * g + 1]));
+              b[4 * g + 2] = __float_as_uint(s0 * __uint_as_float(b[4 * g + 2]));
+              b[4 * g + 3] = __float_as_uint(s1 * __uint_as_float(b[4 * g + 3]));
+            }
           }
-          if (c + 32 < c_end) tmem_ld_32x32(taddr + c + 32, v);
-          store_transposed<32>(yv, tbuf, lane, ycol + static_cast<int64_t>(c) * p.out_cols, p.out_cols,
-                               x.valid - c);
+          uint32_t pk[16];
+          pack_chunk(a, b, pk);
+          if (c + 32 < c_end) {
+            tmem_ld_16x256b_x4(taddr + c + 32, a);
+            tmem_ld_16x256b_x4(taddr_b + c + 32, b);
+          }
+          stage_rows<4>(pk, tbuf, lane);
+          rows_to_global<32>(tbuf, lane, ycol + static_cast<int64_t>(c) * p.out_cols, p.out_cols, x.valid - c);
           if (c + 32 < c_end) tmem_ld_wait();
         }
       }
       if (failed) break;
-      // this warp is done with the accumulator: tell the leader
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) arrive_remote(lead_tempty);
+      if (!released) release();  // a warp without chunks in this tile
       aphase ^= 1u;
     }
   }
