@@ -47,6 +47,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes: one swizzle row
+constexpr int kPackHalf = 64;  // gate (then up) columns of one packed gate/up weight tile
 constexpr int UMMA_K = 16;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -81,6 +82,7 @@ struct Params {
   int K;
   int n_per_expert;
   int n_tiles;
+  int b_block_rows;  // rows of one packed weight tile (BN, or 128 for gate/up)
   int out_cols;
 };
 
@@ -211,8 +213,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         int e, mt, nt;
         decode_tile(t, s_pre, p.E, p.n_tiles, e, mt, nt);
         const int row0 = s_off[e] + mt * BM;
-        // weight tiles are stored tile-major: block (e, nt, kb) is BN x 64
-        const int bblk = (e * p.n_tiles + nt) * num_kb;
+        // weight tiles are stored tile-major: block (e, tile, kb) is
+        // b_block_rows x 64, and an N tile spans BN / b_block_rows of them
+        const int per_tile = BN / p.b_block_rows;
+        const int bblk = (e * p.n_tiles + nt) * per_tile * num_kb;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&S->empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -224,7 +228,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             mbar_arrive_expect_tx(&S->full[stage], C::kStageBytes);
             tma_load_2d(sA + stage * C::kABytes, &tm_a, &S->full[stage], kb * BK, row0);
           }
-          tma_load_3d(sB + stage * C::kBBytes, &tm_b, &S->full[stage], 0, 0, bblk + kb);
+          for (int j = 0; j < per_tile; ++j)
+            tma_load_3d(sB + stage * C::kBBytes + j * p.b_block_rows * BK * 2, &tm_b, &S->full[stage], 0, 0,
+                        bblk + j * num_kb + kb);
           last_stage = stage;
           last_phase = phase;
           if (++stage == C::kStages) {
@@ -403,15 +409,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         if (lane == 0) mbar_arrive(&S->tempty[acc]);
       };
       if constexpr (kSwiGLU) {
-        constexpr int H = BN / 2;  // gate columns [0, H), up columns [H, 2H)
+        // the tile's output features [nt * H, nt * H + H) come from packed
+        // gate/up tiles of 64 gate then the same 64 up columns
+        constexpr int H = BN / 2;
         constexpr int kCols = H / (kEpi / 4);
         const int c0 = half * kCols;
         __nv_bfloat16* dst = p.out + wrow0 * p.out_cols + static_cast<int64_t>(nt) * H + c0;
 #pragma unroll 1
         for (int c = 0; c < kCols; c += 32) {
           uint32_t g[32], u[32];
-          tmem_ld_32x32(taddr + c0 + c, g);
-          tmem_ld_32x32(taddr + H + c0 + c, u);
+          const int o = c0 + c;
+          const int gcol = (o / kPackHalf) * 2 * kPackHalf + o % kPackHalf;
+          tmem_ld_32x32(taddr + gcol, g);
+          tmem_ld_32x32(taddr + gcol + kPackHalf, u);
           tmem_ld_wait();
           if (c + 32 == kCols) release_accumulator();
           uint32_t packed[16];
@@ -463,9 +473,10 @@ cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t st
   // the gathered variant reads A with plain copies; its map is unused (built over the same matrix)
   if (!make_bf16_map_2d(&ma, pb.a, kGather ? pb.a_rows : pb.P, pb.K, BK, kGather ? 1 : BM))
     return cudaErrorInvalidValue;
-  // tile-major weights as [blocks][BN rows][64], one block per box
-  const int64_t blocks = static_cast<int64_t>(pb.E) * (pb.n_per_expert / BN) * ((pb.K + BK - 1) / BK);
-  if (!make_bf16_map_3d(&mb, pb.b, BK, BN, blocks, BK, BN)) return cudaErrorInvalidValue;
+  // tile-major weights as [blocks][block rows][64], one block per box
+  const int block_rows = kSwiGLU ? 2 * kPackHalf : BN;
+  const int64_t blocks = static_cast<int64_t>(pb.E) * (pb.n_per_expert / block_rows) * ((pb.K + BK - 1) / BK);
+  if (!make_bf16_map_3d(&mb, pb.b, BK, block_rows, blocks, BK, block_rows)) return cudaErrorInvalidValue;
   Params prm;
   prm.offsets = pb.offsets;
   prm.gather_rows = pb.gather_rows;
@@ -480,6 +491,7 @@ cudaError_t launch_bn(const GroupedGemmProblem& pb, int num_sms, cudaStream_t st
   prm.K = pb.K;
   prm.n_per_expert = pb.n_per_expert;
   prm.n_tiles = pb.n_per_expert / BN;
+  prm.b_block_rows = block_rows;
   prm.out_cols = pb.out_cols;
   const size_t smem = 1024 + static_cast<size_t>(C::kStages) * C::kStageBytes + sizeof(Smem) +
                       2 * static_cast<size_t>(pb.E + 1) * sizeof(int32_t) + 16 + kStoreStageBytes;
@@ -502,8 +514,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int 
   if (pb.gather_rows == nullptr && grouped_gemm_2sm_supported(pb, epi))
     return launch_grouped_gemm_2sm(pb, epi, num_sms, stream);
   if (epi == Epilogue::kSwiGLU) {
-    // N tile = matching gate and up halves of gate_up_half_tile(f) columns
-    const bool wide = gate_up_tile_n(pb.out_cols) == 256;
+    // N tile = one or two packed gate/up tiles (64 gate + 64 up columns each)
+    if (gate_up_half_tile(pb.out_cols) != kPackHalf) return cudaErrorNotSupported;
+    const bool wide = pb.n_per_expert % 256 == 0;
     if (pb.gather_rows != nullptr)
       return wide ? launch_bn<256, true, true>(pb, num_sms, stream) : launch_bn<128, true, true>(pb, num_sms, stream);
     return wide ? launch_bn<256, true, false>(pb, num_sms, stream) : launch_bn<128, true, false>(pb, num_sms, stream);
