@@ -217,13 +217,10 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
           uint8_t* b_dst = sB + stage * C::kBBytes;
           mbar_arrive_expect_tx(&S->full[stage], C::kStageBytes);
           if constexpr (kW) {
-            // rows row0 + kb*64 .. +63 of both operands, 64 columns a chunk
-#pragma unroll
-            for (int c = 0; c < BM / 64; ++c)
-              tma_load_2d(a_dst + c * kChunk, &tm_a, &S->full[stage], mt * BM + c * 64, row0 + kb * BK);
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(b_dst + c * kChunk, &tm_b, &S->full[stage], nt * BN + c * 64, row0 + kb * BK);
+            // rows row0 + kb*64 .. +63 of both operands: one copy per operand
+            // of BM / 64 (BN / 64) consecutive 64-column chunks
+            tma_load_3d(a_dst, &tm_a, &S->full[stage], 0, row0 + kb * BK, mt * (BM / 64));
+            tma_load_3d(b_dst, &tm_b, &S->full[stage], 0, row0 + kb * BK, nt * (BN / 64));
           } else {
             tma_load_2d(a_dst, &tm_a, &S->full[stage], kb * BK, row0);
             if constexpr (M == Mode::kGateUpSave) {
@@ -231,13 +228,11 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
             } else {
               // K rows kb*64.. of this expert's weights are rows of packed
               // N tile (kb*64)/b_rows; N chunk c is that tile's K block
-              // nt*BN/64 + c
+              // nt*BN/64 + c: one copy of BN / 64 consecutive blocks
               const int kr = kb * BK;
               const int blk0 = (e * p.b_tiles + kr / p.b_rows) * p.b_kblocks + nt * (BN / 64);
               const int brow = kr % p.b_rows;
-#pragma unroll
-              for (int c = 0; c < BN / 64; ++c)
-                tma_load_3d(b_dst + c * kChunk, &tm_b, &S->full[stage], 0, brow, blk0 + c);
+              tma_load_3d(b_dst, &tm_b, &S->full[stage], 0, brow, blk0);
             }
           }
           last_stage = stage;
@@ -303,21 +298,28 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
         tc_fence_after_sync();
         uint8_t* a_st = sA + stage * C::kABytes;
         uint8_t* b_st = sB + stage * C::kBBytes;
+        // MMAs of 16 K rows each; in an expert's last K block only those
+        // holding its rows run (kWgrad)
+        int n_kk = BK / UMMA_K;
         if constexpr (kW) {
           const int valid = rows - kb * BK;
           if (valid < BK) {
-            // rows valid..63 of every chunk belong to the next expert (or lie
-            // past the matrix): a whole 128-byte row is zero whatever the
-            // swizzle does inside it
-            // lane: 16-byte piece lane % 8 of rows valid + lane / 8, +4, ...
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            const int piece = lane & 7;
+            n_kk = (valid + UMMA_K - 1) / UMMA_K;
+            const int zend = n_kk * UMMA_K;
+            if (valid < zend) {
+              // rows valid .. zend-1 of every chunk belong to the next expert
+              // (or lie past the matrix): a whole 128-byte row is zero
+              // whatever the swizzle does inside it
+              // lane: 16-byte piece lane % 8 of rows valid + lane / 8, +4, ...
+              const uint4 zero = make_uint4(0, 0, 0, 0);
+              const int piece = lane & 7;
 #pragma unroll
-            for (int c = 0; c < (BM + BN) / 64; ++c) {
-              uint8_t* cb = c < BM / 64 ? a_st + c * kChunk : b_st + (c - BM / 64) * kChunk;
-              for (int r = valid + (lane >> 3); r < BK; r += 4) reinterpret_cast<uint4*>(cb + r * 128)[piece] = zero;
+              for (int c = 0; c < (BM + BN) / 64; ++c) {
+                uint8_t* cb = c < BM / 64 ? a_st + c * kChunk : b_st + (c - BM / 64) * kChunk;
+                for (int r = valid + (lane >> 3); r < zend; r += 4) reinterpret_cast<uint4*>(cb + r * 128)[piece] = zero;
+              }
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
           }
         }
@@ -326,6 +328,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
           const uint32_t b0 = smem_addr(b_st);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            if (kk >= n_kk) break;
             const uint64_t da = C::kAMN ? sw128_mnmajor_desc(a0 + kk * UMMA_K * 128, kChunk)
                                         : sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
             const uint64_t db = C::kBMN ? sw128_mnmajor_desc(b0 + kk * UMMA_K * 128, kChunk)
@@ -594,7 +597,7 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
       CUtensorMap ma, mb;
       if (!make_bf16_map_2d(&ma, a.dy, a.P, a.d, BK, BM)) return cudaErrorInvalidValue;
       const int64_t blocks = static_cast<int64_t>(a.E) * (a.d / bn_dn) * (a.f / BK);
-      if (!make_bf16_map_3d(&mb, wdn, BK, bn_dn, blocks, BK, 64)) return cudaErrorInvalidValue;
+      if (!make_bf16_map_3d(&mb, wdn, BK, bn_dn, blocks, BK, 64, bn / 64)) return cudaErrorInvalidValue;
       Params prm = base_params(a.offsets, a.E, a.counters + 2, a.status);
       prm.K = a.d;
       prm.n_tiles = a.f / bn;
@@ -618,7 +621,7 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
       CUtensorMap ma, mb;
       if (!make_bf16_map_2d(&ma, a.dgu, a.P, 2 * a.f, BK, BM)) return cudaErrorInvalidValue;
       const int64_t blocks = static_cast<int64_t>(a.E) * (2 * a.f / bn_gu) * (a.d / BK);
-      if (!make_bf16_map_3d(&mb, wgu, BK, bn_gu, blocks, BK, 64)) return cudaErrorInvalidValue;
+      if (!make_bf16_map_3d(&mb, wgu, BK, bn_gu, blocks, BK, 64, bn / 64)) return cudaErrorInvalidValue;
       Params prm = base_params(a.offsets, a.E, a.counters + 3, a.status);
       prm.K = 2 * a.f;
       prm.n_tiles = a.d / bn;
@@ -638,8 +641,8 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
     const int bn = tile_n_for(a.d);
     CUtensorMap ma, mb;
     const int64_t rows = a.P > 0 ? a.P : 1;
-    if (!make_bf16_map_2d(&ma, a.P > 0 ? a.h : a.dw_down, rows, a.f, 64, BK)) return cudaErrorInvalidValue;
-    if (!make_bf16_map_2d(&mb, a.P > 0 ? a.dy : a.dw_down, rows, a.d, 64, BK)) return cudaErrorInvalidValue;
+    if (!make_bf16_map_col_blocks(&ma, a.P > 0 ? a.h : a.dw_down, rows, a.f, BK, BM / 64)) return cudaErrorInvalidValue;
+    if (!make_bf16_map_col_blocks(&mb, a.P > 0 ? a.dy : a.dw_down, rows, a.d, BK, bn / 64)) return cudaErrorInvalidValue;
     Params prm = base_params(a.offsets, a.E, a.counters + 4, a.status);
     prm.m_tiles = (a.f + BM - 1) / BM;
     prm.n_tiles = a.d / bn;
@@ -656,8 +659,10 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
     const int bn = tile_n_for(2 * a.f);  // may span two interleaved gate/up tiles
     CUtensorMap ma, mb;
     const int64_t rows = a.P > 0 ? a.P : 1;
-    if (!make_bf16_map_2d(&ma, a.P > 0 ? a.x_perm : a.dw_gate, rows, a.d, 64, BK)) return cudaErrorInvalidValue;
-    if (!make_bf16_map_2d(&mb, a.P > 0 ? a.dgu : a.dw_gate, rows, 2 * a.f, 64, BK)) return cudaErrorInvalidValue;
+    if (!make_bf16_map_col_blocks(&ma, a.P > 0 ? a.x_perm : a.dw_gate, rows, a.d, BK, BM / 64))
+      return cudaErrorInvalidValue;
+    if (!make_bf16_map_col_blocks(&mb, a.P > 0 ? a.dgu : a.dw_gate, rows, 2 * a.f, BK, bn / 64))
+      return cudaErrorInvalidValue;
     Params prm = base_params(a.offsets, a.E, a.counters + 5, a.status);
     prm.m_tiles = (a.d + BM - 1) / BM;
     prm.n_tiles = 2 * a.f / bn;

@@ -131,7 +131,10 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
 // 2-D: row-major [rows, cols], box [box_rows, box_cols].  3-D: dense
 // [d2][d1][d0] (d0 contiguous), box [1][box1][box0].
 bool make_bf16_map_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
-bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int box0, int box1);
+bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int box0, int box1,
+                      int box2 = 1);
+bool make_bf16_map_col_blocks(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows,
+                              int box_blocks);
 
 // Bounded-wait check: one block waits on a phase that never completes and
 // records a timeout in *status after limit_ns.

@@ -46,10 +46,26 @@ bool make_bf16_map_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t c
   return encode(map, ptr, 2, dims, strides, box);
 }
 
-bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int box0, int box1) {
+bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int box0, int box1,
+                      int box2) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1), static_cast<cuuint64_t>(d2)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d0) * 2, static_cast<cuuint64_t>(d0 * d1) * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1), 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1),
+                             static_cast<cuuint32_t>(box2)};
+  return encode(map, ptr, 3, dims, strides, box);
+}
+
+// A row-major [rows, cols] matrix seen as (64 columns, rows, cols / 64
+// column blocks): the block stride (128 bytes) is below the row stride, so
+// one box of (64, box_rows, box_blocks) lands in shared memory as
+// box_blocks consecutive [box_rows][64] chunks, each in the 128-byte
+// swizzled MN-major layout the MMA descriptors read.
+bool make_bf16_map_col_blocks(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows,
+                              int box_blocks) {
+  if (cols % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_blocks)};
   return encode(map, ptr, 3, dims, strides, box);
 }
 
