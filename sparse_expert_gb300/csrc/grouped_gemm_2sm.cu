@@ -68,11 +68,19 @@ constexpr int kRing = 4;                          // tile ids published ahead
 // thread and epilogue warps, the peer's producer and epilogue warps
 constexpr int kRingReaders = 2 + 2 * kEpiWarps;
 
+// What the epilogue makes of the accumulator (weight rows x token columns)
+enum : int {
+  kModeSwiGLU = 0,     // gate/up: H = Silu(G) * U (and optionally G, U themselves)
+  kModeRows = 1,       // the rows as they are (down, dX), optionally scaled per token
+  kModeSwiGLUBwd = 2,  // dH: dG = dH U Silu'(G), dU = dH Silu(G) from the saved G, U
+};
+
 struct Params {
   const int32_t* offsets;
-  const float* row_scale;  // down: gate of each row, or null
-  __nv_bfloat16* out;      // H [P, f] or Y [P, d]
-  __nv_bfloat16* gu;       // gate/up: also G, U [P, 2f] in the packed interleave, or null
+  const float* row_scale;  // kModeRows: gate of each row, or null
+  __nv_bfloat16* out;      // H [P, f], Y [P, d], dX [P, d] or dG,dU [P, 2f] (packed interleave)
+  __nv_bfloat16* gu;       // kModeSwiGLU: also G, U [P, 2f] in the packed interleave, or null
+  const __nv_bfloat16* gu_in;  // kModeSwiGLUBwd: the saved G, U [P, 2f]
   int32_t* status;
   int32_t* tile_counter;   // zeroed before launch
   int E;
@@ -80,8 +88,10 @@ struct Params {
   int m_tiles;         // 256-row weight tiles per expert
   int a_tile_rows;     // rows of one packed weight tile (128 gate/up, 256 down)
   int a_tiles;         // packed weight tiles per expert
-  int out_cols;        // f or d
-  int swiglu;
+  int a_mn;            // weights read transposed: M runs along a packed tile's columns
+  int a_mblocks;       // a_mn: 64-column blocks of one packed tile
+  int out_cols;        // f or d (kModeSwiGLUBwd: f, rows of 2f)
+  int mode;
 };
 
 struct Smem {
@@ -307,6 +317,45 @@ __device__ __forceinline__ void rows_to_global(const uint8_t* buf, int lane, __n
   __syncwarp();
 }
 
+// 16 token rows of a 64-byte column segment of src (row stride ld; rows
+// >= valid as zeros) into two 16-byte registers per thread, and from there
+// into the staging buffer (8 rows x 64 contiguous bytes per load
+// instruction): split so the loads can be issued early.
+__device__ __forceinline__ void load_rows16(uint4 (&v)[2], int lane, const __nv_bfloat16* src, int64_t ld,
+                                            int valid) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int idx = i * 32 + lane;
+    const int r = idx >> 2;
+    const int q = idx & 3;
+    v[i] = r < valid ? __ldg(reinterpret_cast<const uint4*>(src + r * ld + q * 8)) : make_uint4(0, 0, 0, 0);
+  }
+}
+__device__ __forceinline__ void store_rows16(uint8_t* buf, int lane, const uint4 (&v)[2]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int idx = i * 32 + lane;
+    const int r = idx >> 2;
+    const int q = idx & 3;
+    *reinterpret_cast<uint4*>(buf + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) = v[i];
+  }
+  __syncwarp();
+}
+
+// The inverse of stage_rows: ldmatrix .trans hands thread i features
+// 8m + i/4 of tokens 8g + 2(i%4) and +1 (p[4g + m], packed low/high).
+template <int G>
+__device__ __forceinline__ void rows_to_fragment(const uint8_t* buf, int lane, uint32_t (&p)[4 * G]) {
+  const uint32_t a0 = smem_addr(buf) + (lane & 7) * 64 + ((((lane >> 3) ^ (lane >> 1)) & 3) << 4);
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(p[4 * g]), "=r"(p[4 * g + 1]), "=r"(p[4 * g + 2]), "=r"(p[4 * g + 3])
+                 : "r"(a0 + g * 512)
+                 : "memory");
+  __syncwarp();
+}
+
 // The fragment of a 32-feature x 32-token chunk from its two 16x256b loads
 // (a: features 0-15, b: 16-31), rounded to bf16.
 __device__ __forceinline__ void pack_chunk(const uint32_t (&a)[16], const uint32_t (&b)[16], uint32_t (&p)[16]) {
@@ -424,7 +473,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         }
         if (t < 0) break;
         const Tile x = decode(t, s_off, s_pre, p.E, p.m_tiles);
-        // this CTA's 128 weight rows: packed tile and row inside it
+        // this CTA's 128 weight rows: packed tile and row inside it (K-major),
+        // or, read transposed, the two 64-column blocks that hold them
         const int w0 = x.mt * 2 * kHalfRows + static_cast<int>(rank) * kHalfRows;
         const int wblk = (x.e * p.a_tiles + w0 / p.a_tile_rows) * num_kb;
         const int wrow = w0 % p.a_tile_rows;
@@ -441,7 +491,15 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           const uint32_t lead_full = leader_addr(&S->full[stage]);
           uint8_t* st = s_stage0 + stage * kStageBytes;
           if (rank == 0) mbar_arrive_expect_tx(&S->full[stage], bytes);
-          tma_load_3d_pair(st, &tm_w, lead_full, 0, wrow, wblk + kb);
+          if (p.a_mn) {
+            // K rows kb*64 .. +63 lie in packed tile k0 / a_tile_rows; M values
+            // w0 .. w0+127 are its column blocks w0/64 and w0/64 + 1
+            const int k0 = kb * BK;
+            const int blk = (x.e * p.a_tiles + k0 / p.a_tile_rows) * p.a_mblocks + w0 / 64;
+            tma_load_3d_pair(st, &tm_w, lead_full, 0, k0 % p.a_tile_rows, blk);
+          } else {
+            tma_load_3d_pair(st, &tm_w, lead_full, 0, wrow, wblk + kb);
+          }
           tma_load_2d_pair(st + kABytes, &tm_x, lead_full, kb * BK, xrow1);
           if (n2 > 0) tma_load_2d_pair(st + kABytes + kBBytes, &tm_x, lead_full, kb * BK, xrow2);
           if (++stage == kStages) {
@@ -459,7 +517,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       int stage = 0;
       uint32_t phase = 0;
       uint32_t aphase = 0;
-      const uint32_t idesc0 = umma_idesc_bf16_f32(2 * kHalfRows, 16) & ~(0x3Fu << 17);
+      const uint32_t idesc0 = umma_idesc_bf16_f32_major(2 * kHalfRows, 16, p.a_mn != 0, false) & ~(0x3Fu << 17);
       int rs = 0;
       uint32_t rphase = 0;
       for (;;) {
@@ -496,7 +554,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           const uint32_t b2 = b1 + kBBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t da = sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
+            // MN-major A: two 8 KB chunks of [64 K][64 M]; 16 K rows = 2 KB
+            const uint64_t da = p.a_mn ? sw128_mnmajor_desc(a0 + kk * UMMA_K * 128, kABytes / 2)
+                                       : sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
             const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
             umma_pair(d_tmem, da, sw128_kmajor_desc(b1 + kk * UMMA_K * 2), idesc1, accumulate);
             if (n2 > 0)
@@ -573,7 +633,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         tmem_ld_16x256b_x4(taddr_b + c_begin, b);
         tmem_ld_wait();
       }
-      if (p.swiglu) {
+      if (p.mode == kModeSwiGLU) {
         // lanes of quads 0/1: gate features j0 + 32*(quad&1) + lane; quads
         // 2/3: the up features of the same j.  The gate warp keeps token
         // columns 0-15 of each chunk, the up warp 16-31.
@@ -655,6 +715,68 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           const int r0 = c + keep0;  // first token column of my 16
           stage_rows<2>(ph, tbuf, lane);
           rows_to_global<16>(tbuf, lane, hcol + static_cast<int64_t>(r0) * p.out_cols, p.out_cols, x.valid - r0);
+          if (c + 32 < c_end) tmem_ld_wait();
+        }
+      } else if (p.mode == kModeSwiGLUBwd) {
+        // lanes: features j0 .. j0+31 of dH (gate features of the packed
+        // interleave: gate column (j / 64) * 128 + j % 64, up 64 further on)
+        const int j0 = x.mt * 2 * kHalfRows + static_cast<int>(rank) * kHalfRows + quad * 32;
+        const int64_t ld = 2 * static_cast<int64_t>(p.out_cols);
+        const int64_t gcol0 = static_cast<int64_t>(j0 / 64) * 128 + j0 % 64;
+        const __nv_bfloat16* gsrc = p.gu_in + static_cast<int64_t>(x.tok0) * ld + gcol0;
+        __nv_bfloat16* gdst = p.out + static_cast<int64_t>(x.tok0) * ld + gcol0;
+        // G, U of the next 16 tokens are loaded into registers one half ahead,
+        // so their latency overlaps the math and stores of the current half
+        uint4 gv[2], uv[2];
+        if (c_begin < c_end) {
+          load_rows16(gv, lane, gsrc + static_cast<int64_t>(c_begin) * ld, ld, x.valid - c_begin);
+          load_rows16(uv, lane, gsrc + static_cast<int64_t>(c_begin) * ld + 64, ld, x.valid - c_begin);
+        }
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; c += 32) {
+          if (c + 32 >= c_end) release();
+          // two halves of 16 tokens (token groups 2h, 2h + 1) keep the
+          // register footprint of G, U and the results small
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r0 = c + 16 * h;
+            uint32_t pg[8], pu[8];
+            store_rows16(tbuf, lane, gv);
+            rows_to_fragment<2>(tbuf, lane, pg);
+            store_rows16(tbuf, lane, uv);
+            rows_to_fragment<2>(tbuf, lane, pu);
+            // Silu(g) = g s, Silu'(g) = s (1 + g (1 - s)), s = sigmoid(g);
+            // dG and dU replace G and U in pg, pu
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int i = 4 * (2 * h + gg) + 2 * (m & 1);
+                const float d0 = __uint_as_float(m < 2 ? a[i] : b[i]);
+                const float d1 = __uint_as_float(m < 2 ? a[i + 1] : b[i + 1]);
+                const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pg[4 * gg + m]));
+                const float2 uf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pu[4 * gg + m]));
+                const float s0 = __fdividef(1.0f, 1.0f + __expf(-gf.x));
+                const float s1 = __fdividef(1.0f, 1.0f + __expf(-gf.y));
+                pg[4 * gg + m] = pack_bf16x2(d0 * uf.x * s0 * (1.0f + gf.x * (1.0f - s0)),
+                                             d1 * uf.y * s1 * (1.0f + gf.y * (1.0f - s1)));
+                pu[4 * gg + m] = pack_bf16x2(d0 * gf.x * s0, d1 * gf.y * s1);
+              }
+            }
+            if (h == 1 && c + 32 < c_end) {
+              tmem_ld_16x256b_x4(taddr + c + 32, a);
+              tmem_ld_16x256b_x4(taddr_b + c + 32, b);
+            }
+            const int rn = r0 + 16;  // the next half (of this chunk or the next)
+            if (rn < c_end) {
+              load_rows16(gv, lane, gsrc + static_cast<int64_t>(rn) * ld, ld, x.valid - rn);
+              load_rows16(uv, lane, gsrc + static_cast<int64_t>(rn) * ld + 64, ld, x.valid - rn);
+            }
+            stage_rows<2>(pg, tbuf, lane);
+            rows_to_global<16>(tbuf, lane, gdst + static_cast<int64_t>(r0) * ld, ld, x.valid - r0);
+            stage_rows<2>(pu, tbuf, lane);
+            rows_to_global<16>(tbuf, lane, gdst + static_cast<int64_t>(r0) * ld + 64, ld, x.valid - r0);
+          }
           if (c + 32 < c_end) tmem_ld_wait();
         }
       } else {
@@ -741,6 +863,34 @@ size_t grouped_gemm_2sm_smem(int E) {
          2 * static_cast<size_t>(E + 1) * sizeof(int32_t);
 }
 
+namespace {
+
+cudaError_t launch_pairs(const CUtensorMap& mw, const CUtensorMap& mx, const Params& prm, int64_t P, int num_sms,
+                         cudaStream_t stream) {
+  const size_t smem = grouped_gemm_2sm_smem(prm.E);
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  // persistent: one pair per two SMs, never more pairs than an upper bound on tiles
+  const int64_t max_tiles = (P / kTileN + prm.E) * static_cast<int64_t>(prm.m_tiles);
+  int pairs = num_sms / 2;
+  if (max_tiles < pairs) pairs = static_cast<int>(max_tiles);
+  grouped_gemm_2sm_kernel<<<2 * pairs, kThreads, smem, stream>>>(mw, mx, prm);
+  return cudaGetLastError();
+}
+
+Params base_params(const int32_t* offsets, int E, int K, int32_t* tile_counter, int32_t* status) {
+  Params prm{};
+  prm.offsets = offsets;
+  prm.status = status;
+  prm.tile_counter = tile_counter;
+  prm.E = E;
+  prm.K = K;
+  return prm;
+}
+
+}  // namespace
+
 cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream) {
   if (pb.P == 0) return cudaSuccess;
   if (!grouped_gemm_2sm_supported(pb, epi)) return cudaErrorNotSupported;
@@ -752,30 +902,43 @@ cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, 
   const int64_t blocks = static_cast<int64_t>(pb.E) * (n_rows / a_tile_rows) * num_kb;
   if (!make_bf16_map_3d(&mw, pb.b, BK, a_tile_rows, blocks, BK, kHalfRows)) return cudaErrorInvalidValue;
   if (!make_bf16_map_2d(&mx, pb.a, pb.P, pb.K, BK, kHalfRows)) return cudaErrorInvalidValue;
-  Params prm;
-  prm.offsets = pb.offsets;
+  Params prm = base_params(pb.offsets, pb.E, pb.K, pb.tile_counter, pb.status);
   prm.row_scale = swiglu ? nullptr : pb.row_scale;
   prm.out = static_cast<__nv_bfloat16*>(pb.out);
   prm.gu = swiglu ? static_cast<__nv_bfloat16*>(pb.gu_out) : nullptr;
-  prm.status = pb.status;
-  prm.tile_counter = pb.tile_counter;
-  prm.E = pb.E;
-  prm.K = pb.K;
   prm.m_tiles = n_rows / (2 * kHalfRows);
   prm.a_tile_rows = a_tile_rows;
   prm.a_tiles = n_rows / a_tile_rows;
   prm.out_cols = pb.out_cols;
-  prm.swiglu = swiglu ? 1 : 0;
-  const size_t smem = grouped_gemm_2sm_smem(pb.E);
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  // persistent: one pair per two SMs, never more pairs than an upper bound on tiles
-  const int64_t max_tiles = (pb.P / kTileN + pb.E) * static_cast<int64_t>(prm.m_tiles);
-  int pairs = num_sms / 2;
-  if (max_tiles < pairs) pairs = static_cast<int>(max_tiles);
-  grouped_gemm_2sm_kernel<<<2 * pairs, kThreads, smem, stream>>>(mw, mx, prm);
-  return cudaGetLastError();
+  prm.mode = swiglu ? kModeSwiGLU : kModeRows;
+  return launch_pairs(mw, mx, prm, pb.P, num_sms, stream);
+}
+
+bool dgrad_2sm_supported(const DgradProblem& g) {
+  return g.m_out % (2 * kHalfRows) == 0 && g.K % BK == 0 && g.w_tile_rows % BK == 0 &&
+         (g.mode != DgradEpilogue::kSwiGLUBwd || gate_up_half_tile(g.m_out) == 64);
+}
+
+cudaError_t launch_dgrad_2sm(const DgradProblem& g, int num_sms, cudaStream_t stream) {
+  if (g.P == 0) return cudaSuccess;
+  if (!dgrad_2sm_supported(g)) return cudaErrorNotSupported;
+  CUtensorMap mw, mx;
+  // packed weights as (64 columns, tile rows, blocks): two consecutive column
+  // blocks of one packed tile per CTA and K block
+  const int64_t blocks = static_cast<int64_t>(g.E) * g.w_tiles * (g.m_out / 64);
+  if (!make_bf16_map_3d(&mw, g.w_packed, BK, g.w_tile_rows, blocks, BK, BK, 2)) return cudaErrorInvalidValue;
+  if (!make_bf16_map_2d(&mx, g.tokens, g.P, g.K, BK, kHalfRows)) return cudaErrorInvalidValue;
+  Params prm = base_params(g.offsets, g.E, g.K, g.tile_counter, g.status);
+  prm.out = static_cast<__nv_bfloat16*>(g.out);
+  prm.gu_in = static_cast<const __nv_bfloat16*>(g.gu_in);
+  prm.m_tiles = g.m_out / (2 * kHalfRows);
+  prm.a_tile_rows = g.w_tile_rows;
+  prm.a_tiles = g.w_tiles;
+  prm.a_mn = 1;
+  prm.a_mblocks = g.m_out / 64;
+  prm.out_cols = g.m_out;
+  prm.mode = g.mode == DgradEpilogue::kSwiGLUBwd ? kModeSwiGLUBwd : kModeRows;
+  return launch_pairs(mw, mx, prm, g.P, num_sms, stream);
 }
 
 }  // namespace moe

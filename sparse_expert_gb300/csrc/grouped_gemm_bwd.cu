@@ -590,7 +590,15 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
   const int bn_dn = down_tile_n(a.d);     // packed down N tile
   const int64_t mt_bound = a.P / BM + a.E;
   cudaError_t err = cudaSuccess;
-  if (a.P > 0) {
+  // the dgrad GEMMs run on SM pairs (grouped_gemm_2sm.cu) where the output
+  // features per expert are a multiple of 256, else on single SMs below
+  DgradProblem gd{a.dy, wdn, a.offsets, a.P, a.E, a.d, a.f, bn_dn, a.d / bn_dn, DgradEpilogue::kSwiGLUBwd,
+                  a.gu, a.dgu, a.counters + 2, a.status};
+  DgradProblem gx{a.dgu, wgu, a.offsets, a.P, a.E, 2 * a.f, a.d, bn_gu, 2 * a.f / bn_gu, DgradEpilogue::kRows,
+                  nullptr, a.dx_perm, a.counters + 3, a.status};
+  if (a.P > 0 && dgrad_2sm_supported(gd)) {
+    if ((err = launch_dgrad_2sm(gd, num_sms, stream)) != cudaSuccess) return err;
+  } else if (a.P > 0) {
     // dH = dY Wd^T with dG, dU in the epilogue: N = f, K = d, B from packed down
     {
       const int bn = tile_n_for(a.f);
@@ -614,7 +622,9 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
     }
   }
   if ((err = mark(0)) != cudaSuccess) return err;
-  if (a.P > 0) {
+  if (a.P > 0 && dgrad_2sm_supported(gx)) {
+    if ((err = launch_dgrad_2sm(gx, num_sms, stream)) != cudaSuccess) return err;
+  } else if (a.P > 0) {
     // dX = [dG | dU] [Wg ; Wu]^T: N = d, K = 2f (interleaved), B from packed gate/up
     {
       const int bn = tile_n_for(a.d);

@@ -99,6 +99,30 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int 
 bool grouped_gemm_2sm_supported(const GroupedGemmProblem& pb, Epilogue epi);
 cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
 
+// A dgrad GEMM of the backward on SM pairs: out[r, :] = tokens[r, :] W_e^T
+// for the rows r of expert e, with W_e the forward's packed weights read
+// transposed (the M = m_out output features run along a packed tile's
+// columns, K along its rows).
+enum class DgradEpilogue { kRows, kSwiGLUBwd };
+struct DgradProblem {
+  const void* tokens;      // [P, K] bf16: [dG | dU] interleaved (K = 2f) or dY (K = d)
+  const void* w_packed;    // packed gate/up (tile rows 128 along 2f) or down (tile rows 256 along d)
+  const int32_t* offsets;  // [E+1]
+  int64_t P;
+  int E;
+  int K;
+  int m_out;               // d (dX) or f (dH)
+  int w_tile_rows;         // rows of one packed tile
+  int w_tiles;             // packed tiles per expert (= K / w_tile_rows)
+  DgradEpilogue mode;      // kRows: out = dX [P, d]; kSwiGLUBwd: out = dG,dU [P, 2f] from gu_in
+  const void* gu_in;       // kSwiGLUBwd: the saved G, U [P, 2f]
+  void* out;
+  int32_t* tile_counter;
+  int32_t* status;
+};
+bool dgrad_2sm_supported(const DgradProblem& g);
+cudaError_t launch_dgrad_2sm(const DgradProblem& g, int num_sms, cudaStream_t stream);
+
 // ---- stage 4 backward: expert GEMMs of the backward pass
 struct BackwardGemmArgs {
   int64_t P;
