@@ -1,0 +1,147 @@
+// Helpers of the kernels that run on SM pairs (2-CTA clusters, tcgen05
+// cta_group::2): cluster addressing, bounded waits on barriers that the
+// other CTA arrives on, remote arrives, TMA copies counted on the leader's
+// barrier, paired TMEM allocation, MMA and commit.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the pair.
+__device__ __forceinline__ uint32_t pair_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t leader_addr(const void* p) { return pair_addr(p, 0); }
+
+__device__ __forceinline__ void st_cluster(uint32_t addr, int32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Waits on a barrier that the other CTA of the pair arrives on (acquire at
+// cluster scope), bounded like mbar_wait / mbar_wait_warp.
+__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t a = smem_addr(bar);
+  if (try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (try_wait_cluster(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ bool wait_cluster_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t a = smem_addr(bar);
+  uint64_t t0 = 0;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    const bool ok = try_wait_cluster(a, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((it & 31u) == 31u) {
+      int give_up = 0;
+      if (lane == 0) give_up = (*abort_flag != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Same without release semantics: the arrive does not wait for this
+// thread's earlier global stores to become visible.  Used where the waiter
+// consumes no memory this thread wrote (the accumulator hand-back: the TMEM
+// loads have completed at tcgen05.wait::ld).
+__device__ __forceinline__ void arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory whose completion is counted
+// on a stage barrier of the leader CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* map, uint32_t bar, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* map, uint32_t bar, int32_t c0, int32_t c1,
+                                                 int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` in both CTAs of the pair once every MMA issued so far by
+// this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// Both partner warps arrive, then wait (bounded) for the phase to complete.
+__device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t& parity, volatile int* abort_flag) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait_warp(bar, parity, abort_flag);
+  parity ^= 1u;
+  return ok;
+}
+
+}  // namespace moe
