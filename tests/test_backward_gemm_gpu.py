@@ -96,6 +96,13 @@ def test_swiglu_backward_empty_and_huge_groups(moe):
     assert (counts == 0).sum() > 0 and counts.max() > 1000
 
 
+def test_swiglu_backward_paired_empty_and_huge_groups(moe):
+    # d and f multiples of 256: both dgrad GEMMs run on SM pairs, here with
+    # experts without rows and experts spanning several 512-token tiles
+    counts = _expert_case(moe, 2048, 512, 32, 4, 256, seed=6, skew=3.0)
+    assert (counts == 0).sum() > 0 and counts.max() > 1000
+
+
 def test_swiglu_backward_single_expert_long_k(moe):
     # E = 1: every row in one group; the weight gradients contract over 700 rows
     _expert_case(moe, 700, 1024, 1, 1, 256, seed=9)
