@@ -143,9 +143,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def file_sha256(path):
-    with open(path, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()
+def code_sha256(path):
+    """sha256 of a C++/CUDA source with its // comments and blank lines
+    removed: counters recorded for a kernel stay valid across edits to its
+    comments, and only those."""
+    lines = []
+    with open(path) as fh:
+        for line in fh:
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
 def recorded_traffic(workload: str):
@@ -156,7 +164,7 @@ def recorded_traffic(workload: str):
             rec = json.load(fh)
     except (OSError, ValueError):
         return None
-    if rec.get("workload") != workload or rec.get("source_sha256") != file_sha256(GEMM_SOURCE):
+    if rec.get("workload") != workload or rec.get("source_code_sha256") != code_sha256(GEMM_SOURCE):
         return None
     return rec.get("dram_bytes_per_launch")
 

@@ -1,11 +1,14 @@
-// Grouped expert GEMMs of the forward on SM pairs (tcgen05 cta_group::2,
-// sm_103a), with the weights as the 256-row operand and the tokens as N.
+// Grouped expert GEMMs on SM pairs (tcgen05 cta_group::2, sm_103a), with
+// the weights as the 256-row operand and the tokens as N: the forward's two
+// GEMMs and the backward's two dgrad GEMMs.
 //
 // "Scalable Pretraining of Large MoE LMs on Aurora Super Computer", §3.1,
 // Algorithm 1, stage 4: gate_out/up_out = Grouped_mm(mlp_in, weight);
 // mul_out = Silu(gate_out) * up_out; mlp_out = Grouped_mm(mul_out,
 // down_weight), over expert-contiguous rows bounded by the cumulative
-// token counts.
+// token counts; and the same stage differentiated for the activations:
+// dH = dY Wd^T with dG = dH U Silu'(G), dU = dH Silu(G); dX = [dG | dU]
+// [Wg ; Wu]^T.
 //
 // Each tile computes D^T = W_e[256 rows, K] x X_e[N tokens, K]^T on a pair
 // of SMs (a 2-CTA cluster) for up to 512 of the expert's tokens at once
@@ -18,16 +21,25 @@
 // in each CTA's TMEM as its 128 weight rows x N token columns.  Per SM this
 // takes in 8.3 KB of operands per MFLOP (a one-SM 128 x 256 tile: 11.4).
 // One accumulator: the epilogue drains a tile before the next one starts.
+// The forward reads the packed weights K-major; the dgrad GEMMs read the
+// same packed tiles transposed (MN-major A: two consecutive 64-column
+// blocks of a packed tile per CTA and K block).
 //
-// Gate/up: a tile's 256 weight rows are two packed gate/up tiles of 64 gate
-// then the same 64 up columns, one per CTA, so TMEM lanes 0-63 of a CTA hold
-// gate features j..j+63 and lanes 64-127 the up features of the same j.  The
-// epilogue warps of lanes 0-31 and 64-95 (and 32-63 with 96-127) swap half
-// of their token columns through shared memory, form Silu(gate)*up in fp32,
-// and store H[token, j] in bf16.  Down: D^T rows are output features; the
-// epilogue scales each token column by its gate and stores Y[token, i].
-// Both transpose 32 x 32 chunks through shared memory so every global store
-// writes whole token-row segments.
+// Epilogues (each warp: 32 TMEM lanes = weight rows, 32-token chunks,
+// loaded as two 16x256b blocks whose fragment is stmatrix's, staged as
+// token rows in shared memory so every global access covers whole
+// token-row segments):
+//   gate/up: a tile's 256 weight rows are two packed gate/up tiles of 64
+//     gate then the same 64 up columns, one per CTA, so TMEM lanes 0-63 of
+//     a CTA hold gate features j..j+63 and lanes 64-127 the up features of
+//     the same j.  The warps of lanes 0-31 and 64-95 (and 32-63 with
+//     96-127) swap half of their token columns through shared memory, form
+//     Silu(gate)*up in fp32 and store H[token, j] (and, for the backward's
+//     recomputation, the raw G and U);
+//   rows: Y[token, i] or dX[token, i] as they are, or scaled by a gate per
+//     token;
+//   SwiGLU backward: dH with the saved G, U of the same rows (ldmatrix.trans
+//     turns their token rows into the fragment), stores dG and dU.
 //
 // Roles in each CTA of the pair (320 threads): warp 0 TMA producer (both
 // CTAs load their halves; every copy signals the leader's stage barrier),
@@ -37,8 +49,9 @@
 // scheduling): the leader claims each tile and writes its id into both
 // CTAs' rings, over a flat order expert -> weight tile -> token tile
 // (consecutive tiles share a weight tile in L2; an expert's tokens stay in
-// L2 across its weight tiles).  Every wait is bounded; a CTA that gives up records a timeout,
-// and both CTAs meet at a cluster barrier before TMEM is released.
+// L2 across its weight tiles).  Every wait is bounded; a CTA that gives up
+// records a timeout, and both CTAs meet at a cluster barrier before TMEM is
+// released.
 #include <cuda.h>
 
 #include "common.cuh"
