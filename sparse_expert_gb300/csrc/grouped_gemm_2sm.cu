@@ -120,14 +120,15 @@ struct Smem {
 };
 
 // Tile t: expert, weight tile, token tile.  s_pre[e] = tiles of experts
-// before e; an expert has m_tiles x ceil(rows / 256) tiles, token tile
+// before e; an expert has m_tiles x ceil(rows / 512) tiles, token tile
 // fastest.
 struct Tile {
   int e, mt, nt, tok0, valid, n;
 };
 
-// An expert's rows are split into ceil(rows / 256) near-equal token tiles
-// of S rows (a multiple of 16); returns the tile count and sets S.
+// An expert's rows are split into ceil(rows / 512) near-equal token tiles
+// of S rows (a multiple of 16, at most 512); returns the tile count and
+// sets S.
 __host__ __device__ __forceinline__ int token_tiles(int rows, int& S) {
   if (rows <= 0) {
     S = 0;
