@@ -103,6 +103,13 @@ def test_swiglu_backward_paired_empty_and_huge_groups(moe):
     assert (counts == 0).sum() > 0 and counts.max() > 1000
 
 
+def test_swiglu_backward_max_experts(moe):
+    # E = MOE_MAX_EXPERTS with d and f multiples of 256: paired dgrad and the
+    # weight gradients over ~16 rows per expert (one partial K block each)
+    counts = _expert_case(moe, 2048, 256, 1024, 8, 256, seed=12)
+    assert len(counts) == 1024
+
+
 def test_swiglu_backward_single_expert_long_k(moe):
     # E = 1: every row in one group; the weight gradients contract over 700 rows
     _expert_case(moe, 700, 1024, 1, 1, 256, seed=9)

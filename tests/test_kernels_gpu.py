@@ -231,6 +231,13 @@ def test_grouped_swiglu_empty_and_huge_groups(moe):
     assert (counts == 0).sum() > 0 and counts.max() > 1000
 
 
+def test_grouped_swiglu_max_experts(moe):
+    # E = MOE_MAX_EXPERTS: the largest expert tables in the paired GEMM's shared
+    # memory, ~16 rows per expert (one 16-token MMA per tile)
+    counts = _gemm_case(moe, 2048, 256, 1024, 8, 128, seed=11)
+    assert len(counts) == 1024
+
+
 def test_grouped_swiglu_single_expert_long_k(moe):
     # E=1: one group covering every row; d = 2048 gives 32 K blocks
     _gemm_case(moe, 700, 2048, 1, 1, 256, seed=9)
