@@ -47,7 +47,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kRing = 4;
 constexpr int kStoreStageBytes = kEpiWarps * 32 * 64;
-constexpr int kStageBudget = 227 * 1024 - 1024 - 1024 - 2 * 1025 * 4 - 16 - kStoreStageBytes;
+constexpr int kStageBudget = 227 * 1024 - 1024 - 1024 - 2 * 1025 * 4 - 1024 - kStoreStageBytes;
 
 enum class Mode { kGateUpSave, kDgradSwiGLU, kDgradPlain, kWgrad };
 
@@ -108,6 +108,7 @@ __device__ __forceinline__ float sigmoid_f32(float z) { return 1.0f / (1.0f + __
 template <int BN, Mode M>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                        const __grid_constant__ CUtensorMap tm_o1, const __grid_constant__ CUtensorMap tm_o2,
                         const Params p) {
   using C = Cfg<BN, M>;
   constexpr bool kW = (M == Mode::kWgrad);
@@ -118,7 +119,10 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
   Smem* S = reinterpret_cast<Smem*>(sB + C::kStages * C::kBBytes);
   int32_t* s_off = reinterpret_cast<int32_t*>(S + 1);  // [E+1] group boundaries
   int32_t* s_pre = s_off + (p.E + 1);                 // [E+1] M-tile prefix (M-grouped modes)
-  uint4* s_stage = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(s_pre + p.E + 1) + 15) & ~uintptr_t(15));
+  // per epilogue warp 2 KB of store staging, 1024-byte aligned (the 64-byte
+  // swizzle of the weight gradients' TMA stores repeats every 512 bytes)
+  uint4* s_stage =
+      reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(s_pre + p.E + 1) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -481,6 +485,43 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if constexpr (kW) {
+            // the 32 x 32 chunk goes out with one TMA store from the staging
+            // buffer (rows of 64 bytes, 16-byte pieces permuted by (row >> 1) & 3
+            // = the 64-byte swizzle); the previous store has read the buffer.
+            // (The gradient's rows come in multiples of 64, so a chunk has all
+            // 32 of its rows or none.)
+            if (valid_rows == 32) {
+              if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                sbuf[lane * 4 + (j ^ ((lane >> 1) & 3))] =
+                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              __syncwarp();
+              if (lane == 0) {
+                const CUtensorMap* map = &tm_o1;
+                int32_t x = n;
+                if (p.interleaved) {
+                  // interleaved gate/up column n -> gate or up column of [E, d, f]
+                  const int H = p.half;
+                  const int within = n % (2 * H);
+                  x = (n / (2 * H)) * H + within % H;
+                  if (within >= H) map = &tm_o2;
+                }
+                const int32_t y = static_cast<int32_t>(static_cast<int64_t>(e) * p.M_ext + wrow0);
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                        reinterpret_cast<uint64_t>(map)),
+                    "r"(smem_addr(sbuf)), "r"(x), "r"(y)
+                    : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+              }
+              continue;
+            }
+            if (valid_rows == 0) continue;
+          }
           __nv_bfloat16* dst;
           int64_t ld;
           if constexpr (kW) {
@@ -505,6 +546,8 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
       acc ^= 1;
       if (acc == 0) aphase ^= 1u;
     }
+    if constexpr (kW)
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the last stores completed
   }
 
   tc_fence_before_sync();
@@ -520,25 +563,28 @@ int tile_n_for(int n) { return n % 256 == 0 ? 256 : n % 128 == 0 ? 128 : 64; }
 
 template <int BN, Mode M>
 cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const Params& prm, int64_t max_tiles,
-                        int num_sms, cudaStream_t stream) {
+                        int num_sms, cudaStream_t stream, const CUtensorMap* mo1 = nullptr,
+                        const CUtensorMap* mo2 = nullptr) {
   using C = Cfg<BN, M>;
   const size_t smem = 1024 + static_cast<size_t>(C::kStages) * C::kStageBytes + sizeof(Smem) +
-                      2 * static_cast<size_t>(prm.E + 1) * sizeof(int32_t) + 16 + kStoreStageBytes;
+                      2 * static_cast<size_t>(prm.E + 1) * sizeof(int32_t) + 1024 + kStoreStageBytes;
   auto kernel = grouped_gemm_bwd_kernel<BN, M>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
-  kernel<<<grid, kThreads, smem, stream>>>(ma, mb, prm);
+  // output maps: the weight gradients' TMA stores (other modes pass an unused copy)
+  kernel<<<grid, kThreads, smem, stream>>>(ma, mb, mo1 ? *mo1 : ma, mo2 ? *mo2 : ma, prm);
   return cudaGetLastError();
 }
 
 template <Mode M>
 cudaError_t launch_tile_n(int bn, const CUtensorMap& ma, const CUtensorMap& mb, const Params& prm,
-                          int64_t max_tiles, int num_sms, cudaStream_t stream) {
+                          int64_t max_tiles, int num_sms, cudaStream_t stream, const CUtensorMap* mo1 = nullptr,
+                          const CUtensorMap* mo2 = nullptr) {
   switch (bn) {
-    case 256: return launch_mode<256, M>(ma, mb, prm, max_tiles, num_sms, stream);
-    case 128: return launch_mode<128, M>(ma, mb, prm, max_tiles, num_sms, stream);
-    default: return launch_mode<64, M>(ma, mb, prm, max_tiles, num_sms, stream);
+    case 256: return launch_mode<256, M>(ma, mb, prm, max_tiles, num_sms, stream, mo1, mo2);
+    case 128: return launch_mode<128, M>(ma, mb, prm, max_tiles, num_sms, stream, mo1, mo2);
+    default: return launch_mode<64, M>(ma, mb, prm, max_tiles, num_sms, stream, mo1, mo2);
   }
 }
 
@@ -659,8 +705,11 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
     prm.M_ext = a.f;
     prm.N_ext = a.d;
     prm.out = static_cast<__nv_bfloat16*>(a.dw_down);
+    CUtensorMap mo;  // dW_down [E * f, d]: 32 x 32 store boxes
+    if (!make_bf16_map_2d_sw64(&mo, a.dw_down, static_cast<int64_t>(a.E) * a.f, a.d, 32, 32))
+      return cudaErrorInvalidValue;
     err = launch_tile_n<Mode::kWgrad>(bn, ma, mb, prm, static_cast<int64_t>(a.E) * prm.m_tiles * prm.n_tiles, num_sms,
-                                      stream);
+                                      stream, &mo, &mo);
     if (err != cudaSuccess) return err;
   }
   if ((err = mark(2)) != cudaSuccess) return err;
@@ -683,8 +732,12 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
     prm.out = static_cast<__nv_bfloat16*>(a.dw_gate);
     prm.out2 = static_cast<__nv_bfloat16*>(a.dw_up);
     prm.out_cols = a.f;
+    CUtensorMap mg, mu;  // dW_gate, dW_up [E * d, f]: 32 x 32 store boxes
+    if (!make_bf16_map_2d_sw64(&mg, a.dw_gate, static_cast<int64_t>(a.E) * a.d, a.f, 32, 32) ||
+        !make_bf16_map_2d_sw64(&mu, a.dw_up, static_cast<int64_t>(a.E) * a.d, a.f, 32, 32))
+      return cudaErrorInvalidValue;
     err = launch_tile_n<Mode::kWgrad>(bn, ma, mb, prm, static_cast<int64_t>(a.E) * prm.m_tiles * prm.n_tiles, num_sms,
-                                      stream);
+                                      stream, &mg, &mu);
     if (err != cudaSuccess) return err;
   }
   return mark(3);

@@ -157,6 +157,8 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
 bool make_bf16_map_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
 bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int box0, int box1,
                       int box2 = 1);
+bool make_bf16_map_2d_sw64(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols,
+                           int box_rows);
 bool make_bf16_map_col_blocks(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows,
                               int box_blocks);
 

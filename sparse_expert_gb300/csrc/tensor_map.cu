@@ -28,12 +28,12 @@ EncodeTiledFn encode_fn() {
 }
 
 bool encode(CUtensorMap* map, const void* ptr, cuuint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides,
-            const cuuint32_t* box) {
+            const cuuint32_t* box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -44,6 +44,16 @@ bool make_bf16_map_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t c
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   return encode(map, ptr, 2, dims, strides, box);
+}
+
+// The same with 64-byte swizzling (boxes of 32 bf16 columns): the 16-byte
+// pieces of row r of a 512-byte atom are permuted by (r >> 1) & 3.
+bool make_bf16_map_2d_sw64(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols,
+                           int box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  return encode(map, ptr, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int box0, int box1,
