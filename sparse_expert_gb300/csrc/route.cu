@@ -16,11 +16,16 @@ constexpr int kRouteWarps = 8;  // tokens per block
 // is the float's bits made monotone (negative values inverted, sign bit set
 // on the others) after folding -0.0 onto +0.0; the low word decreases with
 // the expert index.  Key 0 is below every finite logit's key.
-__device__ __forceinline__ uint64_t route_key(float x, int e) {
-  uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+__device__ __forceinline__ uint32_t route_hi(float x) {
+  const uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+
+__device__ __forceinline__ uint64_t route_key_hi(uint32_t hi, int e) {
+  return (static_cast<uint64_t>(hi) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+
+__device__ __forceinline__ uint64_t route_key(float x, int e) { return route_key_hi(route_hi(x), e); }
 
 __device__ __forceinline__ float key_logit(uint64_t key) {
   uint32_t u = static_cast<uint32_t>(key >> 32);
@@ -41,13 +46,16 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t b) {
   return b;
 }
 
-// Bitonic sort of one key per lane into descending lane order.
-__device__ __forceinline__ uint64_t warp_sort_desc_u64(uint64_t v, int lane) {
+// Bitonic sort of one key per lane over each aligned group of W lanes.
+// Lanes 0 .. W-1 end in descending order (the other groups alternate in
+// direction, as the network leaves them before a wider merge).
+template <int W, typename Key>
+__device__ __forceinline__ Key warp_sort_desc(Key v, int lane) {
 #pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
+  for (int size = 2; size <= W; size <<= 1) {
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const Key o = __shfl_xor_sync(0xffffffffu, v, stride);
       const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
       v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
     }
@@ -55,9 +63,50 @@ __device__ __forceinline__ uint64_t warp_sort_desc_u64(uint64_t v, int lane) {
   return v;
 }
 
+// Exact top-k of one token's keys by k rounds of warp arg-max: round j takes
+// the warp maximum of the lanes' best keys, and only the lane that held it
+// drops that key and rescans its own values.  Lane j < k gets the j-th key.
+template <int NV>
+__device__ __forceinline__ uint64_t topk_rounds(const float (&v)[NV], int E, int k, int lane) {
+  uint64_t key[NV];
+  uint64_t lbest = 0;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = (e < E) ? route_key(v[i], e) : 0ull;
+    lbest = key[i] > lbest ? key[i] : lbest;
+  }
+  uint64_t mine = 0;
+  for (int j = 0; j < k; ++j) {
+    const uint64_t b = warp_max_u64(lbest);
+    if (lane == j) mine = b;
+    if (lbest == b) {  // keys are unique: exactly one lane held it
+      lbest = 0;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        if (key[i] == b) key[i] = 0;
+        lbest = key[i] > lbest ? key[i] : lbest;
+      }
+    }
+  }
+  return mine;
+}
+
 // NV logits per lane: lane l holds experts l, l+32, ..., l+32*(NV-1).
-// Round j takes the warp maximum of the lanes' best keys; only the lane
-// that held it drops that key and rescans its own values.
+//
+// Without groups the selection first narrows the field.  Let H be the k-th
+// largest of the 32 lanes' maximum high words (the logit part of the key).
+// At least k lanes hold a logit whose high word is >= H, so the k-th
+// largest key has a high word >= H and every selected expert is among the
+// candidates with high word >= H.  (If H is the 0 of a lane without
+// experts, every expert is a candidate.)  For N(0,1) logits over 384
+// experts there are about nine candidates; when they number at most 32 the
+// warp gathers their full keys into one lane each and a bitonic sort of
+// the smallest width that holds them puts the k winners in lanes 0..k-1.
+// Otherwise (wide ties) the k rounds of topk_rounds decide.  Both give the
+// k largest keys in descending order, so the result does not depend on the
+// path taken.
+//
 // With n_groups > 1 ("Training a 1T-Params MoE on EU public
 // infrastructure", Group-limited expert routing), group g = experts
 // [g*E/G, (g+1)*E/G) gets k/G rounds restricted to its own experts, and a
@@ -67,46 +116,72 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int n_groups, int renormalize,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts) {
   extern __shared__ int32_t s_hist[];  // [E] when counts != nullptr
+  __shared__ uint64_t s_cand[kRouteWarps * 32];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   if (counts) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
   }
+  uint64_t* cand = s_cand + warp * 32;
 
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kRouteWarps;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp; t < T; t += warps_total) {
     const float* row = logits + t * E;
     float v[NV];
-    uint64_t key[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       v[i] = (e < E) ? __ldg(row + e) : 0.0f;
     }
-    uint64_t lbest = 0;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      key[i] = (e < E) ? route_key(v[i], e) : 0ull;
-      lbest = key[i] > lbest ? key[i] : lbest;
-    }
     uint64_t mine = 0, first = 0;
     if (n_groups == 1) {
-      for (int j = 0; j < k; ++j) {
-        const uint64_t b = warp_max_u64(lbest);
-        if (j == 0) first = b;
-        if (lane == j) mine = b;
-        if (lbest == b) {  // keys are unique: exactly one lane held it
-          lbest = 0;
+      uint32_t hw[NV];
+      uint32_t hm = 0;
 #pragma unroll
-          for (int i = 0; i < NV; ++i) {
-            if (key[i] == b) key[i] = 0;
-            lbest = key[i] > lbest ? key[i] : lbest;
-          }
-        }
+      for (int i = 0; i < NV; ++i) {
+        hw[i] = route_hi(v[i]);
+        if (lane + 32 * i < E) hm = max(hm, hw[i]);
       }
+      const uint32_t H = __shfl_sync(0xffffffffu, warp_sort_desc<32>(hm, lane), k - 1);
+      uint32_t cnt = 0;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) cnt += (lane + 32 * i < E && hw[i] >= H) ? 1u : 0u;
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, s);
+        if (lane >= s) incl += o;
+      }
+      const uint32_t C = __shfl_sync(0xffffffffu, incl, 31);
+      if (C <= 32) {
+        uint32_t pos = incl - cnt;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E && hw[i] >= H) cand[pos++] = route_key_hi(hw[i], e);
+        }
+        __syncwarp();
+        uint64_t c = (static_cast<uint32_t>(lane) < C) ? cand[lane] : 0ull;
+        __syncwarp();
+        if (C <= 8)
+          c = warp_sort_desc<8>(c, lane);
+        else if (C <= 16)
+          c = warp_sort_desc<16>(c, lane);
+        else
+          c = warp_sort_desc<32>(c, lane);
+        mine = c;
+      } else {
+        mine = topk_rounds<NV>(v, E, k, lane);
+      }
+      first = __shfl_sync(0xffffffffu, mine, 0);
     } else {
+      uint64_t key[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = (e < E) ? route_key(v[i], e) : 0ull;
+      }
       const int gsize = E / n_groups, per = k / n_groups;
       int j = 0;
       for (int g = 0; g < n_groups; ++g) {
@@ -125,7 +200,7 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
             if (key[i] == b) key[i] = 0;
         }
       }
-      mine = warp_sort_desc_u64(mine, lane);  // lanes >= k hold key 0
+      mine = warp_sort_desc<32>(mine, lane);  // lanes >= k hold key 0
       first = __shfl_sync(0xffffffffu, mine, 0);
     }
     const float mx = key_logit(first);
