@@ -13,9 +13,10 @@
 //      (warp match + per-warp running counts), publishes its per-expert
 //      aggregate, and takes the exclusive per-expert prefix of all earlier
 //      blocks by decoupled look-back (Merrill & Garland's single-pass scan,
-//      applied to an E-wide vector).  Block order comes from an atomic
-//      ticket, so a block only ever waits for blocks that are already
-//      running, and every wait is bounded.
+//      applied to an E-wide vector, with the predecessors' flags read 32 at
+//      a time so that the walk costs one round trip per 32 blocks).  Block
+//      order comes from an atomic ticket, so a block only ever waits for
+//      blocks that are already running, and every wait is bounded.
 #include "common.cuh"
 #include "internal.h"
 
@@ -142,20 +143,28 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
   for (int i = tid; i < kWarps * E; i += kDispatchThreads) s_warp[i] = 0;
   __syncthreads();
   const int64_t b = s_block;
+  // this thread's pairs and gates, all in flight before the scan below
+  const int64_t base = b * kDispatchChunk + static_cast<int64_t>(warp) * (32 * kDispatchPairsPerThread);
+  int my_e[kDispatchPairsPerThread];
+  float my_w[kDispatchPairsPerThread];
+#pragma unroll
+  for (int r = 0; r < kDispatchPairsPerThread; ++r) {
+    const int64_t p = base + r * 32 + lane;
+    my_e[r] = (p < P) ? __ldcg(topk_idx + p) : -1;
+    my_w[r] = (p < P && row_w) ? __ldcg(topk_w + p) : 0.0f;
+  }
   block_exclusive_scan(s_cnt, s_off, E, s_tmp);
   if (b == 0)
     for (int e = tid; e <= E; e += kDispatchThreads) offsets[e] = s_off[e];
 
   // rank each pair among the earlier pairs of its warp with the same expert
-  const int64_t base = b * kDispatchChunk + static_cast<int64_t>(warp) * (32 * kDispatchPairsPerThread);
-  int my_e[kDispatchPairsPerThread];
   int my_rank[kDispatchPairsPerThread];
   bool bad = false;
   const unsigned lanes_below = (1u << lane) - 1u;
 #pragma unroll
   for (int r = 0; r < kDispatchPairsPerThread; ++r) {
     const int64_t p = base + r * 32 + lane;
-    int e = (p < P) ? __ldg(topk_idx + p) : -1;
+    int e = my_e[r];
     if (p < P && (e < 0 || e >= E)) {
       bad = true;
       e = -1;
@@ -188,35 +197,51 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
   __syncthreads();
   if (tid == 0) store_release(&flags[b], b == 0 ? kFlagInclusive : kFlagAggregate);
 
-  // decoupled look-back over the earlier blocks
+  // decoupled look-back over the earlier blocks, a window of 32 at a time:
+  // warp 0 reads the flags of blocks hi, hi-1, ..., hi-31 at once and waits
+  // (bounded) until each has published at least its aggregate; the block
+  // then adds the vectors of the blocks from hi down to the nearest one that
+  // has published its inclusive prefix, or of the whole window, and goes on
+  // below it.  Block 0 publishes its inclusive prefix first, so the walk
+  // ends there at the latest.
   if (b > 0) {
-    int64_t pred = b - 1;
+    int64_t hi = b - 1;
     for (;;) {
-      if (tid == 0) {
-        int32_t f = load_acquire(flags + pred);
-        if (f == 0) {
+      if (warp == 0) {
+        const int64_t c = hi - lane;
+        int32_t f = (c >= 0) ? load_acquire(flags + c) : kFlagAggregate;
+        if (__any_sync(0xffffffffu, f == 0)) {
           const uint64_t t0 = global_timer_ns();
-          while ((f = load_acquire(flags + pred)) == 0) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-              f = -1;
+          for (;;) {
+            __nanosleep(64);
+            if (f == 0) f = load_acquire(flags + c);
+            if (!__any_sync(0xffffffffu, f == 0)) break;
+            if (__any_sync(0xffffffffu, global_timer_ns() - t0 > kWaitLimitNs)) {
+              if (f == 0) f = -1;
               break;
             }
-            __nanosleep(64);
           }
         }
-        s_flag = f;
+        const unsigned inclusive = __ballot_sync(0xffffffffu, c >= 0 && f == kFlagInclusive);
+        const bool lost = __any_sync(0xffffffffu, f < 0);
+        // lane of the nearest inclusive block, 32 when the window has none
+        if (lane == 0) s_flag = lost ? -1 : (inclusive ? __ffs(inclusive) - 1 : 32);
       }
       __syncthreads();
-      const int32_t f = s_flag;
-      if (f < 0) {
+      const int32_t stop = s_flag;
+      if (stop < 0) {
         if (tid == 0) record_status(&hdr->status, kStatusTimeout);
         return;  // successors walk past this block on its aggregate
       }
-      const int32_t* src = (f == kFlagInclusive ? incl : agg) + pred * E;
-      for (int e = tid; e < E; e += kDispatchThreads) s_excl[e] += __ldcg(src + e);
+      for (int e = tid; e < E; e += kDispatchThreads) {
+        int32_t acc = (stop < 32) ? __ldcg(incl + (hi - stop) * E + e) : 0;
+#pragma unroll 8
+        for (int i = 0; i < min(stop, 32); ++i) acc += __ldcg(agg + (hi - i) * E + e);
+        s_excl[e] += acc;
+      }
       __syncthreads();  // s_flag is rewritten next round
-      if (f == kFlagInclusive) break;
-      --pred;
+      if (stop < 32) break;
+      hi -= 32;
     }
     for (int e = tid; e < E; e += kDispatchThreads) incl[b * E + e] = s_excl[e] + s_agg[e];
     __threadfence();
@@ -237,7 +262,7 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
     const int32_t row = s_off[e] + s_excl[e] + s_warp[warp * E + e] + my_rank[r];
     dest_row[p] = row;
     src_token[row] = static_cast<int32_t>(p / k);
-    if (row_w) row_w[row] = __ldg(topk_w + p);
+    if (row_w) row_w[row] = my_w[r];
   }
 }
 

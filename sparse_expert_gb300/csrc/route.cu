@@ -112,7 +112,7 @@ __device__ __forceinline__ uint64_t topk_rounds(const float (&v)[NV], int E, int
 // [g*E/G, (g+1)*E/G) gets k/G rounds restricted to its own experts, and a
 // warp sort puts the k winners back in descending slot order.
 template <int NV>
-__global__ void __launch_bounds__(kRouteWarps * 32)
+__global__ void __launch_bounds__(kRouteWarps * 32, NV <= 12 ? 4 : NV <= 16 ? 2 : 1)
 route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int n_groups, int renormalize,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts) {
   extern __shared__ int32_t s_hist[];  // [E] when counts != nullptr
