@@ -37,9 +37,14 @@
 //     Silu(gate)*up in fp32 and store H[token, j] (and, for the backward's
 //     recomputation, the raw G and U);
 //   rows: Y[token, i] or dX[token, i] as they are, or scaled by a gate per
-//     token;
+//     token; a warp reads its last kHold chunks into registers (bf16) before
+//     it hands the accumulator back, so their stores overlap the next
+//     tile's MMAs;
 //   SwiGLU backward: dH with the saved G, U of the same rows (ldmatrix.trans
 //     turns their token rows into the fragment), stores dG and dU.
+//
+// The kernel is instantiated once per epilogue, so that each gets the
+// registers of its own epilogue (10 warps: at most 168 per thread).
 //
 // Roles in each CTA of the pair (320 threads): warp 0 TMA producer (both
 // CTAs load their halves; every copy signals the leader's stage barrier),
@@ -74,6 +79,7 @@ constexpr int kBBytes = kHalfRows * BK * 2;          // one token part
 constexpr int kStageBytes = kABytes + 2 * kBBytes;   // A | B part 1 | B part 2
 constexpr int kEpiParts = 2;     // epilogue warps per TMEM lane quadrant, each a share of the token chunks
 constexpr int kEpiWarps = 4 * kEpiParts;
+constexpr int kHold = 4;        // row-epilogue chunks a warp holds in registers across the hand-back
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;    // one accumulator: the tile's weight rows x up to 512 tokens
 constexpr int kEpiBytes = kEpiWarps * 32 * 64;   // per epilogue warp 2 KB: SwiGLU exchange, then transpose
@@ -249,6 +255,9 @@ __device__ __forceinline__ void pack_chunk(const uint32_t (&a)[16], const uint32
   }
 }
 
+// One instantiation per epilogue mode, so that each mode's registers are
+// allocated for its own epilogue.
+template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                         const Params p) {
@@ -509,12 +518,12 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         released = true;
       };
       uint32_t a[16], b[16];
-      if (c_begin < c_end) {
+      if (c_begin < c_end && kMode != kModeRows) {
         tmem_ld_16x256b_x4(taddr + c_begin, a);
         tmem_ld_16x256b_x4(taddr_b + c_begin, b);
         tmem_ld_wait();
       }
-      if (p.mode == kModeSwiGLU) {
+      if constexpr (kMode == kModeSwiGLU) {
         // lanes of quads 0/1: gate features j0 + 32*(quad&1) + lane; quads
         // 2/3: the up features of the same j.  The gate warp keeps token
         // columns 0-15 of each chunk, the up warp 16-31.
@@ -598,7 +607,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           rows_to_global<16>(tbuf, lane, hcol + static_cast<int64_t>(r0) * p.out_cols, p.out_cols, x.valid - r0);
           if (c + 32 < c_end) tmem_ld_wait();
         }
-      } else if (p.mode == kModeSwiGLUBwd) {
+      } else if constexpr (kMode == kModeSwiGLUBwd) {
         // lanes: features j0 .. j0+31 of dH (gate features of the packed
         // interleave: gate column (j / 64) * 128 + j % 64, up 64 further on)
         const int j0 = x.mt * 2 * kHalfRows + static_cast<int>(rank) * kHalfRows + quad * 32;
@@ -661,39 +670,68 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           if (c + 32 < c_end) tmem_ld_wait();
         }
       } else {
-        // lanes: output features i0 + lane; columns: tokens
+        // lanes: output features i0 + lane; columns: tokens.  The warp's last
+        // kHold chunks are read from TMEM into registers (as bf16 pairs)
+        // before the accumulator goes back to the MMA, so that their staging
+        // and stores overlap the next tile's MMAs; earlier chunks (tiles of
+        // more than 2 * 32 * kHold tokens) are stored as they are read.
         const int i0 = x.mt * 2 * kHalfRows + static_cast<int>(rank) * kHalfRows + quad * 32;
         __nv_bfloat16* ycol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + i0;
-#pragma unroll 1
-        for (int c = c_begin; c < c_end; c += 32) {
-          if (c + 32 >= c_end) release();
-          if (p.row_scale != nullptr) {
-            // lane i loads the gate of token column c + i; thread i's columns
-            // are 8g + 2(i%4) and +1
-            const float s_l = c + lane < x.valid ? __ldg(p.row_scale + x.tok0 + c + lane) : 1.0f;
+        auto scale = [&](uint32_t (&v)[16], int c) {
+          if (p.row_scale == nullptr) return;
+          // lane i loads the gate of token column c + i; thread i's columns
+          // are 8g + 2(i%4) and +1
+          const float s_l = c + lane < x.valid ? __ldg(p.row_scale + x.tok0 + c + lane) : 1.0f;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float s0 = __shfl_sync(0xffffffffu, s_l, 8 * g + 2 * (lane & 3));
+            const float s1 = __shfl_sync(0xffffffffu, s_l, 8 * g + 2 * (lane & 3) + 1);
+            v[4 * g] = __float_as_uint(s0 * __uint_as_float(v[4 * g]));
+            v[4 * g + 1] = __float_as_uint(s1 * __uint_as_float(v[4 * g + 1]));
+            v[4 * g + 2] = __float_as_uint(s0 * __uint_as_float(v[4 * g + 2]));
+            v[4 * g + 3] = __float_as_uint(s1 * __uint_as_float(v[4 * g + 3]));
+          }
+        };
+        // chunk c as a bf16 fragment (see pack_chunk), read from TMEM one
+        // 16-lane half at a time
+        auto fill = [&](int c, uint32_t (&pk)[16]) {
+          uint32_t v[16];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            tmem_ld_16x256b_x4((half ? taddr_b : taddr) + c, v);
+            tmem_ld_wait();
+            scale(v, c);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              const float s0 = __shfl_sync(0xffffffffu, s_l, 8 * g + 2 * (lane & 3));
-              const float s1 = __shfl_sync(0xffffffffu, s_l, 8 * g + 2 * (lane & 3) + 1);
-              a[4 * g] = __float_as_uint(s0 * __uint_as_float(a[4 * g]));
-              a[4 * g + 1] = __float_as_uint(s1 * __uint_as_float(a[4 * g + 1]));
-              a[4 * g + 2] = __float_as_uint(s0 * __uint_as_float(a[4 * g + 2]));
-              a[4 * g + 3] = __float_as_uint(s1 * __uint_as_float(a[4 * g + 3]));
-              b[4 * g] = __float_as_uint(s0 * __uint_as_float(b[4 * g]));
-              b[4 * g + 1] = __float_as_uint(s1 * __uint_as_float(b[4 * g + 1]));
-              b[4 * g + 2] = __float_as_uint(s0 * __uint_as_float(b[4 * g + 2]));
-              b[4 * g + 3] = __float_as_uint(s1 * __uint_as_float(b[4 * g + 3]));
+              pk[4 * g + 2 * half] = pack_bf16x2(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]));
+              pk[4 * g + 2 * half + 1] = pack_bf16x2(__uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
             }
           }
+        };
+        const int n_chunks = c_begin < c_end ? (c_end - c_begin + 31) >> 5 : 0;
+        const int n_stream = max(n_chunks - kHold, 0);
+#pragma unroll 1
+        for (int i = 0; i < n_stream; ++i) {
+          const int c = c_begin + 32 * i;
           uint32_t pk[16];
-          pack_chunk(a, b, pk);
-          if (c + 32 < c_end) {
-            tmem_ld_16x256b_x4(taddr + c + 32, a);
-            tmem_ld_16x256b_x4(taddr_b + c + 32, b);
-          }
+          fill(c, pk);
           stage_rows<4>(pk, tbuf, lane);
           rows_to_global<32>(tbuf, lane, ycol + static_cast<int64_t>(c) * p.out_cols, p.out_cols, x.valid - c);
-          if (c + 32 < c_end) tmem_ld_wait();
+        }
+        uint32_t held[kHold][16];
+#pragma unroll
+        for (int h = 0; h < kHold; ++h) {
+          const int c = c_begin + 32 * (n_stream + h);
+          if (c < c_end) fill(c, held[h]);
+        }
+        release();
+#pragma unroll
+        for (int h = 0; h < kHold; ++h) {
+          const int c = c_begin + 32 * (n_stream + h);
+          if (c < c_end) {
+            stage_rows<4>(held[h], tbuf, lane);
+            rows_to_global<32>(tbuf, lane, ycol + static_cast<int64_t>(c) * p.out_cols, p.out_cols, x.valid - c);
+          }
         }
       }
       if (failed) break;
@@ -749,14 +787,16 @@ namespace {
 cudaError_t launch_pairs(const CUtensorMap& mw, const CUtensorMap& mx, const Params& prm, int64_t P, int num_sms,
                          cudaStream_t stream) {
   const size_t smem = grouped_gemm_2sm_smem(prm.E);
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  auto* kernel = prm.mode == kModeSwiGLU      ? grouped_gemm_2sm_kernel<kModeSwiGLU>
+                 : prm.mode == kModeSwiGLUBwd ? grouped_gemm_2sm_kernel<kModeSwiGLUBwd>
+                                              : grouped_gemm_2sm_kernel<kModeRows>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   // persistent: one pair per two SMs, never more pairs than an upper bound on tiles
   const int64_t max_tiles = (P / kTileN + prm.E) * static_cast<int64_t>(prm.m_tiles);
   int pairs = num_sms / 2;
   if (max_tiles < pairs) pairs = static_cast<int>(max_tiles);
-  grouped_gemm_2sm_kernel<<<2 * pairs, kThreads, smem, stream>>>(mw, mx, prm);
+  kernel<<<2 * pairs, kThreads, smem, stream>>>(mw, mx, prm);
   return cudaGetLastError();
 }
 
