@@ -30,12 +30,12 @@
 // token rows in shared memory so every global access covers whole
 // token-row segments):
 //   gate/up: a tile's 256 weight rows are two packed gate/up tiles of 64
-//     gate then the same 64 up columns, one per CTA, so TMEM lanes 0-63 of
-//     a CTA hold gate features j..j+63 and lanes 64-127 the up features of
-//     the same j.  The warps of lanes 0-31 and 64-95 (and 32-63 with
-//     96-127) swap half of their token columns through shared memory, form
-//     Silu(gate)*up in fp32 and store H[token, j] (and, for the backward's
-//     recomputation, the raw G and U);
+//     gate then the same 64 up columns, one per CTA, loaded by a 4-D tensor
+//     map in quarter order: each 32-lane TMEM quadrant holds 16 gate
+//     features and, 16 lanes further on, the same 16 up features, so each
+//     warp forms Silu(gate)*up in fp32 from its own two 16-lane loads and
+//     stores H[token, j] for its 16 features (and, for the backward's
+//     recomputation, the raw G and U in the packed column order);
 //   rows: Y[token, i] or dX[token, i] as they are, or scaled by a gate per
 //     token; a warp reads its last kHold chunks into registers (bf16) before
 //     it hands the accumulator back, so their stores overlap the next
@@ -80,9 +80,10 @@ constexpr int kStageBytes = kABytes + 2 * kBBytes;   // A | B part 1 | B part 2
 constexpr int kEpiParts = 2;     // epilogue warps per TMEM lane quadrant, each a share of the token chunks
 constexpr int kEpiWarps = 4 * kEpiParts;
 constexpr int kHold = 4;        // row-epilogue chunks a warp holds in registers across the hand-back
+constexpr int kHoldH = 4;       // the same for the chunks of H in the gate/up epilogue
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;    // one accumulator: the tile's weight rows x up to 512 tokens
-constexpr int kEpiBytes = kEpiWarps * 32 * 64;   // per epilogue warp 2 KB: SwiGLU exchange, then transpose
+constexpr int kEpiBytes = kEpiWarps * 32 * 64;   // per epilogue warp 2 KB: the staging of its stores
 constexpr int kRing = 4;                          // tile ids published ahead
 // readers of a ring slot, counted on the leader's rempty: the leader's MMA
 // thread and epilogue warps, the peer's producer and epilogue warps
@@ -117,7 +118,6 @@ struct Params {
 struct Smem {
   uint64_t full[kStages], empty[kStages];
   uint64_t tfull[2], tempty[2];
-  uint64_t xsync[2 * kEpiParts];  // SwiGLU: one per pair of partner epilogue warps
   uint64_t rfull[kRing], rempty[kRing];
   int32_t ring[kRing];
   uint64_t drain;
@@ -199,6 +199,52 @@ __device__ __forceinline__ void rows_to_global(const uint8_t* buf, int lane, __n
     const int r = idx >> 2;
     const int q = idx & 3;
     const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+    if (r < valid) *reinterpret_cast<uint4*>(out + r * ld + q * 8) = v;
+  }
+  __syncwarp();
+}
+
+// rows_to_global with the row's first 32 bytes going to out and its last
+// 32 bytes to out + hi (elements).
+__device__ __forceinline__ void rows_to_global_split(const uint8_t* buf, int lane, __nv_bfloat16* out, int hi,
+                                                     int64_t ld, int valid) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = i * 32 + lane;
+    const int r = idx >> 2;
+    const int q = idx & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+    if (r < valid) *reinterpret_cast<uint4*>(out + r * ld + (q < 2 ? q * 8 : hi + (q - 2) * 8)) = v;
+  }
+  __syncwarp();
+}
+
+// A warp's 16-feature staging buffer: 32 token rows of 32 bytes, the
+// 16-byte half h of row t at position h ^ ((t >> 2) & 1), so that both the
+// stmatrix writes and the row reads are free of bank conflicts.  p[2g + m]
+// holds features 8m .. 8m+7 of tokens 8g .. 8g+7 as an stmatrix fragment
+// (thread i: feature 8m + i/4 of tokens 8g + 2(i%4) and +1).
+__device__ __forceinline__ void stage_rows_16f(const uint32_t (&p)[8], uint8_t* buf, int lane) {
+  const int j = lane >> 3;  // the matrix of each x4 whose row this lane addresses: (m = j & 1, g = 2s + j / 2)
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int r = 8 * (2 * s + (j >> 1)) + (lane & 7);
+    stmatrix_x4_trans(smem_addr(buf) + r * 32 + (((j & 1) ^ ((r >> 2) & 1)) << 4), p[4 * s], p[4 * s + 1],
+                      p[4 * s + 2], p[4 * s + 3]);
+  }
+  __syncwarp();
+}
+
+// Rows 0 .. 31 of a 16-feature staging buffer to out (row stride ld), rows
+// >= valid skipped: each 16-byte store instruction covers 16 rows x 32 bytes.
+__device__ __forceinline__ void rows16f_to_global(const uint8_t* buf, int lane, __nv_bfloat16* out, int64_t ld,
+                                                  int valid) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int idx = i * 32 + lane;
+    const int r = idx >> 1;
+    const int q = idx & 1;
+    const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 32 + ((q ^ ((r >> 2) & 1)) << 4));
     if (r < valid) *reinterpret_cast<uint4*>(out + r * ld + q * 8) = v;
   }
   __syncwarp();
@@ -307,7 +353,6 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       mbar_init(&S->tfull[i], 1);
       mbar_init(&S->tempty[i], 2 * kEpiWarps);  // both CTAs' epilogue warps (leader's copy is used)
     }
-    for (int i = 0; i < 2 * kEpiParts; ++i) mbar_init(&S->xsync[i], 2);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&S->rfull[i], 1);
       mbar_init(&S->rempty[i], kRingReaders);  // the leader's copy is used
@@ -387,6 +432,10 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             const int k0 = kb * BK;
             const int blk = (x.e * p.a_tiles + k0 / p.a_tile_rows) * p.a_mblocks + w0 / 64;
             tma_load_3d_pair(st, &tm_w, lead_full, 0, k0 % p.a_tile_rows, blk);
+          } else if constexpr (kMode == kModeSwiGLU) {
+            // the packed gate/up tile in quarter order (16 gate rows, then
+            // their 16 up rows): 8 groups of 16 rows per block
+            tma_load_4d_pair(st, &tm_w, lead_full, 0, 0, 0, (wblk + kb) * 8);
           } else {
             tma_load_3d_pair(st, &tm_w, lead_full, 0, wrow, wblk + kb);
           }
@@ -469,13 +518,10 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     const int quad = warp & 3;            // TMEM lanes 32*quad .. +31
     const int part = (warp - 2) >> 2;     // which share of the tile's 32-token chunks
     const int ew = warp - 2;
-    // one 2 KB buffer per warp: the SwiGLU exchange with the partner warp,
-    // then (the partner having read it) the transpose of the warp's stores
-    uint8_t* xbuf = s_epi + ew * 2048;
-    uint8_t* tbuf = xbuf;
+    // one 2 KB buffer per warp: the staging of its stores
+    uint8_t* tbuf = s_epi + ew * 2048;
     const uint32_t lead_tempty = leader_addr(&S->tempty[0]);
     uint32_t aphase = 0;
-    uint32_t xparity = 0;
     int rs = 0;
     uint32_t rphase = 0;
     const uint32_t lead_rempty0 = leader_addr(&S->rempty[0]);
@@ -524,88 +570,69 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         tmem_ld_wait();
       }
       if constexpr (kMode == kModeSwiGLU) {
-        // lanes of quads 0/1: gate features j0 + 32*(quad&1) + lane; quads
-        // 2/3: the up features of the same j.  The gate warp keeps token
-        // columns 0-15 of each chunk, the up warp 16-31.
-        const bool is_gate = quad < 2;
-        const int j = (x.mt * 2 + static_cast<int>(rank)) * 64 + (quad & 1) * 32 + lane;
-        // packed gate/up tile t = 2*mt + rank: TMEM lane l is interleaved
-        // column 128t + l of G,U (gate 64t.. then up 64t..)
+        // The weight rows arrive in quarter order, so TMEM lanes 32q .. 32q+15
+        // hold gate features j0 .. j0+15 (j0 = 64t + 16q of packed gate/up
+        // tile t = 2*mt + rank) and lanes 32q+16 .. 32q+31 the up features of
+        // the same j: a thread's registers of the two 16-lane loads pair up
+        // element by element, and Silu(gate)*up needs no exchange.
+        const int tp = x.mt * 2 + static_cast<int>(rank);
+        __nv_bfloat16* hcol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + tp * 64 + quad * 16;
+        // G,U for the backward: packed columns 128t + 16q (gate) and +64 (up)
         __nv_bfloat16* gucol =
-            p.gu ? p.gu + static_cast<int64_t>(x.tok0) * 2 * p.out_cols + (x.mt * 2 + static_cast<int>(rank)) * 128 +
-                       quad * 32
-                 : nullptr;
-        uint64_t* xsync = &S->xsync[(quad & 1) + 2 * part];    // shared with the partner warp
-        uint8_t* my_x = xbuf;
-        uint8_t* partner_x = s_epi + (ew ^ 2) * 2048;           // quad ^ 2, same part
-        __nv_bfloat16* hcol = p.out + static_cast<int64_t>(x.tok0) * p.out_cols + (j - lane);
-#pragma unroll 1
-        for (int c = c_begin; c < c_end; c += 32) {
-          if (c + 32 >= c_end) release();
+            p.gu ? p.gu + static_cast<int64_t>(x.tok0) * 2 * p.out_cols + tp * 128 + quad * 16 : nullptr;
+        // chunk c (in a, b): G,U stored if requested, then H as an stmatrix
+        // fragment; the next chunk's TMEM loads are issued once a, b are read
+        auto swiglu_chunk = [&](int c, uint32_t (&ph)[8]) {
           if (gucol != nullptr) {  // the raw pre-activations, for the backward
             uint32_t pk[16];
             pack_chunk(a, b, pk);
             stage_rows<4>(pk, tbuf, lane);
-            rows_to_global<32>(tbuf, lane, gucol + static_cast<int64_t>(c) * 2 * p.out_cols, 2 * p.out_cols,
-                               x.valid - c);
+            rows_to_global_split(tbuf, lane, gucol + static_cast<int64_t>(c) * 2 * p.out_cols, 64, 2 * p.out_cols,
+                                 x.valid - c);
           }
-          // token groups 0-1 (columns c .. c+15) stay with the gate warp, 2-3
-          // with the up warp; each sends the other half, 16 words per thread
-          // (static indices on both sides of the selects keep a, b in registers)
+          float h[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint32_t* src_up = q4 < 2 ? &a[4 * q4] : &b[4 * (q4 - 2)];
-            const uint32_t* src_gate = q4 < 2 ? &a[8 + 4 * q4] : &b[8 + 4 * (q4 - 2)];
-            const uint4 w_up = make_uint4(src_up[0], src_up[1], src_up[2], src_up[3]);
-            const uint4 w_gate = make_uint4(src_gate[0], src_gate[1], src_gate[2], src_gate[3]);
-            *reinterpret_cast<uint4*>(my_x + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4)) = is_gate ? w_gate : w_up;
-          }
-          if (!pair_sync(xsync, xparity, abort_flag)) {
-            failed = true;
-            break;
-          }
-          const int keep0 = is_gate ? 0 : 16;
-          // k = 0..7: features 0-15 (a), k = 8..15: features 16-31 (b) of the
-          // two kept token groups, in fragment order
-          float g[16], u[16];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint4 r = *reinterpret_cast<const uint4*>(partner_x + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4));
-            const float o[4] = {__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w)};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int k = 4 * q4 + i;
-              const uint32_t mine_gate = k < 8 ? a[k] : b[k - 8];
-              const uint32_t mine_up = k < 8 ? a[8 + k] : b[k];
-              const float mine = __uint_as_float(is_gate ? mine_gate : mine_up);
-              g[k] = is_gate ? mine : o[i];
-              u[k] = is_gate ? o[i] : mine;
-            }
-          }
+          for (int k = 0; k < 16; ++k) h[k] = silu_f32(__uint_as_float(a[k])) * __uint_as_float(b[k]);
           if (c + 32 < c_end) {
             tmem_ld_16x256b_x4(taddr + c + 32, a);
             tmem_ld_16x256b_x4(taddr_b + c + 32, b);
           }
-          if (!pair_sync(xsync, xparity, abort_flag)) {  // the partner has read my buffer
-            tmem_ld_wait();
-            failed = true;
-            break;
-          }
-          float h[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) h[k] = silu_f32(g[k]) * u[k];
+          for (int g = 0; g < 4; ++g) {
+            ph[2 * g] = pack_bf16x2(h[4 * g], h[4 * g + 1]);
+            ph[2 * g + 1] = pack_bf16x2(h[4 * g + 2], h[4 * g + 3]);
+          }
+        };
+        // as in the row epilogue, the warp's last kHoldH chunks of H stay in
+        // registers until the accumulator has been handed back
+        const int n_chunks = c_begin < c_end ? (c_end - c_begin + 31) >> 5 : 0;
+        const int n_stream = max(n_chunks - kHoldH, 0);
+#pragma unroll 1
+        for (int i = 0; i < n_stream; ++i) {
+          const int c = c_begin + 32 * i;
           uint32_t ph[8];
+          swiglu_chunk(c, ph);
+          stage_rows_16f(ph, tbuf, lane);
+          rows16f_to_global(tbuf, lane, hcol + static_cast<int64_t>(c) * p.out_cols, p.out_cols, x.valid - c);
+          tmem_ld_wait();
+        }
+        uint32_t held[kHoldH][8];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            ph[4 * t] = pack_bf16x2(h[4 * t], h[4 * t + 1]);
-            ph[4 * t + 1] = pack_bf16x2(h[4 * t + 2], h[4 * t + 3]);
-            ph[4 * t + 2] = pack_bf16x2(h[8 + 4 * t], h[8 + 4 * t + 1]);
-            ph[4 * t + 3] = pack_bf16x2(h[8 + 4 * t + 2], h[8 + 4 * t + 3]);
+        for (int hh = 0; hh < kHoldH; ++hh) {
+          const int c = c_begin + 32 * (n_stream + hh);
+          if (c < c_end) {
+            if (c + 32 >= c_end) release();
+            swiglu_chunk(c, held[hh]);
+            if (c + 32 < c_end) tmem_ld_wait();
           }
-          const int r0 = c + keep0;  // first token column of my 16
-          stage_rows<2>(ph, tbuf, lane);
-          rows_to_global<16>(tbuf, lane, hcol + static_cast<int64_t>(r0) * p.out_cols, p.out_cols, x.valid - r0);
-          if (c + 32 < c_end) tmem_ld_wait();
+        }
+#pragma unroll
+        for (int hh = 0; hh < kHoldH; ++hh) {
+          const int c = c_begin + 32 * (n_stream + hh);
+          if (c < c_end) {
+            stage_rows_16f(held[hh], tbuf, lane);
+            rows16f_to_global(tbuf, lane, hcol + static_cast<int64_t>(c) * p.out_cols, p.out_cols, x.valid - c);
+          }
         }
       } else if constexpr (kMode == kModeSwiGLUBwd) {
         // lanes: features j0 .. j0+31 of dH (gate features of the packed
@@ -821,7 +848,9 @@ cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, 
   const int num_kb = pb.K / BK;
   CUtensorMap mw, mx;
   const int64_t blocks = static_cast<int64_t>(pb.E) * (n_rows / a_tile_rows) * num_kb;
-  if (!make_bf16_map_3d(&mw, pb.b, BK, a_tile_rows, blocks, BK, kHalfRows)) return cudaErrorInvalidValue;
+  if (swiglu ? !make_bf16_map_gate_up_quads(&mw, pb.b, blocks)
+             : !make_bf16_map_3d(&mw, pb.b, BK, a_tile_rows, blocks, BK, kHalfRows))
+    return cudaErrorInvalidValue;
   if (!make_bf16_map_2d(&mx, pb.a, pb.P, pb.K, BK, kHalfRows)) return cudaErrorInvalidValue;
   Params prm = base_params(pb.offsets, pb.E, pb.K, pb.tile_counter, pb.status);
   prm.row_scale = swiglu ? nullptr : pb.row_scale;

@@ -159,6 +159,7 @@ bool make_bf16_map_3d(CUtensorMap* map, const void* ptr, int64_t d0, int64_t d1,
                       int box2 = 1);
 bool make_bf16_map_2d_sw64(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols,
                            int box_rows);
+bool make_bf16_map_gate_up_quads(CUtensorMap* map, const void* ptr, int64_t blocks);
 bool make_bf16_map_col_blocks(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows,
                               int box_blocks);
 

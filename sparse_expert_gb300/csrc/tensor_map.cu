@@ -31,7 +31,7 @@ bool encode(CUtensorMap* map, const void* ptr, cuuint32_t rank, const cuuint64_t
             const cuuint32_t* box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -77,6 +77,20 @@ bool make_bf16_map_col_blocks(CUtensorMap* map, const void* ptr, int64_t rows, i
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_blocks)};
   return encode(map, ptr, 3, dims, strides, box);
+}
+
+// A stack of packed gate/up blocks of [128 rows][64 columns] (rows 0-63
+// gate features, 64-127 the same up features) seen as (64 columns, 16 rows,
+// 2 halves, 8 * blocks groups of 16 rows): the half stride (64 rows) lies
+// above the group stride (16 rows), so one box of (64, 16, 2, 4) at group
+// 8 * block lands a block in shared memory with its rows reordered as
+// [group][half][row]: each 32-row quarter holds 16 gate features followed
+// by the same 16 up features.
+bool make_bf16_map_gate_up_quads(CUtensorMap* map, const void* ptr, int64_t blocks) {
+  const cuuint64_t dims[4] = {64, 16, 2, static_cast<cuuint64_t>(blocks) * 8};
+  const cuuint64_t strides[3] = {128, 64 * 128, 16 * 128};
+  const cuuint32_t box[4] = {64, 16, 2, 4};
+  return encode(map, ptr, 4, dims, strides, box);
 }
 
 }  // namespace moe
