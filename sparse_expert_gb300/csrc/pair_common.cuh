@@ -144,13 +144,4 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
       : "memory");
 }
 
-// Both partner warps arrive, then wait (bounded) for the phase to complete.
-__device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t& parity, volatile int* abort_flag) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait_warp(bar, parity, abort_flag);
-  parity ^= 1u;
-  return ok;
-}
-
 }  // namespace moe
