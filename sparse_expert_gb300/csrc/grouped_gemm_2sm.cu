@@ -719,21 +719,16 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             v[4 * g + 3] = __float_as_uint(s1 * __uint_as_float(v[4 * g + 3]));
           }
         };
-        // chunk c as a bf16 fragment (see pack_chunk), read from TMEM one
-        // 16-lane half at a time
+        // chunk c as a bf16 fragment (see pack_chunk): both 16-lane halves
+        // read from TMEM behind one wait
         auto fill = [&](int c, uint32_t (&pk)[16]) {
-          uint32_t v[16];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            tmem_ld_16x256b_x4((half ? taddr_b : taddr) + c, v);
-            tmem_ld_wait();
-            scale(v, c);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              pk[4 * g + 2 * half] = pack_bf16x2(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]));
-              pk[4 * g + 2 * half + 1] = pack_bf16x2(__uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
-            }
-          }
+          uint32_t v[16], w[16];
+          tmem_ld_16x256b_x4(taddr + c, v);
+          tmem_ld_16x256b_x4(taddr_b + c, w);
+          tmem_ld_wait();
+          scale(v, c);
+          scale(w, c);
+          pack_chunk(v, w, pk);
         };
         const int n_chunks = c_begin < c_end ? (c_end - c_begin + 31) >> 5 : 0;
         const int n_stream = max(n_chunks - kHold, 0);
