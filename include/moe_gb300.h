@@ -532,6 +532,20 @@ MOE_API moe_status_t moe_selftest_wait_timeout(void* workspace, size_t workspace
 MOE_API moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream,
                                     int32_t* status);
 
+/* ------------------------------------------------------------------------
+ * The activation functions of the expert-GEMM epilogues ("Scalable
+ * Pretraining of Large MoE LMs on Aurora Super Computer", §3.1, Algorithm 1,
+ * stage 4: Silu(gate) * up, and its derivative through sigmoid), applied
+ * elementwise with the very device functions the epilogues use, so that
+ * their error can be measured: silu[i] = Silu(z[i]) = z[i] * sigmoid(z[i]),
+ * sigmoid[i] = sigmoid(z[i]), fp32.  z, silu, sigmoid: device pointers to n
+ * floats (no overlap between the inputs and the outputs); n >= 0.  Errors:
+ * MOE_ERR_INVALID_ARG (n < 0, or NULL with n > 0), MOE_ERR_NO_DEVICE,
+ * MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_selftest_activation(const float* z, int64_t n, float* silu, float* sigmoid,
+                                             moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

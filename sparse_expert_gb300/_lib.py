@@ -76,6 +76,7 @@ SIGNATURES = {
     "moe_forward_host": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P]),
     "moe_read_device_status": (_S, [_P, _P, ctypes.POINTER(_I32)]),
     "moe_selftest_wait_timeout": (_S, [_P, _SZ, _I64, _P]),
+    "moe_selftest_activation": (_S, [_P, _I64, _P, _P, _P]),
     "moe_forward_host_stream": (_S, [_P, _P, _P, _I32, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
                                      _P, _P, _P]),
     "moe_grouped_gate_up_save": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -536,6 +537,16 @@ def moe_selftest_wait_timeout(workspace, limit_ns, stream=None):
     """Runs the bounded-wait check; read the status with moe_read_device_status."""
     _check(lib.moe_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(limit_ns), _stream(stream)),
            "moe_selftest_wait_timeout")
+
+
+def moe_selftest_activation(z, stream=None):
+    """Silu(z) and sigmoid(z), fp32, computed by the device functions of the expert-GEMM epilogues."""
+    z = _contig(z, torch.float32, "z")
+    silu = torch.empty_like(z)
+    sig = torch.empty_like(z)
+    _check(lib.moe_selftest_activation(_ptr(z), z.numel(), _ptr(silu), _ptr(sig), _stream(stream)),
+           "moe_selftest_activation")
+    return silu, sig
 
 
 def forward_intermediates(workspace, T, E, k, d, f):

@@ -924,6 +924,16 @@ moe_status_t moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, 
   return MOE_OK;
 }
 
+moe_status_t moe_selftest_activation(const float* z, int64_t n, float* silu, float* sigmoid, moe_stream_t stream) {
+  if (n < 0 || (n > 0 && (!z || !silu || !sigmoid))) return fail(MOE_ERR_INVALID_ARG, "bad n or NULL pointer");
+  DeviceInfo dev;
+  moe_status_t s = device_info(&dev);
+  if (s != MOE_OK) return s;
+  MOE_CUDA(launch_activation(z, n, silu, sigmoid, dev.num_sms, static_cast<cudaStream_t>(stream)),
+           "activation launch");
+  return MOE_OK;
+}
+
 moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream, int32_t* status) {
   if (!workspace || !status) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   MOE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");

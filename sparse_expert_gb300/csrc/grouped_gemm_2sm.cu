@@ -673,8 +673,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
                 const float d1 = __uint_as_float(m < 2 ? a[i + 1] : b[i + 1]);
                 const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pg[4 * gg + m]));
                 const float2 uf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pu[4 * gg + m]));
-                const float s0 = __fdividef(1.0f, 1.0f + __expf(-gf.x));
-                const float s1 = __fdividef(1.0f, 1.0f + __expf(-gf.y));
+                const float s0 = sigmoid_f32(gf.x);
+                const float s1 = sigmoid_f32(gf.y);
                 pg[4 * gg + m] = pack_bf16x2(d0 * uf.x * s0 * (1.0f + gf.x * (1.0f - s0)),
                                              d1 * uf.y * s1 * (1.0f + gf.y * (1.0f - s1)));
                 pu[4 * gg + m] = pack_bf16x2(d0 * gf.x * s0, d1 * gf.y * s1);

@@ -103,8 +103,6 @@ __device__ __forceinline__ void decode_wgrad(int t, int m_tiles, int n_tiles, in
   mt = local - nt * m_tiles;
 }
 
-__device__ __forceinline__ float sigmoid_f32(float z) { return 1.0f / (1.0f + __expf(-z)); }
-
 template <int BN, Mode M>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,

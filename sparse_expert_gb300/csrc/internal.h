@@ -166,6 +166,8 @@ bool make_bf16_map_col_blocks(CUtensorMap* map, const void* ptr, int64_t rows, i
 // Bounded-wait check: one block waits on a phase that never completes and
 // records a timeout in *status after limit_ns.
 cudaError_t launch_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+cudaError_t launch_activation(const float* z, int64_t n, float* silu, float* sigmoid, int num_sms,
+                              cudaStream_t stream);
 
 // Device properties of the current device (cached per device).
 struct DeviceInfo {

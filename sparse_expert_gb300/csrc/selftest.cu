@@ -1,7 +1,9 @@
-// Check of the failure path shared by every kernel: a bounded wait on an
-// mbarrier phase that never completes gives up after its limit, records
+// Checks of pieces every kernel shares.  The failure path: a bounded wait on
+// an mbarrier phase that never completes gives up after its limit, records
 // MOE_ERR_TIMEOUT in the workspace status word and returns, leaving the
-// context usable.  Nothing here faults, traps or spins without a bound.
+// context usable (nothing here faults, traps or spins without a bound).  The
+// activation functions: the exact device functions the expert-GEMM
+// epilogues apply, elementwise, so that their error can be measured.
 #include "common.cuh"
 #include "internal.h"
 
@@ -29,7 +31,26 @@ __global__ void __launch_bounds__(64) wait_timeout_kernel(int32_t* status, uint6
   }
 }
 
+__global__ void activation_kernel(const float* __restrict__ z, int64_t n, float* __restrict__ silu,
+                                  float* __restrict__ sigmoid) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float v = z[i];
+    silu[i] = silu_f32(v);
+    sigmoid[i] = sigmoid_f32(v);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_activation(const float* z, int64_t n, float* silu, float* sigmoid, int num_sms,
+                              cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int64_t want = (n + 255) / 256;
+  const int grid = static_cast<int>(want < num_sms * 8 ? want : num_sms * 8);
+  activation_kernel<<<grid, 256, 0, stream>>>(z, n, silu, sigmoid);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t stream) {
   wait_timeout_kernel<<<1, 64, 0, stream>>>(status, limit_ns);

@@ -155,3 +155,9 @@ def test_wait_check_argument_errors():
     assert lib.moe_selftest_wait_timeout(FAKE, 256, 3_000_000_000, NULL) == INVALID
     assert lib.moe_selftest_wait_timeout(NULL, 256, 1000, NULL) == WORKSPACE
     assert lib.moe_selftest_wait_timeout(FAKE, 255, 1000, NULL) == WORKSPACE
+
+
+def test_activation_check_argument_errors():
+    assert lib.moe_selftest_activation(FAKE, -1, FAKE, FAKE, NULL) == INVALID
+    assert lib.moe_selftest_activation(NULL, 4, FAKE, FAKE, NULL) == INVALID
+    assert lib.moe_selftest_activation(FAKE, 4, FAKE, NULL, NULL) == INVALID
