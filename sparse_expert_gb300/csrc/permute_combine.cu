@@ -12,7 +12,7 @@
 namespace moe {
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
+constexpr int kWarpsPerBlock = 16;  // one token per warp at 16k tokens: a single wave of warps
 constexpr int kVecPerLane = 4;  // 16-byte vectors in flight per lane
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
