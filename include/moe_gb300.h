@@ -513,11 +513,6 @@ MOE_API moe_status_t moe_forward_host_stream(const void* const* x_host, const fl
                                      moe_stream_t copy_in, moe_stream_t copy_out);
 
 /* ------------------------------------------------------------------------
- * Reads the device status word at the start of a workspace used by
- * moe_dispatch_scan, moe_grouped_swiglu or moe_forward, after waiting for
- * `stream`.  *status receives MOE_OK or the first device error.
- * ---------------------------------------------------------------------- */
-/* ------------------------------------------------------------------------
  * Check of the failure path every kernel shares: one block waits, with the
  * same bounded helpers the kernels use, on an mbarrier phase that never
  * completes, gives up after limit_ns (1 .. 2e9 ns, the kernels' own bound
@@ -529,6 +524,11 @@ MOE_API moe_status_t moe_forward_host_stream(const void* const* x_host, const fl
 MOE_API moe_status_t moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_ns,
                                        moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Reads the device status word at the start of a workspace used by
+ * moe_dispatch_scan, moe_grouped_swiglu or moe_forward, after waiting for
+ * `stream`.  *status receives MOE_OK or the first device error.
+ * ---------------------------------------------------------------------- */
 MOE_API moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream,
                                     int32_t* status);
 
