@@ -10,8 +10,11 @@ synthetic inputs.  The working set (25 GB of weights, 201 MB of tokens)
 is far larger than L2, so no flush is needed between steps.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
-Under torchrun (N > 1) every rank runs its own replica (weak scaling, no
-collective on the data path); rank 0 prints one JSON line.
+With N > 1 every rank runs its own replica on its own GPU (weak scaling, no
+collective on the data path; a barrier and a max over ranks around the
+timed region); rank 0 prints one JSON line.  Under torchrun the ranks come
+from the environment (WORLD_SIZE must equal N); otherwise bench.py starts N
+local ranks itself.
 """
 from __future__ import annotations
 
@@ -75,7 +78,7 @@ def job_throughput(units_per_rank: float, world: int, max_seconds: float) -> flo
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons every 100 ms."""
+    """nvidia-smi samples of SM clock and throttle reasons every 50 ms."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -92,7 +95,7 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -228,12 +231,151 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline_stages(cfg, x, logits, w_gate, w_up, w_down, n_tokens, n_experts):
+    """The fp64 oracle on the host cores, stage by stage, on bounded samples
+    of the workload (only the oracle calls are timed; fetching its inputs
+    from the device is not):
+      route, dispatch   every token;
+      permute, combine  the first n_tokens tokens with their own dispatch
+                        (the expert rows stand in for the expert outputs),
+                        scaled by T / n_tokens;
+      expert MLP        every row of n_experts experts spread over the
+                        non-empty ones, scaled by P / rows sampled.
+    Returns (seconds per stage, whether each is extrapolated, description)."""
+    import oracle
+    T, E, k = cfg.T, cfg.E, cfg.k
+    P = T * k
+    secs, extrap = {}, {}
+    l_h = logits.cpu().numpy()
+    t0 = time.perf_counter()
+    idx, w = oracle.route_topk(l_h, k, cfg.renormalize)
+    secs["route"], extrap["route"] = time.perf_counter() - t0, False
+    t0 = time.perf_counter()
+    counts, offsets, src, _ = oracle.dispatch(idx, E)
+    secs["dispatch"], extrap["dispatch"] = time.perf_counter() - t0, False
+
+    n = min(n_tokens, T)
+    x_s = x[:n].double().cpu().numpy()
+    _, _, src_s, dst_s = oracle.dispatch(idx[:n], E)
+    t0 = time.perf_counter()
+    xp = oracle.permute(x_s, src_s)
+    t_perm = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.combine(xp, dst_s, w[:n])
+    t_comb = time.perf_counter() - t0
+    secs["permute"], secs["combine"] = t_perm * T / n, t_comb * T / n
+    extrap["permute"] = extrap["combine"] = n < T
+    del xp, x_s
+
+    nonempty = np.nonzero(counts)[0]
+    pick = nonempty[np.linspace(0, len(nonempty) - 1, min(n_experts, len(nonempty))).astype(np.int64)]
+    mlp_s, rows = 0.0, 0
+    for e in np.unique(pick):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        X = x[torch.from_numpy(src[a:b]).to(x.device)].double().cpu().numpy()
+        wg = w_gate[e:e + 1].double().cpu().numpy()
+        wu = w_up[e:e + 1].double().cpu().numpy()
+        wd = w_down[e:e + 1].double().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.expert_mlp(X, np.array([0, b - a]), wg, wu, wd)
+        mlp_s += time.perf_counter() - t0
+        rows += b - a
+        del X, wg, wu, wd
+    secs["expert_mlp"], extrap["expert_mlp"] = mlp_s * P / max(rows, 1), rows < P
+    desc = (f"fp64 numpy oracle stage by stage: route and dispatch of all {T} tokens; permute and combine of the "
+            f"first {n} tokens x {T / n:.1f}; expert MLP of all {rows} rows of {len(np.unique(pick))} experts "
+            f"x {P / max(rows, 1):.1f}")
+    return secs, extrap, desc
+
+
 def time_oracle(cfg, sample):
     import oracle
     x_rows, l_rows, wg, wu, wd, _ = sample
     t0 = time.perf_counter()
     oracle.moe_forward_tokens(x_rows, l_rows, wg, wu, wd, cfg.k, cfg.renormalize)
     return time.perf_counter() - t0
+
+
+def stage_table(stage_ms, work, peaks):
+    """Per-stage ms with TFLOP/s and fraction of the bf16 peak (GEMMs) or GB/s
+    and fraction of the HBM copy bandwidth (the rest)."""
+    stages = {}
+    for name, ms in stage_ms.items():
+        st = {"ms": round(ms, 4)}
+        if "flops" in work[name]:
+            st["tflops"] = round(work[name]["flops"] / (ms * 1e-3) / 1e12, 2)
+            st["frac_bf16_peak"] = round(st["tflops"] / peaks["bf16_tflops"], 4)
+        else:
+            st["gbs"] = round(work[name]["bytes"] / (ms * 1e-3) / 1e9, 1)
+            st["frac_hbm"] = round(st["gbs"] / peaks["hbm_gbs"], 4)
+        stages[name] = st
+    return stages
+
+
+def measure_workload(moe, name, seed, steps, warmup, world, local):
+    """moe_forward of another seeded workload, timed like the headline (CUDA
+    events on the launching stream, per-stage events, max over ranks)."""
+    cfg = workloads.get(name)
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
+    inp = workloads.generate(cfg, seed=seed, device="cuda")
+    packed = moe.moe_pack_weights(inp["w_gate"], inp["w_up"], inp["w_down"])
+    x, logits = inp["x"], inp["logits"]
+    del inp  # the unpacked weights
+    ws = torch.empty(moe.moe_forward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device="cuda")
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    nstage = len(moe.FORWARD_STAGES)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)] for _ in range(steps)]
+    for _ in range(warmup):
+        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, events[0], cfg.renormalize, stream)
+    torch.cuda.synchronize()
+    if moe.moe_read_device_status(ws) != 0:
+        raise SystemExit(f"device status after the {name} warm-up")
+    counts = moe.forward_intermediates(ws, T, E, k, d, f)["counts"].cpu().numpy()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s_ in range(steps):
+        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, events[s_], cfg.renormalize, stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if moe.moe_read_device_status(ws) != 0:
+        raise SystemExit(f"device status after the {name} steps")
+    max_s = max_over_ranks(t0.elapsed_time(t1) / 1e3, world, device="cuda")
+    stage_ms = {nm: statistics.mean(events[s_][i].elapsed_time(events[s_][i + 1]) for s_ in range(steps))
+                for i, nm in enumerate(moe.FORWARD_STAGES)}
+    peaks = load_peaks()
+    work = stage_work(cfg)
+    stages = stage_table(stage_ms, work, peaks)
+    gemm_ms = stage_ms["gate_up"] + stage_ms["down"]
+    gemm_tf = (work["gate_up"]["flops"] + work["down"]["flops"]) / (gemm_ms * 1e-3) / 1e12
+    return {
+        "workload": f"{name}: T={T}, d={d}, E={E}, top-{k}, f={f}, {cfg.routing} routing, seed {seed}",
+        "value": round(job_throughput(T * steps, world, max_s), 1), "unit": "tokens/s",
+        "ms_per_step": round(max_s * 1e3 / steps, 4), "steps": steps, "warmup": warmup,
+        "grouped_gemm": {"tflops": round(gemm_tf, 2), "frac_bf16_peak": round(gemm_tf / peaks["bf16_tflops"], 4),
+                         "weight_bytes_read": weight_bytes_read(cfg, counts)},
+        "permute_gbs": stages["permute"]["gbs"], "combine_gbs": stages["combine"]["gbs"],
+        "experts_nonempty": int((counts > 0).sum()), "largest_group_rows": int(counts.max()),
+        "stages": stages, "clocks": clk,
+    }
 
 
 # ------------------------------------------------------------------ arms
@@ -287,16 +429,7 @@ def gpu_arm(args):
                 for i, name in enumerate(moe.FORWARD_STAGES)}
     work = stage_work(cfg)
     peaks = load_peaks()
-    stages = {}
-    for name, ms in stage_ms.items():
-        st = {"ms": round(ms, 4)}
-        if "flops" in work[name]:
-            st["tflops"] = round(work[name]["flops"] / (ms * 1e-3) / 1e12, 2)
-            st["frac_bf16_peak"] = round(st["tflops"] / peaks["bf16_tflops"], 4)
-        else:
-            st["gbs"] = round(work[name]["bytes"] / (ms * 1e-3) / 1e9, 1)
-            st["frac_hbm"] = round(st["gbs"] / peaks["hbm_gbs"], 4)
-        stages[name] = st
+    stages = stage_table(stage_ms, work, peaks)
     gemm_ms = stage_ms["gate_up"] + stage_ms["down"]
     gemm_tflops = (work["gate_up"]["flops"] + work["down"]["flops"]) / (gemm_ms * 1e-3) / 1e12
     dominant = max(("gate_up", "down"), key=lambda n: stage_ms[n])
@@ -449,13 +582,27 @@ def gpu_arm(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = min(args.cpu_sample_tokens, T)
-        tokens = torch.arange(n, device="cuda")
-        sample = oracle_sample(cfg, x, logits, inp["w_gate"], inp["w_up"], inp["w_down"], tokens)
-        secs = time_oracle(cfg, sample)
-        cpu = {"value": round(n / secs, 3), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"fp64 numpy oracle, full layer forward of the first {n} tokens of the {args.workload} "
-                         f"workload ({sample[5]} experts touched), {secs:.1f} s"}
+        secs, extrap, desc = cpu_baseline_stages(cfg, x, logits, inp["w_gate"], inp["w_up"], inp["w_down"],
+                                                 args.cpu_sample_tokens, args.cpu_sample_experts)
+        total = sum(secs.values())
+        cpu = {"value": round(T / total, 3), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": desc, "cpu_model": cpu_model(),
+               "stages_s": {k_: round(v, 4) for k_, v in secs.items()},
+               "extrapolated": sorted(k_ for k_, v in extrap.items() if v),
+               "note": "value = T / the sum of the stage times (timed or scaled), one layer forward"}
+
+    configs = None
+    if not args.no_configs:
+        # the other seeded workloads beside the headline one, each timed the same way
+        del inp, x, logits, packed, ws, out, events
+        torch.cuda.empty_cache()
+        configs = {}
+        for name in ("small", "skew", "long"):
+            if name == args.workload:
+                continue
+            configs[name] = measure_workload(moe, name, args.seed + rank, max(3, min(args.steps, 20)),
+                                             args.warmup, world, local)
+            torch.cuda.empty_cache()
 
     if rank == 0:
         line = {
@@ -470,8 +617,9 @@ def gpu_arm(args):
             "grouped_gemm": {"tflops": round(gemm_tflops, 2), "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
                              "weight_bytes_read": weight_bytes_read(cfg, counts)},
             "permute_gbs": stages["permute"]["gbs"],
-            "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed, "gathered_forward": gathered,
-            "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk, "backward": backward,
+            "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed,
+            "gathered_forward": gathered, "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk,
+            "backward": backward, "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -511,7 +659,41 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def main(argv=None):
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _spawned_rank(rank, world, port, argv, arm):
+    """Entry of a rank that bench.py started itself: the environment torchrun
+    would have set, then the arm."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    arm(parse_args(argv))
+
+
+def launch(args, argv, arm):
+    """Runs `arm` on args.gpus ranks: the current process when it is already
+    one rank of a torchrun job (WORLD_SIZE set) or when N = 1, else N local
+    processes started here, one per GPU."""
+    world_env = os.environ.get("WORLD_SIZE")
+    if world_env is not None:
+        if int(world_env) != args.gpus:
+            raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world_env}: launch one rank per GPU")
+        arm(args)
+        return
+    if args.gpus == 1:
+        arm(args)
+        return
+    if arm is gpu_arm and torch.cuda.device_count() < args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but {torch.cuda.device_count()} CUDA devices are visible")
+    import torch.multiprocessing as mp
+    mp.spawn(_spawned_rank, args=(args.gpus, _free_port(), list(argv), arm), nprocs=args.gpus, join=True)
+
+
+def parse_args(argv):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -524,14 +706,25 @@ def main(argv=None):
     ap.add_argument("--no-routed", action="store_true", help="skip the fused-router forward measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the layer-backward measurement")
     ap.add_argument("--no-gathered", action="store_true", help="skip the gathered (no x_perm) forward measurement")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    ap.add_argument("--no-configs", action="store_true", help="skip the other seeded workloads (small, skew, long)")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2048,
+                    help="tokens of the CPU baseline's permute/combine sample")
+    ap.add_argument("--cpu-sample-experts", type=int, default=16,
+                    help="experts of the CPU baseline's expert-MLP sample")
     ap.add_argument("--ref-sample-tokens", type=int, default=4)
     args = ap.parse_args(argv)
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
-    if args.impl == "reference":
-        reference_arm(args)
-    else:
-        gpu_arm(args)
+    return args
+
+
+def main(argv=None, arm=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
+    args = parse_args(argv)
+    if arm is None:
+        arm = reference_arm if args.impl == "reference" else gpu_arm
+    launch(args, argv, arm)
 
 
 if __name__ == "__main__":

@@ -31,12 +31,14 @@
  *     bit patterns (2 bytes each); they are typed void* here.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream) and returns without waiting for it.  Only
- *     moe_read_device_status, moe_forward_host and moe_forward_host_stream
- *     synchronise.
+ *     moe_read_device_status, moe_get_device_status,
+ *     moe_dispatch_noalloc_status, moe_forward_host and
+ *     moe_forward_host_stream synchronise.
  *   - Argument errors are found on the host and returned at once with no
  *     work enqueued.  Errors found by a kernel (a bounded wait that ran out,
- *     an out-of-range expert index) are written to a status word at the
- *     start of the workspace and read back with moe_read_device_status.
+ *     an out-of-range expert index or row index) are written to a status
+ *     word at the start of the workspace and read back with
+ *     moe_get_device_status or moe_read_device_status.
  *   - Calls that share a workspace must not overlap on the GPU.
  *   - Supported sizes: 1 <= E <= 1024, 1 <= k <= min(E, 32), 0 <= T,
  *     T*k < 2^31.  The GEMM stages and moe_forward need d and f to be
@@ -192,17 +194,24 @@ MOE_API moe_status_t moe_dispatch_scan(const int32_t* topk_idx, const float* top
  *   device current; make it before any stream capture.  All calls share
  *   the array: calls that overlap on the GPU race and must be serialised
  *   by the caller.  Allocates nothing (no cudaMalloc, cudaFree or
- *   allocating library routine).  Device-detected errors are not readable
- *   through moe_read_device_status; a pair with an out-of-range expert
- *   index still gets dest_row = -1.
+ *   allocating library routine).  A pair with an out-of-range expert index
+ *   gets dest_row = -1, as with moe_dispatch_scan.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_NO_DEVICE,
  *         MOE_ERR_CUDA.
+ *
+ * moe_dispatch_noalloc_status waits for `stream` and copies into *status
+ * (host memory) the device status of the latest moe_dispatch_scan_noalloc
+ * on the current device: MOE_OK, or the first error its kernels found
+ * (MOE_ERR_BAD_INDEX, MOE_ERR_TIMEOUT).  The next call clears it, so read
+ * it before that call is enqueued.  Allocates nothing.
+ * Errors: MOE_ERR_INVALID_ARG (NULL status), MOE_ERR_NO_DEVICE, MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 MOE_API moe_status_t moe_dispatch_scan_noalloc(const int32_t* topk_idx, const float* topk_w,
                                        int64_t T, int32_t E, int32_t k,
                                        int32_t* counts, int32_t* offsets,
                                        int32_t* src_token, int32_t* dest_row, float* row_w,
                                        moe_stream_t stream);
+MOE_API moe_status_t moe_dispatch_noalloc_status(moe_stream_t stream, int32_t* status);
 
 /* ------------------------------------------------------------------------
  * Stage 4, first step — mlp_in = input[input_indices] (Algorithm 1,
@@ -211,6 +220,9 @@ MOE_API moe_status_t moe_dispatch_scan_noalloc(const int32_t* topk_idx, const fl
  * the same as gathering x_perm[r] = x[src_token[r]].
  *   x [T, d] bf16 in; dest_row [T*k] int32 in (a bijection onto [0, T*k));
  *   x_perm [T*k, d] bf16 out.
+ * An entry of dest_row outside [0, T*k) (such as the -1 the dispatch pass
+ * writes for a pair it could not place) is skipped: nothing is written for
+ * that pair, and no memory outside x_perm is touched.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 MOE_API moe_status_t moe_permute(const void* x, int64_t T, int32_t d, const int32_t* dest_row,
@@ -291,6 +303,8 @@ MOE_API moe_status_t moe_grouped_swiglu(const void* x_perm, const int32_t* offse
  * row_scale).
  *   y [T*k, d] bf16 in; dest_row [T*k] int32 in; topk_w [T, k] fp32 in,
  *   optional; out [T, d] bf16 out.
+ * A slot whose dest_row lies outside [0, T*k) is left out of its token's
+ * sum (no memory outside y is read).
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 MOE_API moe_status_t moe_combine(const void* y, const int32_t* dest_row, const float* topk_w,
@@ -345,6 +359,8 @@ MOE_API moe_status_t moe_grouped_swiglu_backward(const void* x_perm, const void*
  *   dout [T, d] bf16; mlp_out [T*k, d] bf16, the expert outputs BEFORE the
  *   gate (moe_grouped_swiglu with row_scale = NULL); dest_row [T*k];
  *   topk_w [T, k] fp32; d_mlp_out [T*k, d] bf16 out; d_topk_w [T, k] out.
+ * A slot whose dest_row lies outside [0, T*k) writes no row gradient and
+ * gets d_topk_w = 0.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 MOE_API moe_status_t moe_combine_backward(const void* dout, const void* mlp_out, const int32_t* dest_row,
@@ -377,6 +393,9 @@ MOE_API moe_status_t moe_route_backward(const float* logits, const int32_t* topk
  *   fp32 out, optional (the workspace keeps its own copy).
  * Workspace: moe_forward_workspace_bytes(T, E, k, d, f); the intermediates
  * stay there after the call at the byte offsets moe_forward_layout gives.
+ * If a look-back wait of the index pass runs out, its pairs get dest_row
+ * = -1, the permute and the combine skip them, and the status word reads
+ * MOE_ERR_TIMEOUT; the output rows of those tokens are then incomplete.
  * Errors: as the stages.
  * ---------------------------------------------------------------------- */
 typedef struct {
@@ -531,6 +550,15 @@ MOE_API moe_status_t moe_selftest_wait_timeout(void* workspace, size_t workspace
  * ---------------------------------------------------------------------- */
 MOE_API moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream,
                                     int32_t* status);
+
+/* ------------------------------------------------------------------------
+ * The same read with the device status as the return value: waits for
+ * `stream` and returns MOE_OK or the first error a kernel recorded in the
+ * workspace (MOE_ERR_TIMEOUT, MOE_ERR_BAD_INDEX).  When the read itself
+ * fails it returns MOE_ERR_INVALID_ARG (NULL workspace) or MOE_ERR_CUDA,
+ * and moe_last_error says which.
+ * ---------------------------------------------------------------------- */
+MOE_API moe_status_t moe_get_device_status(const void* workspace, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * The activation functions of the expert-GEMM epilogues ("Scalable

@@ -75,6 +75,8 @@ SIGNATURES = {
     "moe_forward_gathered_timed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "moe_forward_host": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P]),
     "moe_read_device_status": (_S, [_P, _P, ctypes.POINTER(_I32)]),
+    "moe_get_device_status": (_S, [_P, _P]),
+    "moe_dispatch_noalloc_status": (_S, [_P, ctypes.POINTER(_I32)]),
     "moe_selftest_wait_timeout": (_S, [_P, _SZ, _I64, _P]),
     "moe_selftest_activation": (_S, [_P, _I64, _P, _P, _P]),
     "moe_forward_host_stream": (_S, [_P, _P, _P, _I32, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
@@ -574,4 +576,21 @@ def forward_intermediates(workspace, T, E, k, d, f):
 def moe_read_device_status(workspace, stream=None) -> int:
     st = _I32(0)
     _check(lib.moe_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(st)), "moe_read_device_status")
+    return st.value
+
+
+def moe_get_device_status(workspace, stream=None) -> int:
+    """The workspace's device status as the C call returns it (0 = MOE_OK,
+    4 = MOE_ERR_TIMEOUT, 5 = MOE_ERR_BAD_INDEX); raises only when the read
+    itself fails."""
+    s = lib.moe_get_device_status(_ptr(workspace), _stream(stream))
+    if s in (1, 3):  # MOE_ERR_INVALID_ARG, MOE_ERR_CUDA: the read failed
+        _check(s, "moe_get_device_status")
+    return s
+
+
+def moe_dispatch_noalloc_status(stream=None) -> int:
+    """Device status of the latest moe_dispatch_scan_noalloc on this device."""
+    st = _I32(0)
+    _check(lib.moe_dispatch_noalloc_status(_stream(stream), ctypes.byref(st)), "moe_dispatch_noalloc_status")
     return st.value

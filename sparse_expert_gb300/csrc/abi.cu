@@ -35,14 +35,6 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 constexpr int32_t kRouterMaxExperts = 512;  // the fused router's accumulator fits TMEM's 512 columns
 
-moe_status_t check_routing(int64_t T, int32_t E, int32_t k) {
-  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
-  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
-  if (k < 1 || k > E || k > MOE_MAX_TOPK) return fail(MOE_ERR_UNSUPPORTED, "k must be in [1, min(E, 32)]");
-  if (T * static_cast<int64_t>(k) >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
-  return MOE_OK;
-}
-
 moe_status_t check_row(int32_t d, const char* name) {
   if (d < 8 || d > 65536 || d % 8 != 0)
     return fail(MOE_ERR_UNSUPPORTED, std::string(name) + " must be a multiple of 8 in [8, 65536]");
@@ -152,6 +144,16 @@ DispatchState dispatch_state_split(void* ws, size_t state_at, int64_t P, int E) 
 }  // namespace
 
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+moe_status_t check_routing(int64_t T, int32_t E, int32_t k) {
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
+  if (E < 1 || E > MOE_MAX_EXPERTS)
+    return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, " + std::to_string(MOE_MAX_EXPERTS) + "]");
+  if (k < 1 || k > E || k > MOE_MAX_TOPK)
+    return fail(MOE_ERR_UNSUPPORTED, "k must be in [1, min(E, " + std::to_string(MOE_MAX_TOPK) + ")]");
+  if (T * static_cast<int64_t>(k) >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  return MOE_OK;
+}
 
 cudaError_t current_device_info(DeviceInfo* info) {
   static DeviceInfo cache[64];
@@ -316,7 +318,7 @@ moe_status_t moe_permute(const void* x, int64_t T, int32_t d, const int32_t* des
   if (!aligned(x, 16) || !aligned(x_perm, 16)) return fail(MOE_ERR_INVALID_ARG, "x and x_perm must be 16-byte aligned");
   DeviceInfo dev;
   if ((s = device_info(&dev)) != MOE_OK) return s;
-  MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, dev.num_sms, static_cast<cudaStream_t>(stream)),
+  MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, nullptr, dev.num_sms, static_cast<cudaStream_t>(stream)),
            "permute launch");
   return MOE_OK;
 }
@@ -408,7 +410,7 @@ moe_status_t moe_combine(const void* y, const int32_t* dest_row, const float* to
   if (!aligned(y, 16) || !aligned(out, 16)) return fail(MOE_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
   DeviceInfo dev;
   if ((s = device_info(&dev)) != MOE_OK) return s;
-  MOE_CUDA(launch_combine(y, dest_row, topk_w, T, k, d, out, dev.num_sms, static_cast<cudaStream_t>(stream)),
+  MOE_CUDA(launch_combine(y, dest_row, topk_w, T, k, d, out, nullptr, dev.num_sms, static_cast<cudaStream_t>(stream)),
            "combine launch");
   return MOE_OK;
 }
@@ -427,7 +429,7 @@ moe_status_t moe_combine_backward(const void* dout, const void* mlp_out, const i
     return fail(MOE_ERR_INVALID_ARG, "dout, mlp_out and d_mlp_out must be 16-byte aligned");
   DeviceInfo dev;
   if ((s = device_info(&dev)) != MOE_OK) return s;
-  MOE_CUDA(launch_combine_backward(dout, mlp_out, dest_row, topk_w, T, k, d, d_mlp_out, d_topk_w, dev.num_sms,
+  MOE_CUDA(launch_combine_backward(dout, mlp_out, dest_row, topk_w, T, k, d, d_mlp_out, d_topk_w, nullptr, dev.num_sms,
                                    static_cast<cudaStream_t>(stream)),
            "combine backward launch");
   return MOE_OK;
@@ -624,7 +626,8 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* router
            "index launch");
   MOE_CUDA(mark(2), "event record");
   // stage 4
-  if (!gathered) MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, dev.num_sms, st), "permute launch");
+  if (!gathered)
+    MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, &hdr->status, dev.num_sms, st), "permute launch");
   MOE_CUDA(mark(3), "event record");
   const auto* wgu = static_cast<const __nv_bfloat16*>(packed);
   const auto* wdn = wgu + static_cast<int64_t>(E) * 2 * f * d;
@@ -642,7 +645,7 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* router
   MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
   MOE_CUDA(mark(5), "event record");
   // stage 5: each token sums its k rows weighted by its TopK weights
-  MOE_CUDA(launch_combine(y, dest_row, topk_w, T, k, d, out, dev.num_sms, st), "combine launch");
+  MOE_CUDA(launch_combine(y, dest_row, topk_w, T, k, d, out, &hdr->status, dev.num_sms, st), "combine launch");
   MOE_CUDA(mark(6), "event record");
   return MOE_OK;
 }
@@ -865,7 +868,7 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   DispatchState dstate = dispatch_state_split(ws, F.dispatch_state, P, E);
   MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, ws, dstate, st),
            "index launch");
-  MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, dev.num_sms, st), "permute launch");
+  MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, &hdr->status, dev.num_sms, st), "permute launch");
   MOE_CUDA(mark(1), "event record");
   MOE_CUDA(launch_gate_up_save(a, dev.num_sms, st), "gate/up GEMM launch");
   MOE_CUDA(mark(2), "event record");
@@ -874,7 +877,7 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
   MOE_CUDA(mark(3), "event record");
   // stage 5 backward, then the gates back to the logits
-  MOE_CUDA(launch_combine_backward(dout, y, dest_row, topk_w, T, k, d, dy, d_topk_w, dev.num_sms, st),
+  MOE_CUDA(launch_combine_backward(dout, y, dest_row, topk_w, T, k, d, dy, d_topk_w, &hdr->status, dev.num_sms, st),
            "combine backward launch");
   MOE_CUDA(launch_route_backward(logits, topk_idx, d_topk_w, T, E, k, renormalize, d_logits, dev.num_sms, st),
            "route backward launch");
@@ -882,7 +885,7 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   // stage 4 backward: dgrad (down, gate/up), wgrad (down, gate/up)
   MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 5 : nullptr), "backward GEMM launch");
   // the transpose of the permute: each token sums its k row gradients
-  MOE_CUDA(launch_combine(dx_perm, dest_row, nullptr, T, k, d, dx, dev.num_sms, st), "un-permute launch");
+  MOE_CUDA(launch_combine(dx_perm, dest_row, nullptr, T, k, d, dx, &hdr->status, dev.num_sms, st), "un-permute launch");
   MOE_CUDA(mark(9), "event record");
   return MOE_OK;
 }
@@ -939,6 +942,14 @@ moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream, 
   MOE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");
   MOE_CUDA(cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost), "status read");
   return MOE_OK;
+}
+
+moe_status_t moe_get_device_status(const void* workspace, moe_stream_t stream) {
+  int32_t status = MOE_OK;
+  const moe_status_t s = moe_read_device_status(workspace, stream, &status);
+  if (s != MOE_OK) return s;
+  if (status != MOE_OK) set_last_error(std::string("device status: ") + moe_status_string(static_cast<moe_status_t>(status)));
+  return static_cast<moe_status_t>(status);
 }
 
 }  // extern "C"

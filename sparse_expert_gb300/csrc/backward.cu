@@ -28,11 +28,16 @@ template <int KMAX>
 __global__ void __launch_bounds__(kWarps * 32)
 combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ mlp_out,
                         const int32_t* __restrict__ dest_row, const float* __restrict__ w, int64_t T, int k, int dvec,
-                        uint4* __restrict__ d_mlp_out, float* __restrict__ d_w) {
+                        uint4* __restrict__ d_mlp_out, float* __restrict__ d_w, int32_t* status) {
   const int lane = threadIdx.x & 31;
+  const int64_t P = T * k;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarps;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < T; t += warps_total) {
     const int64_t my_row = lane < k ? __ldg(dest_row + t * k + lane) : 0;
+    // a row outside [0, P) is never an address: that slot gets no row
+    // gradient and a zero gate gradient
+    const unsigned bad_slots = __ballot_sync(0xffffffffu, my_row < 0 || my_row >= P);
+    if (bad_slots != 0u && lane == 0) record_status(status, kStatusBadIndex);
     const float my_w = lane < k ? __ldg(w + t * k + lane) : 0.f;
     const uint4* g = dout + t * dvec;
     float dot[KMAX];
@@ -53,7 +58,7 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
         if (j < k) {
           const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
           const float wj = __shfl_sync(0xffffffffu, my_w, j);
-          if (active) {
+          if (active && !((bad_slots >> j) & 1u)) {
             const uint4 yv = __ldg(mlp_out + row * dvec + v);
             const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yv);
             uint32_t o[4];
@@ -147,18 +152,18 @@ int token_grid(int64_t T, int num_sms) {
 }  // namespace
 
 cudaError_t launch_combine_backward(const void* dout, const void* mlp_out, const int32_t* dest_row, const float* w,
-                                    int64_t T, int k, int d, void* d_mlp_out, float* d_w, int num_sms,
-                                    cudaStream_t stream) {
+                                    int64_t T, int k, int d, void* d_mlp_out, float* d_w, int32_t* status,
+                                    int num_sms, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const auto* g = static_cast<const uint4*>(dout);
   const auto* y = static_cast<const uint4*>(mlp_out);
   auto* dy = static_cast<uint4*>(d_mlp_out);
   if (k <= 8)
     combine_backward_kernel<8><<<token_grid(T, num_sms), kWarps * 32, 0, stream>>>(g, y, dest_row, w, T, k, d / 8, dy,
-                                                                                    d_w);
+                                                                                    d_w, status);
   else
     combine_backward_kernel<32><<<token_grid(T, num_sms), kWarps * 32, 0, stream>>>(g, y, dest_row, w, T, k, d / 8,
-                                                                                     dy, d_w);
+                                                                                     dy, d_w, status);
   return cudaGetLastError();
 }
 

@@ -231,6 +231,13 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
       const int32_t stop = s_flag;
       if (stop < 0) {
         if (tid == 0) record_status(&hdr->status, kStatusTimeout);
+        // this block's pairs get no row: -1 tells the permute and the
+        // combine to skip them (their rows in the expert groups stay unwritten)
+#pragma unroll
+        for (int r = 0; r < kDispatchPairsPerThread; ++r) {
+          const int64_t p = base + r * 32 + lane;
+          if (p < P) dest_row[p] = -1;
+        }
         return;  // successors walk past this block on its aggregate
       }
       for (int e = tid; e < E; e += kDispatchThreads) {

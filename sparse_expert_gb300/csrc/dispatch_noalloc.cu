@@ -19,6 +19,10 @@
 // (cudaGetSymbolAddress) with that device current; make that first call
 // before any stream capture.  The call itself allocates nothing: no
 // cudaMalloc, no cudaFree, no allocating library routine.
+//
+// Errors the kernels find (an expert index outside [0, E), a look-back wait
+// that ran out) land in the status word at the start of the array, which the
+// next call clears; moe_dispatch_noalloc_status reads it back.
 #include <mutex>
 #include <string>
 
@@ -70,12 +74,8 @@ extern "C" moe_status_t moe_dispatch_scan_noalloc(const int32_t* topk_idx, const
                                                   int32_t E, int32_t k, int32_t* counts, int32_t* offsets,
                                                   int32_t* src_token, int32_t* dest_row, float* row_w,
                                                   moe_stream_t stream) {
-  if (T < 0) return noalloc_fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
-  if (E < 1 || E > MOE_MAX_EXPERTS) return noalloc_fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
-  if (k < 1 || k > E || k > MOE_MAX_TOPK)
-    return noalloc_fail(MOE_ERR_UNSUPPORTED, "k must be in [1, min(E, 32)]");
-  if (T * static_cast<int64_t>(k) >= (int64_t(1) << 31))
-    return noalloc_fail(MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  const moe_status_t checked = check_routing(T, E, k);
+  if (checked != MOE_OK) return checked;
   if (!counts || !offsets) return noalloc_fail(MOE_ERR_INVALID_ARG, "NULL counts/offsets");
   if (T > 0 && (!topk_idx || !src_token || !dest_row)) return noalloc_fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (row_w && !topk_w) return noalloc_fail(MOE_ERR_INVALID_ARG, "row_w needs topk_w");
@@ -114,5 +114,21 @@ extern "C" moe_status_t moe_dispatch_scan_noalloc(const int32_t* topk_idx, const
   if ((e = launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, ws, state, st)) !=
       cudaSuccess)
     return noalloc_fail(MOE_ERR_CUDA, std::string("index launch: ") + cudaGetErrorName(e));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_dispatch_noalloc_status(moe_stream_t stream, int32_t* status) {
+  if (!status) return noalloc_fail(MOE_ERR_INVALID_ARG, "NULL status");
+  void* ws = nullptr;
+  cudaError_t e = scratch_address(&ws);
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver)
+    return noalloc_fail(MOE_ERR_NO_DEVICE, "no CUDA device available");
+  if (e != cudaSuccess) return noalloc_fail(MOE_ERR_CUDA, std::string("static scratch address: ") + cudaGetErrorName(e));
+  if ((e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return noalloc_fail(MOE_ERR_CUDA, std::string("stream synchronize: ") + cudaGetErrorName(e));
+  // the header's status word, copied straight into the caller's int (no staging buffer)
+  if ((e = cudaMemcpy(status, &static_cast<const WsHeader*>(ws)->status, sizeof(int32_t), cudaMemcpyDeviceToHost)) !=
+      cudaSuccess)
+    return noalloc_fail(MOE_ERR_CUDA, std::string("status read: ") + cudaGetErrorName(e));
   return MOE_OK;
 }

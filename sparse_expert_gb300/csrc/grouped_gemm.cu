@@ -342,8 +342,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       int e, mt, nt;
       decode_tile(t, s_pre, p.E, p.n_tiles, e, mt, nt);
       const int64_t row = static_cast<int64_t>(s_off[e]) + mt * BM + g;
-      const int src_bytes = row < p.P ? 16 : 0;
-      const __nv_bfloat16* src_row = x_src + (row < p.P ? static_cast<int64_t>(__ldg(p.gather_rows + row)) * p.K : 0);
+      // a source token outside [0, a_rows) (a row the dispatch pass left
+      // unwritten) is read as zeros, never as an address
+      const int64_t tok = row < p.P ? static_cast<int64_t>(__ldg(p.gather_rows + row)) : -1;
+      const bool tok_ok = tok >= 0 && tok < p.a_rows;
+      const int src_bytes = tok_ok ? 16 : 0;
+      const __nv_bfloat16* src_row = x_src + (tok_ok ? tok * p.K : 0);
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!mbar_wait_warp(&S->empty[stage], phase ^ 1u, abort_flag)) {
           ok = false;

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "moe_gb300.h"
+
 namespace moe {
 
 constexpr size_t kAlign = 256;
@@ -25,9 +27,11 @@ cudaError_t launch_router_topk(const void* x, const void* w_packed, int64_t T, i
                                cudaStream_t stream);
 
 // ---- backward of stage 5 and of the routing
+// status (may be null) records a dest_row entry outside [0, T*k); such a
+// slot is skipped (no row gradient, zero gate gradient).
 cudaError_t launch_combine_backward(const void* dout, const void* mlp_out, const int32_t* dest_row, const float* w,
-                                    int64_t T, int k, int d, void* d_mlp_out, float* d_w, int num_sms,
-                                    cudaStream_t stream);
+                                    int64_t T, int k, int d, void* d_mlp_out, float* d_w, int32_t* status,
+                                    int num_sms, cudaStream_t stream);
 cudaError_t launch_route_backward(const float* logits, const int32_t* idx, const float* d_w, int64_t T, int E, int k,
                                   int renormalize, float* d_logits, int num_sms, cudaStream_t stream);
 
@@ -61,10 +65,12 @@ cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P
                          float* row_w, void* header, DispatchState st, cudaStream_t stream);
 
 // ---- stage 4 data movement and stage 5
+// A dest_row entry outside [0, T*k) is skipped (no copy; no term of the sum)
+// and recorded as MOE_ERR_BAD_INDEX in *status when status is not null.
 cudaError_t launch_permute(const void* x, int64_t T, int d, const int32_t* dest_row, int k, void* x_perm,
-                           int num_sms, cudaStream_t stream);
+                           int32_t* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const void* y, const int32_t* dest_row, const float* topk_w, int64_t T, int k, int d,
-                           void* out, int num_sms, cudaStream_t stream);
+                           void* out, int32_t* status, int num_sms, cudaStream_t stream);
 
 // ---- weights
 int gate_up_half_tile(int f);  // N columns of gate (and of up) in one GEMM tile
@@ -179,5 +185,10 @@ cudaError_t current_device_info(DeviceInfo* info);
 
 // Sets the text moe_last_error returns on the calling host thread.
 void set_last_error(const std::string& msg);
+
+// Host checks of the routing sizes every routing entry point shares: T >= 0,
+// 1 <= E <= MOE_MAX_EXPERTS, 1 <= k <= min(E, MOE_MAX_TOPK), T*k < 2^31.
+// Sets the last-error text on failure.
+moe_status_t check_routing(int64_t T, int32_t E, int32_t k);
 
 }  // namespace moe

@@ -161,3 +161,58 @@ def test_activation_check_argument_errors():
     assert lib.moe_selftest_activation(FAKE, -1, FAKE, FAKE, NULL) == INVALID
     assert lib.moe_selftest_activation(NULL, 4, FAKE, FAKE, NULL) == INVALID
     assert lib.moe_selftest_activation(FAKE, 4, FAKE, NULL, NULL) == INVALID
+
+
+# The boundary the hot path was specified against: each call with its
+# parameter names (bf16 buffers are void*, cudaStream_t is moe_stream_t).
+CONTRACT = {
+    "moe_status_string": ["status"],
+    "moe_route_topk": ["logits", "T", "E", "k", "renormalize", "topk_idx", "topk_w", "stream"],
+    "moe_dispatch_workspace_bytes": ["T", "E", "k"],
+    "moe_dispatch_scan": ["topk_idx", "T", "E", "k", "counts", "offsets", "src_token", "dest_row", "topk_w", "row_w",
+                          "workspace", "workspace_bytes", "stream"],
+    "moe_permute": ["x", "T", "d", "src_token", "P", "x_perm", "stream"],
+    "moe_packed_weight_bytes": ["E", "d", "f"],
+    "moe_pack_weights": ["w_gate", "w_up", "w_down", "E", "d", "f", "packed", "stream"],
+    "moe_grouped_swiglu": ["x_perm", "offsets", "E", "d", "f", "packed", "row_scale", "h", "y", "workspace",
+                           "workspace_bytes", "stream"],
+    "moe_combine": ["y", "dest_row", "topk_w", "T", "k", "d", "out", "stream"],
+    "moe_forward_workspace_bytes": ["T", "E", "k", "d", "f"],
+    "moe_forward": ["x", "logits", "packed", "T", "d", "E", "k", "f", "renormalize", "out", "topk_idx_out",
+                    "topk_w_out", "workspace", "workspace_bytes", "stream"],
+    "moe_get_device_status": ["workspace", "stream"],
+}
+
+# Where the exported call departs from that form, and why (the same three
+# lines stand in the design notes of the boundary).
+DEVIATIONS = {
+    "moe_dispatch_scan": (["topk_idx", "topk_w", "T", "E", "k", "counts", "offsets", "src_token", "dest_row", "row_w",
+                           "workspace", "workspace_bytes", "stream"],
+                          "the optional gates sit beside the indices they belong to"),
+    "moe_permute": (["x", "T", "d", "dest_row", "k", "x_perm", "stream"],
+                    "scatter from the token side: each x row is read once and written to its k rows"),
+    "moe_grouped_swiglu": (["x_perm", "offsets", "P", "E", "d", "f", "packed", "row_scale", "h", "y", "workspace",
+                            "workspace_bytes", "stream"],
+                           "P sizes x_perm, h and y on the host without reading offsets[E] back from the device"),
+}
+
+
+def declared_params(name):
+    text = open(HEADER).read()
+    m = re.search(r"MOE_API\s+[\w\s\*]+?\b" + name + r"\s*\((.*?)\);", text, re.S)
+    assert m, name
+    params = [p.strip() for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+    return [re.findall(r"\w+", p)[-1] for p in params]
+
+
+@pytest.mark.parametrize("name", sorted(CONTRACT))
+def test_contract_call_is_exported_as_specified_or_recorded(name):
+    assert hasattr(lib, name), f"{name} is not exported"
+    assert name in lib_mod.SIGNATURES, f"{name} has no binding"
+    want = DEVIATIONS[name][0] if name in DEVIATIONS else CONTRACT[name]
+    assert declared_params(name) == want
+    assert len(lib_mod.SIGNATURES[name][1]) == len(want)
+
+
+def test_get_device_status_argument_check():
+    assert lib.moe_get_device_status(NULL, NULL) == INVALID

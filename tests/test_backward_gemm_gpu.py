@@ -168,14 +168,18 @@ def test_layer_backward_is_deterministic(moe):
         assert torch.equal(a[key], b[key]), key
 
 
-def test_layer_backward_full_size_sampled(moe):
-    """16384 tokens, d = 6144, 384 experts, k = 8, f = 1792: the whole
-    backward runs on the GPU; the oracle recomputes, one by one, the rows of
-    a seeded token sample (all k slots of each) and of two whole experts
-    (the largest group and a random one), and the gradients that depend
-    only on those rows are compared: dx and d_logits of the sampled tokens,
-    the three weight gradients of the sampled experts."""
-    cfg, inp, dout = _layer_inputs("t1", device="cuda")
+@pytest.mark.parametrize("name", ["t1", "skew"])
+def test_layer_backward_full_size_sampled(moe, name):
+    """16384 tokens, d = 6144, 384 experts, k = 8, f = 1792 (normal routing,
+    and the Zipf-skewed routing whose largest group holds ~16,000 rows and
+    ~200 experts none): the whole backward runs on the GPU; the oracle
+    recomputes, one by one, the rows of a seeded token sample (all k slots
+    of each) and of two whole experts (the largest group and a random one,
+    which may be empty: its weight gradients must then be exactly zero),
+    and the gradients that depend only on those rows are compared: dx and
+    d_logits of the sampled tokens, the three weight gradients of the
+    sampled experts."""
+    cfg, inp, dout = _layer_inputs(name, device="cuda")
     g = _gpu_backward(moe, cfg, inp, dout)
     torch.cuda.synchronize()
     logits = to_np(inp["logits"])

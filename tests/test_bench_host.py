@@ -96,3 +96,41 @@ def test_bench_uses_only_names_the_binding_exports():
     assert names, "no binding calls found"
     missing = sorted(n for n in names if not hasattr(moe, n))
     assert not missing, missing
+
+
+def _stub_arm(args):
+    """Stands in for the GPU arm: the same rank environment, barrier, max over
+    ranks and throughput formula, with gloo and made-up times."""
+    world, rank, _ = bench.dist_env()
+    bench.dist_init(world, "gloo")
+    seconds = 0.1 * (rank + 1)              # the last rank is the slowest
+    bench.barrier(world)
+    slowest = bench.max_over_ranks(seconds, world, device="cpu")
+    if rank == 0:
+        print(json.dumps({"n_gpus": world, "steps": args.steps,
+                          "value": bench.job_throughput(1000 * args.steps, world, slowest)}), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def test_gpus_flag_starts_one_rank_per_gpu(capfd, monkeypatch):
+    for var in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    bench.main(["--gpus", "2", "--steps", "3"], arm=_stub_arm)
+    lines = [json.loads(l) for l in capfd.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, lines
+    assert lines[0]["n_gpus"] == 2 and lines[0]["steps"] == 3
+    assert lines[0]["value"] == pytest.approx(2 * 3000 / 0.2)
+
+
+def test_gpus_flag_must_match_the_launcher(monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    with pytest.raises(SystemExit, match="WORLD_SIZE=4"):
+        bench.main(["--gpus", "2"], arm=_stub_arm)
+
+
+def test_one_gpu_runs_in_process(capfd, monkeypatch):
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    bench.main(["--steps", "2"], arm=_stub_arm)
+    lines = [json.loads(l) for l in capfd.readouterr().out.splitlines() if l.startswith("{")]
+    assert lines == [{"n_gpus": 1, "steps": 2, "value": pytest.approx(2000 / 0.1)}]

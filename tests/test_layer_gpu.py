@@ -3,9 +3,12 @@
 tiny and small: every intermediate and every output element.
 t1, skew, long (the 1T-model layer shape, 25 GB of weights): routing,
 counts, offsets and both index maps for all tokens bit for bit, and the
-values of H, Y and the output on a seeded token sample that includes
-tokens of the largest and smallest non-empty expert groups.  This is the
-launch configuration the benchmark times.
+values of H, Y and the output on a seeded sample of 256 random tokens plus
+the tokens of the rows at the edges of the paired GEMM's token tiles (first
+and last row of every tile, both sides of the 256-token MMA split) in the
+largest, the smallest and four random non-empty expert groups -- for the
+skewed workload every tile of its ~16,000-row group.  This is the launch
+configuration the benchmark times.
 """
 import numpy as np
 import pytest
@@ -77,7 +80,7 @@ def test_forward_full_size_sampled(moe, name):
         assert set(counts.tolist()) == {1365, 1366}
     if name == "skew":
         assert (counts == 0).sum() > 100 and counts.max() > 10000
-    toks = pick_sample_tokens(ridx, counts, n_random=16, seed=7)
+    toks = pick_sample_tokens(ridx, counts, n_random=256, seed=7, offsets=offsets, src_token=src)
     x_rows = to_np(inp["x"][torch.from_numpy(toks).cuda()])
     ref = oracle.moe_forward_tokens(x_rows, logits[toks], ExpertSlices(inp["w_gate"]), ExpertSlices(inp["w_up"]),
                                     ExpertSlices(inp["w_down"]), cfg.k, cfg.renormalize)
