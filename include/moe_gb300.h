@@ -271,6 +271,50 @@ MOE_API moe_status_t moe_dequantize_fp8_blockwise(const uint8_t* codes, const fl
                                           void* w_out, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * FP8 expert weights read by the expert GEMMs themselves ("Training a
+ * 1T-Params MoE on EU public infrastructure", FP8 expert weight all-gather:
+ * the weights travel as E4M3 codes with one fp32 scale per 128 values and
+ * become bf16 before the expert computation).  moe_pack_weights_fp8 lays out
+ * the codes and scales of the three projections, as
+ * moe_quantize_fp8_blockwise produced them, for the FP8-weight GEMMs:
+ *   gate_codes, up_codes [E, d, f] uint8 and down_codes [E, f, d] uint8 (the
+ *   stored weights' order); gate_scales, up_scales [E*d*f/128] and
+ *   down_scales [E*f*d/128] fp32 (one per 128 consecutive stored values);
+ *   packed  moe_fp8_packed_weight_bytes(E, d, f) bytes out (about half of
+ *           moe_packed_weight_bytes): the codes of each projection in
+ *           128-row tiles of 64-value K blocks (8 KB each; gate/up tile t
+ *           holds gate features 64t .. 64t+63 and the same up features,
+ *           16 gate rows then their 16 up rows, down tile t output features
+ *           128t .. 128t+127), then per (expert, 128-feature block, K block)
+ *           a record of that block's 64 scales of each projection, times 2^8.
+ * moe_forward_fp8 is moe_forward with those weights: each GEMM stage's codes
+ * are dequantised in shared memory to bf16(E4M3 value x scale), the product
+ * rounded once in fp32 -- exactly what moe_dequantize_fp8_blockwise gives --
+ * and the tensor cores run on them as on bf16 weights, so every
+ * intermediate and the output equal moe_forward's on the dequantised,
+ * moe_pack_weights-packed weights bit for bit.  The HBM traffic of the
+ * weights is halved.  Arguments, workspace, layout and errors as
+ * moe_forward; moe_forward_fp8_timed records events as moe_forward_timed.
+ * Codes must be finite (as the quantiser writes them).
+ * Supported: d and f multiples of 128 (the forward: d a multiple of 256).
+ * Errors: MOE_ERR_INVALID_ARG (NULL, misaligned: codes 16-byte, packed
+ *         256-byte), MOE_ERR_UNSUPPORTED, MOE_ERR_NO_DEVICE, MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+MOE_API size_t moe_fp8_packed_weight_bytes(int32_t E, int32_t d, int32_t f);
+MOE_API moe_status_t moe_pack_weights_fp8(const uint8_t* gate_codes, const float* gate_scales,
+                                          const uint8_t* up_codes, const float* up_scales,
+                                          const uint8_t* down_codes, const float* down_scales, int32_t E,
+                                          int32_t d, int32_t f, void* packed, moe_stream_t stream);
+MOE_API moe_status_t moe_forward_fp8(const void* x, const float* logits, const void* packed_fp8, int64_t T,
+                                     int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out,
+                                     int32_t* topk_idx_out, float* topk_w_out, void* workspace,
+                                     size_t workspace_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_forward_fp8_timed(const void* x, const float* logits, const void* packed_fp8, int64_t T,
+                                           int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize,
+                                           void* out, void* workspace, size_t workspace_bytes,
+                                           moe_stream_t stream, void* const* events);
+
+/* ------------------------------------------------------------------------
  * Stage 4, expert computation — the grouped gate/up GEMM with
  * Silu(gate)*up and the grouped down GEMM (Algorithm 1, stage 4), over the
  * expert groups given by offsets, on the tensor cores (bf16 operands, fp32

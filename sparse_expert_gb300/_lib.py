@@ -62,6 +62,10 @@ SIGNATURES = {
     "moe_pack_weights": (_S, [_P, _P, _P, _I32, _I32, _I32, _P, _P]),
     "moe_quantize_fp8_blockwise": (_S, [_P, _I64, _P, _P, _P]),
     "moe_dequantize_fp8_blockwise": (_S, [_P, _P, _I64, _P, _P]),
+    "moe_fp8_packed_weight_bytes": (_SZ, [_I32, _I32, _I32]),
+    "moe_pack_weights_fp8": (_S, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P]),
+    "moe_forward_fp8": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_fp8_timed": (_S, [_P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "moe_grouped_swiglu_workspace_bytes": (_SZ, []),
     "moe_grouped_swiglu": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_S, [_P, _P, _P, _I64, _I32, _I32, _P, _P]),
@@ -256,6 +260,56 @@ def moe_dequantize_fp8_blockwise(codes, scales, shape=None, stream=None):
     _check(lib.moe_dequantize_fp8_blockwise(_ptr(codes), _ptr(scales), n, _ptr(out), _stream(stream)),
            "moe_dequantize_fp8_blockwise")
     return out if shape is None else out.view(shape)
+
+
+def moe_fp8_packed_weight_bytes(E, d, f) -> int:
+    return lib.moe_fp8_packed_weight_bytes(E, d, f)
+
+
+def moe_pack_weights_fp8(gate, up, down, E, d, f, stream=None):
+    """FP8 weights (uint8 buffer) for moe_forward_fp8 from three (codes, scales)
+    pairs as moe_quantize_fp8_blockwise returns them for w_gate, w_up [E,d,f]
+    and w_down [E,f,d]."""
+    for (c, sc), n in ((gate, "gate"), (up, "up"), (down, "down")):
+        _contig(c, torch.uint8, n + " codes")
+        _contig(sc, torch.float32, n + " scales")
+    dev = gate[0].device
+    packed = torch.empty(lib.moe_fp8_packed_weight_bytes(E, d, f), dtype=torch.uint8, device=dev)
+    _check(lib.moe_pack_weights_fp8(_ptr(gate[0]), _ptr(gate[1]), _ptr(up[0]), _ptr(up[1]), _ptr(down[0]),
+                                    _ptr(down[1]), E, d, f, _ptr(packed), _stream(stream)), "moe_pack_weights_fp8")
+    return packed
+
+
+def moe_forward_fp8(x, logits, packed_fp8, E, k, f, renormalize=True, workspace=None, out=None, topk_idx=None,
+                    topk_w=None, stream=None):
+    """moe_forward with FP8 weights packed by moe_pack_weights_fp8."""
+    _contig(x, torch.bfloat16, "x")
+    _contig(logits, torch.float32, "logits")
+    T, d = x.shape
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(lib.moe_forward_workspace_bytes(T, E, k, d, f), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    _check(lib.moe_forward_fp8(_ptr(x), _ptr(logits), _ptr(packed_fp8), T, d, E, k, f, int(bool(renormalize)),
+                               _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(),
+                               _stream(stream)),
+           "moe_forward_fp8")
+    return out
+
+
+def moe_forward_fp8_timed(x, logits, packed_fp8, E, k, f, workspace, out, events, renormalize=True, stream=None):
+    """moe_forward_fp8 recording events[0..6] at the stage boundaries."""
+    T, d = x.shape
+    s = stream if stream is not None else torch.cuda.current_stream()
+    for ev in events:
+        if ev.cuda_event == 0:
+            ev.record(s)
+    handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    _check(lib.moe_forward_fp8_timed(_ptr(x), _ptr(logits), _ptr(packed_fp8), T, d, E, k, f, int(bool(renormalize)),
+                                     _ptr(out), _ptr(workspace), workspace.numel(), _stream(s), handles),
+           "moe_forward_fp8_timed")
+    return out
 
 
 def moe_grouped_swiglu(x_perm, offsets, E, f, packed, row_scale=None, workspace=None, stream=None):

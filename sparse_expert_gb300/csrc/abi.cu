@@ -55,6 +55,26 @@ moe_status_t check_tile_space(int64_t P, int32_t E, int32_t d, int32_t f) {
   return MOE_OK;
 }
 
+// The FP8-weight layout and GEMMs: d and f multiples of 128 (whole scale
+// blocks per stored row, 128-row code tiles), d a multiple of 256 (the
+// paired down GEMM), and every code row addressable by the tensor maps.
+moe_status_t check_fp8_pack_dims(int32_t E, int32_t d, int32_t f) {
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, 1024]");
+  if (d < 128 || d > 65536 || d % 128 != 0) return fail(MOE_ERR_UNSUPPORTED, "FP8 weights need d a multiple of 128");
+  if (f < 128 || f > 65536 || f % 128 != 0) return fail(MOE_ERR_UNSUPPORTED, "FP8 weights need f a multiple of 128");
+  if (static_cast<int64_t>(E) * 2 * f * (d / 64) >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(E) * d * (f / 64) >= (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "FP8 weights too large for the code tensor maps");
+  return MOE_OK;
+}
+
+moe_status_t check_fp8_forward_dims(int32_t E, int32_t d, int32_t f) {
+  moe_status_t s = check_fp8_pack_dims(E, d, f);
+  if (s != MOE_OK) return s;
+  if (d % 256 != 0) return fail(MOE_ERR_UNSUPPORTED, "the FP8-weight forward needs d a multiple of 256");
+  return MOE_OK;
+}
+
 moe_status_t device_info(DeviceInfo* info) {
   cudaError_t e = current_device_info(info);
   if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver)
@@ -570,12 +590,14 @@ namespace {
 moe_status_t forward_impl(const void* x, const float* logits, const void* router_packed, const void* packed,
                           int64_t T, int32_t d, int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out,
                           int32_t* topk_idx_out, float* topk_w_out, void* workspace, size_t workspace_bytes,
-                          moe_stream_t stream, void* const* events, bool gathered = false) {
+                          moe_stream_t stream, void* const* events, bool gathered = false, bool fp8 = false) {
   moe_status_t s = check_routing(T, E, k);
   if (s != MOE_OK) return s;
   if ((s = check_gemm_dims(d, f)) != MOE_OK) return s;
   const int64_t P = T * k;
   if ((s = check_tile_space(P, E, d, f)) != MOE_OK) return s;
+  if (fp8 && (s = check_fp8_forward_dims(E, d, f)) != MOE_OK) return s;
+  if (fp8 && !aligned(packed, kAlign)) return fail(MOE_ERR_INVALID_ARG, "FP8 packed weights must be 256-byte aligned");
   if (!packed) return fail(MOE_ERR_INVALID_ARG, "NULL packed weights");
   if (T > 0 && (!x || (!logits && !router_packed) || !out)) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (router_packed && E > kRouterMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "the fused router takes E <= 512");
@@ -632,17 +654,30 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* router
   const auto* wgu = static_cast<const __nv_bfloat16*>(packed);
   const auto* wdn = wgu + static_cast<int64_t>(E) * 2 * f * d;
   GroupedGemmProblem g1{x_perm, wgu, offsets, nullptr, h, P, E, d, 2 * f, f, &hdr->tile_counter[0], &hdr->status};
+  // the down GEMM leaves its rows ungated: the gates enter in the output
+  // reduction, where they cost no extra memory traffic
+  GroupedGemmProblem g2{h, wdn, offsets, nullptr, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
+  if (fp8) {
+    size_t off[4];
+    fp8_packed_bytes(E, d, f, off);
+    const auto* pk = static_cast<const uint8_t*>(packed);
+    g1.b = pk + off[0];
+    g1.fp8_scales = reinterpret_cast<const float*>(pk + off[2]);
+    g2.b = pk + off[1];
+    g2.fp8_scales = reinterpret_cast<const float*>(pk + off[3]);
+  }
   if (gathered) {
     g1.a = x;
     g1.gather_rows = src_token;
     g1.a_rows = T;
   }
-  MOE_CUDA(launch_grouped_gemm(g1, Epilogue::kSwiGLU, dev.num_sms, st), "gate/up GEMM launch");
+  MOE_CUDA(fp8 ? launch_grouped_gemm_2sm_fp8(g1, Epilogue::kSwiGLU, dev.num_sms, st)
+               : launch_grouped_gemm(g1, Epilogue::kSwiGLU, dev.num_sms, st),
+           "gate/up GEMM launch");
   MOE_CUDA(mark(4), "event record");
-  // the down GEMM leaves its rows ungated: the gates enter in the output
-  // reduction, where they cost no extra memory traffic
-  GroupedGemmProblem g2{h, wdn, offsets, nullptr, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
-  MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
+  MOE_CUDA(fp8 ? launch_grouped_gemm_2sm_fp8(g2, Epilogue::kScale, dev.num_sms, st)
+               : launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st),
+           "down GEMM launch");
   MOE_CUDA(mark(5), "event record");
   // stage 5: each token sums its k rows weighted by its TopK weights
   MOE_CUDA(launch_combine(y, dest_row, topk_w, T, k, d, out, &hdr->status, dev.num_sms, st), "combine launch");
@@ -695,6 +730,47 @@ moe_status_t moe_forward_gathered_timed(const void* x, const float* logits, cons
   if (!events) return fail(MOE_ERR_INVALID_ARG, "NULL events");
   return forward_impl(x, logits, nullptr, packed, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
                       workspace_bytes, stream, events, true);
+}
+
+size_t moe_fp8_packed_weight_bytes(int32_t E, int32_t d, int32_t f) {
+  if (E < 1 || d < 128 || f < 128 || d % 128 != 0 || f % 128 != 0) return 0;
+  return fp8_packed_bytes(E, d, f, nullptr);
+}
+
+moe_status_t moe_pack_weights_fp8(const uint8_t* gate_codes, const float* gate_scales, const uint8_t* up_codes,
+                                  const float* up_scales, const uint8_t* down_codes, const float* down_scales,
+                                  int32_t E, int32_t d, int32_t f, void* packed, moe_stream_t stream) {
+  moe_status_t s = check_fp8_pack_dims(E, d, f);
+  if (s != MOE_OK) return s;
+  if (!gate_codes || !gate_scales || !up_codes || !up_scales || !down_codes || !down_scales || !packed)
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(gate_codes, 16) || !aligned(up_codes, 16) || !aligned(down_codes, 16) || !aligned(packed, kAlign))
+    return fail(MOE_ERR_INVALID_ARG, "codes must be 16-byte and packed 256-byte aligned");
+  if (!aligned(gate_scales, 4) || !aligned(up_scales, 4) || !aligned(down_scales, 4))
+    return fail(MOE_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  DeviceInfo dev;
+  if ((s = device_info(&dev)) != MOE_OK) return s;
+  MOE_CUDA(launch_pack_weights_fp8(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, E, d, f,
+                                   packed, dev.num_sms, static_cast<cudaStream_t>(stream)),
+           "FP8 pack launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_fp8(const void* x, const float* logits, const void* packed_fp8, int64_t T, int32_t d,
+                             int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out, int32_t* topk_idx_out,
+                             float* topk_w_out, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return forward_impl(x, logits, nullptr, packed_fp8, T, d, E, k, f, renormalize, out, topk_idx_out, topk_w_out,
+                      workspace, workspace_bytes, stream, nullptr, false, true);
+}
+
+moe_status_t moe_forward_fp8_timed(const void* x, const float* logits, const void* packed_fp8, int64_t T, int32_t d,
+                                   int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out, void* workspace,
+                                   size_t workspace_bytes, moe_stream_t stream, void* const* events) {
+  if (!events) return fail(MOE_ERR_INVALID_ARG, "NULL events");
+  for (int i = 0; i <= MOE_FORWARD_STAGES; ++i)
+    if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "NULL event handle");
+  return forward_impl(x, logits, nullptr, packed_fp8, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
+                      workspace_bytes, stream, events, false, true);
 }
 
 moe_status_t moe_forward_host(const void* x_host, const float* logits_host, void* out_host, void* x_dev,

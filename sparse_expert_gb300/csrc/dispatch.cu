@@ -240,10 +240,16 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
         }
         return;  // successors walk past this block on its aggregate
       }
+      // every load of the window in flight at once: one L2 round trip
+      const int n_agg = min(stop, 32);
       for (int e = tid; e < E; e += kDispatchThreads) {
-        int32_t acc = (stop < 32) ? __ldcg(incl + (hi - stop) * E + e) : 0;
-#pragma unroll 8
-        for (int i = 0; i < min(stop, 32); ++i) acc += __ldcg(agg + (hi - i) * E + e);
+        int32_t part[33];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) part[i] = (i < n_agg) ? __ldcg(agg + (hi - i) * E + e) : 0;
+        part[32] = (stop < 32) ? __ldcg(incl + (hi - stop) * E + e) : 0;
+        int32_t acc = 0;
+#pragma unroll
+        for (int i = 0; i < 33; ++i) acc += part[i];
         s_excl[e] += acc;
       }
       __syncthreads();  // s_flag is rewritten next round

@@ -63,6 +63,76 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint32_t* __restr
   }
 }
 
+// ---- the expert GEMMs' FP8 weight layout
+//
+// Codes of one projection, stored [E][K][N] (rows K = the GEMM's reduction
+// index, columns N = its output features), go to 128-row tiles of 64 K
+// values, one tile = 8 KB in the order (expert, tile, K block, row, k):
+// gate/up tile t holds gate features 64t .. 64t+63 and the same up
+// features, with row s = 32g + 16h + r for feature 64t + 16g + r of gate
+// (h = 0) or up (h = 1); down tile t holds output features 128t + s.
+constexpr int kCodeTile = 64;  // bytes of K per tile row, features per transpose block
+
+__global__ void __launch_bounds__(256) pack_codes_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                                         int K, int C, int kind) {
+  __shared__ uint8_t tile[kCodeTile][kCodeTile + 16];
+  const int64_t e = blockIdx.z;
+  const int c0 = blockIdx.x * kCodeTile, k0 = blockIdx.y * kCodeTile;
+  const int t = threadIdx.x;
+  // 64 K rows x 64 feature bytes in, 16 bytes per thread
+  const uint8_t* s = src + (e * K + k0 + t / 4) * static_cast<int64_t>(C) + c0 + (t % 4) * 16;
+  *reinterpret_cast<uint4*>(&tile[t / 4][(t % 4) * 16]) = __ldg(reinterpret_cast<const uint4*>(s));
+  __syncthreads();
+  // 64 feature rows of 64 K bytes out
+  const int c = c0 + t / 4;
+  int tile_i, row, ntiles;
+  if (kind == 2) {  // down
+    tile_i = c / 128;
+    row = c % 128;
+    ntiles = C / 128;
+  } else {          // gate (0) or up (1)
+    tile_i = c / 64;
+    const int j = c % 64;
+    row = (j / 16) * 32 + kind * 16 + j % 16;
+    ntiles = C / 64;
+  }
+  const int kb = k0 / 64, nkb = K / 64;
+  uint8_t v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = tile[(t % 4) * 16 + i][t / 4];
+  uint8_t* d = dst + (((e * ntiles + tile_i) * nkb + kb) * 128 + row) * 64 + (t % 4) * 16;
+  *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(v);
+}
+
+// Scales of one projection (one fp32 per 128 consecutive stored values, so
+// per (expert, K row, 128-feature block)) to one record per (expert,
+// feature block, K block): gate/up 136 floats (64 gate scales, 4 zeros, 64 up
+// scales, 4 zeros), down 64.  Each scale is stored times 2^8 (exact for
+// every finite fp32 scale of a bf16 block: amax / 448 < 2^120).
+__global__ void __launch_bounds__(256) pack_scales_kernel(const float* __restrict__ gate_or_down,
+                                                          const float* __restrict__ up, float* __restrict__ dst,
+                                                          int E, int K, int C, int gate_up) {
+  const int nfb = C / 128, nkb = K / 64, rec = gate_up ? kFp8GateUpRecord : kFp8DownRecord;
+  const int64_t total = static_cast<int64_t>(E) * nfb * nkb * rec;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(i % rec);
+    const int64_t r = i / rec;
+    const int kb = static_cast<int>(r % nkb);
+    const int fb = static_cast<int>((r / nkb) % nfb);
+    const int64_t e = r / (static_cast<int64_t>(nkb) * nfb);
+    float v = 0.0f;
+    const float* src = gate_or_down;
+    int kk = j;
+    if (gate_up && j >= 68) {
+      src = up;
+      kk = j - 68;
+    }
+    if (kk < 64) v = __ldg(src + (e * K + kb * 64 + kk) * nfb + fb) * 256.0f;  // exact: a power of two
+    dst[i] = v;
+  }
+}
+
 int grid_for(int64_t items, int per_block, int num_sms) {
   const int64_t want = (items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(num_sms) * 16;
@@ -77,6 +147,37 @@ cudaError_t launch_quantize_fp8(const void* w, int64_t n, uint8_t* codes, float*
   if (nblocks == 0) return cudaSuccess;
   quantize_kernel<<<grid_for(nblocks, 8, num_sms), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(w), nblocks,
                                                                      reinterpret_cast<uint32_t*>(codes), scales);
+  return cudaGetLastError();
+}
+
+size_t fp8_packed_bytes(int E, int d, int f, size_t* offsets) {
+  const size_t edf = static_cast<size_t>(E) * d * f;
+  const size_t sc_gu = align_up(static_cast<size_t>(E) * (f / 128) * (d / 64) * kFp8GateUpRecord * 4);
+  const size_t sc_dn = align_up(static_cast<size_t>(E) * (d / 128) * (f / 64) * kFp8DownRecord * 4);
+  if (offsets) {
+    offsets[0] = 0;             // gate/up codes
+    offsets[1] = 2 * edf;       // down codes
+    offsets[2] = 3 * edf;       // gate/up scale records
+    offsets[3] = 3 * edf + sc_gu;  // down scale records
+  }
+  return 3 * edf + sc_gu + sc_dn;
+}
+
+cudaError_t launch_pack_weights_fp8(const uint8_t* gate_codes, const float* gate_scales, const uint8_t* up_codes,
+                                    const float* up_scales, const uint8_t* down_codes, const float* down_scales,
+                                    int E, int d, int f, void* packed, int num_sms, cudaStream_t stream) {
+  size_t off[4];
+  fp8_packed_bytes(E, d, f, off);
+  auto* base = static_cast<uint8_t*>(packed);
+  // gate and up: stored [E][d][f] (K = d, features f); down: [E][f][d] (K = f, features d)
+  const dim3 g_gu(f / kCodeTile, d / kCodeTile, E), g_dn(d / kCodeTile, f / kCodeTile, E);
+  pack_codes_kernel<<<g_gu, 256, 0, stream>>>(gate_codes, base + off[0], d, f, 0);
+  pack_codes_kernel<<<g_gu, 256, 0, stream>>>(up_codes, base + off[0], d, f, 1);
+  pack_codes_kernel<<<g_dn, 256, 0, stream>>>(down_codes, base + off[1], f, d, 2);
+  pack_scales_kernel<<<num_sms * 4, 256, 0, stream>>>(gate_scales, up_scales, reinterpret_cast<float*>(base + off[2]),
+                                                     E, d, f, 1);
+  pack_scales_kernel<<<num_sms * 4, 256, 0, stream>>>(down_scales, nullptr, reinterpret_cast<float*>(base + off[3]),
+                                                     E, f, d, 0);
   return cudaGetLastError();
 }
 

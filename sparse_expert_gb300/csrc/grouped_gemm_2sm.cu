@@ -73,21 +73,38 @@ constexpr int UMMA_K = 16;
 constexpr int kTileN = 512;       // tokens per tile (both CTAs): up to two MMAs of N <= 256
 constexpr int kPartN = 256;       // N of one MMA
 constexpr int kHalfRows = 128;    // weight rows and token rows (per part) staged per CTA
-constexpr int kStages = 4;
 constexpr int kABytes = kHalfRows * BK * 2;
 constexpr int kBBytes = kHalfRows * BK * 2;          // one token part
 constexpr int kStageBytes = kABytes + 2 * kBBytes;   // A | B part 1 | B part 2
 constexpr int kEpiParts = 2;     // epilogue warps per TMEM lane quadrant, each a share of the token chunks
 constexpr int kEpiWarps = 4 * kEpiParts;
-constexpr int kHold = 4;        // row-epilogue chunks a warp holds in registers across the hand-back
-constexpr int kHoldH = 4;       // the same for the chunks of H in the gate/up epilogue
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kHoldH = 4;       // gate/up epilogue: chunks of H a warp holds in registers across the hand-back
 constexpr int kTmemCols = 512;    // one accumulator: the tile's weight rows x up to 512 tokens
 constexpr int kEpiBytes = kEpiWarps * 32 * 64;   // per epilogue warp 2 KB: the staging of its stores
 constexpr int kRing = 4;                          // tile ids published ahead
-// readers of a ring slot, counted on the leader's rempty: the leader's MMA
-// thread and epilogue warps, the peer's producer and epilogue warps
-constexpr int kRingReaders = 2 + 2 * kEpiWarps;
+constexpr int kCodeBytes = kHalfRows * BK;        // FP8 codes of one CTA's weight rows and K block
+
+// Per-instantiation layout.  The FP8-weight form adds four converter warps
+// (one weight row per thread) and a code-producer warp, and a ring of code
+// stages (8 KB of 64-byte-swizzled codes and one scale record each) deep
+// enough to keep the halved weight stream's HBM latency hidden; it keeps
+// three MMA stages so that everything fits in 227 KB of shared memory.
+template <bool kFp8>
+struct Cfg {
+  static constexpr int kStages = kFp8 ? 3 : 4;
+  static constexpr int kConvWarps = kFp8 ? 4 : 0;
+  static constexpr int kCodeWarps = kFp8 ? 1 : 0;
+  static constexpr int kCodeStages = kFp8 ? 6 : 0;
+  static constexpr int kCodeStageBytes = 9216;  // codes + a scale record, rounded to 1 KB
+  static constexpr int kThreads = 64 + 32 * (kEpiWarps + kConvWarps + kCodeWarps);
+  // readers of a ring slot, counted on the leader's rempty: the leader's MMA
+  // thread, the peer's producer, and both CTAs' epilogue, converter and
+  // code-producer warps
+  static constexpr int kRingReaders = 2 + 2 * (kEpiWarps + kConvWarps + kCodeWarps);
+  // row epilogue: chunks a warp holds in registers across the hand-back (the
+  // FP8 form has more warps, so fewer registers per thread)
+  static constexpr int kHold = kFp8 ? 4 : 6;
+};
 
 // What the epilogue makes of the accumulator (weight rows x token columns)
 enum : int {
@@ -113,10 +130,19 @@ struct Params {
   int a_mblocks;       // a_mn: 64-column blocks of one packed tile
   int out_cols;        // f or d (kModeSwiGLUBwd: f, rows of 2f)
   int mode;
+  // FP8 weights: the codes come through the weight tensor map (64-byte rows
+  // of 128-row tiles), the scale records from here
+  const float* scales;  // records of rec_floats floats, one per (expert, scale tile, K block)
+  int code_tiles;       // 128-row code tiles per expert
+  int sc_tiles;         // scale tiles per expert
+  int sc_per_cta;       // 1: each CTA of a pair has its own scale tile (down); 0: one per pair (gate/up)
+  int rec_floats;
 };
 
-struct Smem {
-  uint64_t full[kStages], empty[kStages];
+template <bool kFp8>
+struct SmemT {
+  uint64_t full[Cfg<kFp8>::kStages], empty[Cfg<kFp8>::kStages];
+  uint64_t cfull[kFp8 ? Cfg<kFp8>::kCodeStages : 1], cempty[kFp8 ? Cfg<kFp8>::kCodeStages : 1];
   uint64_t tfull[2], tempty[2];
   uint64_t rfull[kRing], rempty[kRing];
   int32_t ring[kRing];
@@ -301,16 +327,73 @@ __device__ __forceinline__ void pack_chunk(const uint32_t (&a)[16], const uint32
   }
 }
 
-// One instantiation per epilogue mode, so that each mode's registers are
-// allocated for its own epilogue.
-template <int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// FP8 weights: the fp32 whose bits are byte `sel` picks of `word` (an E4M3
+// code) moved so that its sign is bit 31 and its other seven bits are bits
+// 26..20.  That float is the code's value times 2^-120 exactly: the four
+// exponent bits land in the fp32 exponent with a bias 120 lower, normal
+// codes on normal floats and the subnormal codes (exponent 0) on fp32
+// subnormals of the same significand.  sel = byte b into byte 2, its sign
+// replicated into byte 3, zeros below (prmt selector ((8|b) << 12) | (b << 8)
+// | 0x44).
+__device__ __forceinline__ float e4m3_times_2m120(uint32_t word, uint32_t sel) {
+  uint32_t x;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(x) : "r"(word), "r"(0u), "r"(sel));
+  return __uint_as_float((x << 4) & 0x87F00000u);
+}
+
+// One weight row of one K block: its 64 E4M3 codes (a 64-byte row of a tile
+// loaded with 64-byte swizzling: piece c of row s at c ^ ((s >> 1) & 3)) and
+// the K block's 64 scales stored times 2^8 become bf16(value x scale), the
+// product rounded once in fp32 and then to bf16 -- the dequantisation of the
+// "FP8 expert weight all-gather", bit for bit -- written as the row's 128
+// bytes of the 128-byte-swizzled K-major A operand (piece j at j ^ (s & 7)).
+// value x scale = (value 2^-120 x 2^112) x (scale x 2^8): both factors exact
+// and in the normal range, so the one fp32 rounding is that of value x
+// scale.
+__device__ __forceinline__ void convert_code_row(const uint8_t* crow, int s, const float* sc, uint8_t* arow) {
+  uint4 q[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) q[c] = *reinterpret_cast<const uint4*>(crow + ((c ^ ((s >> 1) & 3)) << 4));
+  const uint32_t sel[4] = {0x8044u, 0x9144u, 0xA244u, 0xB344u};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t w[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
+    float scl[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = *reinterpret_cast<const float4*>(sc + 16 * c + 4 * i);
+      scl[4 * i] = v.x;
+      scl[4 * i + 1] = v.y;
+      scl[4 * i + 2] = v.z;
+      scl[4 * i + 3] = v.w;
+    }
+    uint32_t o[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int i0 = 2 * m, i1 = 2 * m + 1;
+      const float p0 = __fmul_rn(__fmul_rn(e4m3_times_2m120(w[i0 >> 2], sel[i0 & 3]), 0x1p112f), scl[i0]);
+      const float p1 = __fmul_rn(__fmul_rn(e4m3_times_2m120(w[i1 >> 2], sel[i1 & 3]), 0x1p112f), scl[i1]);
+      o[m] = pack_bf16x2(p0, p1);
+    }
+    *reinterpret_cast<uint4*>(arow + (((2 * c) ^ (s & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(arow + (((2 * c + 1) ^ (s & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// One instantiation per epilogue mode (and weight format), so that each gets
+// the registers of its own epilogue.
+template <int kMode, bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                         const Params p) {
+  using C = Cfg<kFp8>;
+  using Smem = SmemT<kFp8>;
+  constexpr int kStages = C::kStages;
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   uint8_t* s_stage0 = base;  // stage s at s_stage0 + s * kStageBytes: A | B part 1 | B part 2
-  uint8_t* s_epi = s_stage0 + kStages * kStageBytes;
+  uint8_t* s_code0 = s_stage0 + kStages * kStageBytes;  // FP8: code stage c at s_code0 + c * kCodeStageBytes
+  uint8_t* s_epi = s_code0 + C::kCodeStages * C::kCodeStageBytes;
   Smem* S = reinterpret_cast<Smem*>(s_epi + kEpiBytes);
   int32_t* s_off = reinterpret_cast<int32_t*>(S + 1);
   int32_t* s_pre = s_off + (p.E + 1);
@@ -346,8 +429,14 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     tmem_alloc_pair(&S->tmem_base, kTmemCols);
   } else if (warp == 2 && lane == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&S->full[i], 1);
+      // the leader's producer (bytes to come), and with FP8 weights every
+      // converter warp of both CTAs once its rows are in the A slot
+      mbar_init(&S->full[i], 1 + 2 * C::kConvWarps);
       mbar_init(&S->empty[i], 1);
+    }
+    for (int i = 0; i < C::kCodeStages; ++i) {
+      mbar_init(&S->cfull[i], 1);
+      mbar_init(&S->cempty[i], C::kConvWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S->tfull[i], 1);
@@ -355,7 +444,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&S->rfull[i], 1);
-      mbar_init(&S->rempty[i], kRingReaders);  // the leader's copy is used
+      mbar_init(&S->rempty[i], C::kRingReaders);  // the leader's copy is used
     }
     mbar_init(&S->drain, 1);
     S->abort = 0;
@@ -417,7 +506,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         const int n1 = min(x.n, kPartN), n2 = x.n - n1;
         const int xrow1 = x.tok0 + static_cast<int>(rank) * (n1 >> 1);
         const int xrow2 = x.tok0 + n1 + static_cast<int>(rank) * (n2 >> 1);
-        const uint32_t bytes = 2 * (kABytes + kBBytes + (n2 > 0 ? kBBytes : 0));  // both CTAs
+        // both CTAs' copies; with FP8 weights the A slots are written by the
+        // converter warps, whose arrivals the stage barrier counts instead
+        const uint32_t bytes = 2 * ((kFp8 ? 0 : kABytes) + kBBytes + (n2 > 0 ? kBBytes : 0));
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&S->empty[stage], phase ^ 1u, abort_flag)) {
             failed = true;
@@ -426,7 +517,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           const uint32_t lead_full = leader_addr(&S->full[stage]);
           uint8_t* st = s_stage0 + stage * kStageBytes;
           if (rank == 0) mbar_arrive_expect_tx(&S->full[stage], bytes);
-          if (p.a_mn) {
+          if constexpr (kFp8) {
+            // the code producer and the converters fill the A slot
+          } else if (p.a_mn) {
             // K rows kb*64 .. +63 lie in packed tile k0 / a_tile_rows; M values
             // w0 .. w0+127 are its column blocks w0/64 and w0/64 + 1
             const int k0 = kb * BK;
@@ -512,6 +605,106 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         aphase ^= 1u;
       }
       umma_commit_pair(&S->drain);
+    }
+  } else if (kFp8 && warp >= 2 + kEpiWarps && warp < 2 + kEpiWarps + C::kConvWarps) {
+    // ------------------------------------------------ FP8 code converters
+    // thread = one of this CTA's 128 weight rows, per K block: its codes and
+    // the block's scales from the code stage to bf16 in the MMA stage's A
+    // slot, then a release arrive on the leader's stage barrier
+    const int row = (warp - 2 - kEpiWarps) * 32 + lane;
+    // gate/up rows come in quarter order: 16 gate rows, then 16 up rows
+    const int half = (kMode == kModeSwiGLU) ? ((row >> 4) & 1) : 0;
+    const int num_kb = p.K / BK;
+    int stage = 0, cstage = 0;
+    uint32_t phase = 0, cphase = 0;
+    int rs = 0;
+    uint32_t rphase = 0;
+    const uint32_t lead_rempty0 = leader_addr(&S->rempty[0]);
+    for (;;) {
+      if (!wait_cluster_warp(&S->rfull[rs], rphase, abort_flag)) {
+        failed = true;
+        break;
+      }
+      const int t = S->ring[rs];
+      __syncwarp();
+      if (lane == 0) arrive_remote(lead_rempty0 + rs * static_cast<uint32_t>(sizeof(uint64_t)));
+      if (++rs == kRing) {
+        rs = 0;
+        rphase ^= 1u;
+      }
+      if (t < 0) break;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        // the codes have landed, and the MMA is done with the A slot
+        if (!mbar_wait_warp(&S->cfull[cstage], cphase, abort_flag) ||
+            !mbar_wait_warp(&S->empty[stage], phase ^ 1u, abort_flag)) {
+          failed = true;
+          break;
+        }
+        const uint8_t* cs = s_code0 + cstage * C::kCodeStageBytes;
+        convert_code_row(cs + row * BK, row, reinterpret_cast<const float*>(cs + kCodeBytes) + half * 68,
+                         s_stage0 + stage * kStageBytes + row * (BK * 2));
+        // the generic-proxy stores become visible to the tensor cores' reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          arrive_remote(leader_addr(&S->full[stage]));
+          mbar_arrive(&S->cempty[cstage]);
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++cstage == C::kCodeStages) {
+          cstage = 0;
+          cphase ^= 1u;
+        }
+      }
+      if (failed) break;
+    }
+  } else if (kFp8 && warp == 2 + kEpiWarps + C::kConvWarps) {
+    // ----------------------------------------------- FP8 code producer
+    // per K block: this CTA's 128 rows of codes (one 8 KB TMA box, 64-byte
+    // swizzle) and the block's scale record, into the next code stage
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_w);
+      const int num_kb = p.K / BK;
+      const uint32_t rec_bytes = static_cast<uint32_t>(p.rec_floats) * 4u;
+      int cstage = 0;
+      uint32_t cphase = 0;
+      int rs = 0;
+      uint32_t rphase = 0;
+      for (;;) {
+        if (!wait_cluster(&S->rfull[rs], rphase, abort_flag)) {
+          failed = true;
+          break;
+        }
+        const int t = S->ring[rs];
+        arrive_remote(leader_addr(&S->rempty[rs]));
+        if (++rs == kRing) {
+          rs = 0;
+          rphase ^= 1u;
+        }
+        if (t < 0) break;
+        const Tile x = decode(t, s_off, s_pre, p.E, p.m_tiles);
+        const int ctile = x.mt * 2 + static_cast<int>(rank);  // this CTA's 128-row code tile
+        const int64_t cblk = (static_cast<int64_t>(x.e) * p.code_tiles + ctile) * num_kb;
+        const int64_t rec0 = (static_cast<int64_t>(x.e) * p.sc_tiles + (p.sc_per_cta ? ctile : x.mt)) * num_kb;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&S->cempty[cstage], cphase ^ 1u, abort_flag)) {
+            failed = true;
+            break;
+          }
+          uint8_t* cs = s_code0 + cstage * C::kCodeStageBytes;
+          mbar_arrive_expect_tx(&S->cfull[cstage], kCodeBytes + rec_bytes);
+          tma_load_2d(cs, &tm_w, &S->cfull[cstage], 0, static_cast<int32_t>((cblk + kb) * kHalfRows));
+          bulk_load(cs + kCodeBytes, p.scales + (rec0 + kb) * p.rec_floats, rec_bytes, &S->cfull[cstage]);
+          if (++cstage == C::kCodeStages) {
+            cstage = 0;
+            cphase ^= 1u;
+          }
+        }
+        if (failed) break;
+      }
     }
   } else {
     // ---------------------------------------------------------- epilogue
@@ -731,6 +924,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           pack_chunk(v, w, pk);
         };
         const int n_chunks = c_begin < c_end ? (c_end - c_begin + 31) >> 5 : 0;
+        constexpr int kHold = C::kHold;
         const int n_stream = max(n_chunks - kHold, 0);
 #pragma unroll 1
         for (int i = 0; i < n_stream; ++i) {
@@ -794,31 +988,39 @@ bool grouped_gemm_2sm_supported(const GroupedGemmProblem& pb, Epilogue epi) {
   return pb.out_cols % 256 == 0 && down_tile_n(pb.out_cols) == 256;
 }
 
-// the largest expert count the library takes still fits the opt-in 227 KB
-static_assert(1024 + kStages * kStageBytes + kEpiBytes + sizeof(Smem) + 2 * (MOE_MAX_EXPERTS + 1) * sizeof(int32_t) <=
-                  227 * 1024,
-              "shared memory of the paired GEMM at MOE_MAX_EXPERTS");
-
-size_t grouped_gemm_2sm_smem(int E) {
-  return 1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiBytes + sizeof(Smem) +
-         2 * static_cast<size_t>(E + 1) * sizeof(int32_t);
-}
-
 namespace {
 
+template <bool kFp8>
+constexpr size_t smem_bytes(int E) {
+  return 1024 + static_cast<size_t>(Cfg<kFp8>::kStages) * kStageBytes +
+         static_cast<size_t>(Cfg<kFp8>::kCodeStages) * Cfg<kFp8>::kCodeStageBytes + kEpiBytes +
+         sizeof(SmemT<kFp8>) + 2 * static_cast<size_t>(E + 1) * sizeof(int32_t);
+}
+
+// the largest expert count the library takes still fits the opt-in 227 KB
+static_assert(smem_bytes<false>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory of the paired GEMM");
+static_assert(smem_bytes<true>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory of the FP8-weight paired GEMM");
+
+template <bool kFp8>
 cudaError_t launch_pairs(const CUtensorMap& mw, const CUtensorMap& mx, const Params& prm, int64_t P, int num_sms,
                          cudaStream_t stream) {
-  const size_t smem = grouped_gemm_2sm_smem(prm.E);
-  auto* kernel = prm.mode == kModeSwiGLU      ? grouped_gemm_2sm_kernel<kModeSwiGLU>
-                 : prm.mode == kModeSwiGLUBwd ? grouped_gemm_2sm_kernel<kModeSwiGLUBwd>
-                                              : grouped_gemm_2sm_kernel<kModeRows>;
+  const size_t smem = smem_bytes<kFp8>(prm.E);
+  void (*kernel)(const CUtensorMap, const CUtensorMap, const Params);
+  if constexpr (kFp8) {
+    kernel = prm.mode == kModeSwiGLU ? grouped_gemm_2sm_kernel<kModeSwiGLU, true>
+                                     : grouped_gemm_2sm_kernel<kModeRows, true>;
+  } else {
+    kernel = prm.mode == kModeSwiGLU      ? grouped_gemm_2sm_kernel<kModeSwiGLU, false>
+             : prm.mode == kModeSwiGLUBwd ? grouped_gemm_2sm_kernel<kModeSwiGLUBwd, false>
+                                          : grouped_gemm_2sm_kernel<kModeRows, false>;
+  }
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   // persistent: one pair per two SMs, never more pairs than an upper bound on tiles
   const int64_t max_tiles = (P / kTileN + prm.E) * static_cast<int64_t>(prm.m_tiles);
   int pairs = num_sms / 2;
   if (max_tiles < pairs) pairs = static_cast<int>(max_tiles);
-  kernel<<<2 * pairs, kThreads, smem, stream>>>(mw, mx, prm);
+  kernel<<<2 * pairs, Cfg<kFp8>::kThreads, smem, stream>>>(mw, mx, prm);
   return cudaGetLastError();
 }
 
@@ -856,7 +1058,42 @@ cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, 
   prm.a_tiles = n_rows / a_tile_rows;
   prm.out_cols = pb.out_cols;
   prm.mode = swiglu ? kModeSwiGLU : kModeRows;
-  return launch_pairs(mw, mx, prm, pb.P, num_sms, stream);
+  return launch_pairs<false>(mw, mx, prm, pb.P, num_sms, stream);
+}
+
+bool grouped_gemm_2sm_fp8_supported(const GroupedGemmProblem& pb, Epilogue epi) {
+  if (!grouped_gemm_2sm_supported(pb, epi) || pb.K % 128 != 0 || pb.out_cols % 128 != 0) return false;
+  // code rows (int32 TMA coordinates) of the whole projection
+  return static_cast<int64_t>(pb.E) * pb.n_per_expert * (pb.K / BK) < (int64_t(1) << 31);
+}
+
+cudaError_t launch_grouped_gemm_2sm_fp8(const GroupedGemmProblem& pb, Epilogue epi, int num_sms,
+                                        cudaStream_t stream) {
+  if (pb.P == 0) return cudaSuccess;
+  if (!grouped_gemm_2sm_fp8_supported(pb, epi) || pb.fp8_scales == nullptr) return cudaErrorNotSupported;
+  const bool swiglu = epi == Epilogue::kSwiGLU;
+  const int n_rows = pb.n_per_expert;  // weight rows per expert (2f or d)
+  const int num_kb = pb.K / BK;
+  CUtensorMap mw, mx;
+  if (!make_u8_map_rows64_sw64(&mw, pb.b, static_cast<int64_t>(pb.E) * n_rows * num_kb, kHalfRows))
+    return cudaErrorInvalidValue;
+  if (!make_bf16_map_2d(&mx, pb.a, pb.P, pb.K, BK, kHalfRows)) return cudaErrorInvalidValue;
+  Params prm = base_params(pb.offsets, pb.E, pb.K, pb.tile_counter, pb.status);
+  prm.row_scale = swiglu ? nullptr : pb.row_scale;
+  prm.out = static_cast<__nv_bfloat16*>(pb.out);
+  prm.m_tiles = n_rows / (2 * kHalfRows);
+  prm.a_tile_rows = kHalfRows;  // the producer's bf16 weight indexing is unused here, but kept defined
+  prm.a_tiles = n_rows / kHalfRows;
+  prm.out_cols = pb.out_cols;
+  prm.mode = swiglu ? kModeSwiGLU : kModeRows;
+  prm.scales = pb.fp8_scales;
+  prm.code_tiles = n_rows / kHalfRows;
+  // gate/up: a pair's two code tiles (gate/up features 128 mt .. +127) share
+  // one 128-feature scale block; down: each CTA's 128 output features are one
+  prm.sc_tiles = swiglu ? pb.out_cols / 128 : n_rows / kHalfRows;
+  prm.sc_per_cta = swiglu ? 0 : 1;
+  prm.rec_floats = swiglu ? kFp8GateUpRecord : kFp8DownRecord;
+  return launch_pairs<true>(mw, mx, prm, pb.P, num_sms, stream);
 }
 
 bool dgrad_2sm_supported(const DgradProblem& g) {
@@ -883,7 +1120,7 @@ cudaError_t launch_dgrad_2sm(const DgradProblem& g, int num_sms, cudaStream_t st
   prm.a_mblocks = g.m_out / 64;
   prm.out_cols = g.m_out;
   prm.mode = g.mode == DgradEpilogue::kSwiGLUBwd ? kModeSwiGLUBwd : kModeRows;
-  return launch_pairs(mw, mx, prm, g.P, num_sms, stream);
+  return launch_pairs<false>(mw, mx, prm, g.P, num_sms, stream);
 }
 
 }  // namespace moe

@@ -40,6 +40,16 @@ cudaError_t launch_quantize_fp8(const void* w, int64_t n, uint8_t* codes, float*
                                 cudaStream_t stream);
 cudaError_t launch_dequantize_fp8(const uint8_t* codes, const float* scales, int64_t n, void* out, int num_sms,
                                   cudaStream_t stream);
+// The expert GEMMs' FP8 weight layout (moe_pack_weights_fp8): gate/up codes,
+// down codes, gate/up scale records, down scale records; `offsets` (4
+// entries, may be null) receives their byte offsets.  Needs d and f
+// multiples of 128.
+constexpr int kFp8GateUpRecord = 136;  // floats per gate/up scale record: 64 gate, 4 pad, 64 up, 4 pad
+constexpr int kFp8DownRecord = 64;     // floats per down scale record
+size_t fp8_packed_bytes(int E, int d, int f, size_t* offsets);
+cudaError_t launch_pack_weights_fp8(const uint8_t* gate_codes, const float* gate_scales, const uint8_t* up_codes,
+                                    const float* up_scales, const uint8_t* down_codes, const float* down_scales,
+                                    int E, int d, int f, void* packed, int num_sms, cudaStream_t stream);
 
 // ---- stages 2-3
 constexpr int kDispatchThreads = 256;
@@ -96,6 +106,7 @@ struct GroupedGemmProblem {
   const int32_t* gather_rows = nullptr;  // gate/up only: A row r is a[gather_rows[r]] (src_token)
   void* gu_out = nullptr;                // gate/up, paired form only: also store G, U [P, 2f]
   int64_t a_rows = 0;                    // rows of a when gathering (T)
+  const float* fp8_scales = nullptr;     // FP8 weights: b holds codes, these the scale records
 };
 enum class Epilogue { kSwiGLU, kScale };
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
@@ -104,6 +115,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int 
 // per expert (2f, or d) are a multiple of 256.
 bool grouped_gemm_2sm_supported(const GroupedGemmProblem& pb, Epilogue epi);
 cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
+// The paired form reading FP8 weights (moe_pack_weights_fp8's layout): b =
+// this projection's codes, fp8_scales = its scale records.  Converter warps
+// dequantise each K block in shared memory exactly as
+// moe_dequantize_fp8_blockwise does, so the results equal the bf16 path's on
+// those dequantised weights bit for bit.  Needs what the paired form needs
+// and d, f multiples of 128.
+bool grouped_gemm_2sm_fp8_supported(const GroupedGemmProblem& pb, Epilogue epi);
+cudaError_t launch_grouped_gemm_2sm_fp8(const GroupedGemmProblem& pb, Epilogue epi, int num_sms,
+                                        cudaStream_t stream);
 
 // A dgrad GEMM of the backward on SM pairs: out[r, :] = tokens[r, :] W_e^T
 // for the rows r of expert e, with W_e the forward's packed weights read
@@ -168,6 +188,9 @@ bool make_bf16_map_2d_sw64(CUtensorMap* map, const void* ptr, int64_t rows, int6
 bool make_bf16_map_gate_up_quads(CUtensorMap* map, const void* ptr, int64_t blocks);
 bool make_bf16_map_col_blocks(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows,
                               int box_blocks);
+// Byte rows of 64 (FP8 codes) as [rows][64], box of box_rows rows, 64-byte
+// swizzle: 16-byte piece c of row r lands at piece c ^ ((r >> 1) & 3).
+bool make_u8_map_rows64_sw64(CUtensorMap* map, const void* ptr, int64_t rows, int box_rows);
 
 // Bounded-wait check: one block waits on a phase that never completes and
 // records a timeout in *status after limit_ns.

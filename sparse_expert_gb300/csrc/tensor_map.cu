@@ -28,13 +28,13 @@ EncodeTiledFn encode_fn() {
 }
 
 bool encode(CUtensorMap* map, const void* ptr, cuuint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides,
-            const cuuint32_t* box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+            const cuuint32_t* box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+            CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, type, rank, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -91,6 +91,13 @@ bool make_bf16_map_gate_up_quads(CUtensorMap* map, const void* ptr, int64_t bloc
   const cuuint64_t strides[3] = {128, 64 * 128, 16 * 128};
   const cuuint32_t box[4] = {64, 16, 2, 4};
   return encode(map, ptr, 4, dims, strides, box);
+}
+
+bool make_u8_map_rows64_sw64(CUtensorMap* map, const void* ptr, int64_t rows, int box_rows) {
+  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  return encode(map, ptr, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
 }  // namespace moe
