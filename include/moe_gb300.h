@@ -162,10 +162,11 @@ MOE_API moe_status_t moe_router_topk(const void* x, const void* router_packed, i
  *   row_w     [P] fp32 out, optional (NULL skips it): row_w[dest_row[p]] =
  *             topk_w[p]; needs topk_w.
  *   topk_idx  [T, k] int32 in; topk_w [T, k] fp32 in, optional.
- * Implementation: a block histogram, then one pass in which each block of
- * pairs takes its per-expert base from its predecessors by decoupled
- * look-back.  An expert index outside [0, E) sets MOE_ERR_BAD_INDEX in the
- * device status word and its pair is dropped.
+ * Implementation: a table of per-chunk expert counts (chunks of 2,048
+ * pairs), then one pass, a block per chunk, that takes every chunk's
+ * per-expert base from the table's column sums; no block waits on another.
+ * An expert index outside [0, E) sets MOE_ERR_BAD_INDEX in the device
+ * status word and its pair is dropped (dest_row = -1).
  * Workspace: moe_dispatch_workspace_bytes(T, E, k) bytes.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE,
  *         MOE_ERR_CUDA.
@@ -185,11 +186,11 @@ MOE_API moe_status_t moe_dispatch_scan(const int32_t* topk_idx, const float* top
  * input and output buffers, and latency-critical loops that must not call
  * cudaMalloc.  The pages have no counterpart of this entry point.
  *   Arguments and outputs are those of moe_dispatch_scan, without the
- *   workspace.  The scratch is a fixed 4 MiB device array inside the
- *   library (held on every GPU that loads it until the process exits):
+ *   workspace.  The scratch (status word and count table) is a fixed 4 MiB
+ *   device array inside the library (held on every GPU that loads it until the process exits):
  *   problems whose scratch, moe_dispatch_workspace_bytes(T, E, k), exceeds
  *   4 MiB are rejected with MOE_ERR_UNSUPPORTED (for example E = 384 and
- *   k = 8 fit up to about 170,000 tokens).
+ *   k = 8 fit up to about 699,000 tokens).
  *   The first call on a device looks up the array's address with that
  *   device current; make it before any stream capture.  All calls share
  *   the array: calls that overlap on the GPU race and must be serialised
@@ -201,8 +202,8 @@ MOE_API moe_status_t moe_dispatch_scan(const int32_t* topk_idx, const float* top
  *
  * moe_dispatch_noalloc_status waits for `stream` and copies into *status
  * (host memory) the device status of the latest moe_dispatch_scan_noalloc
- * on the current device: MOE_OK, or the first error its kernels found
- * (MOE_ERR_BAD_INDEX, MOE_ERR_TIMEOUT).  The next call clears it, so read
+ * on the current device: MOE_OK, or MOE_ERR_BAD_INDEX when an expert index
+ * was outside [0, E).  The next call clears it, so read
  * it before that call is enqueued.  Allocates nothing.
  * Errors: MOE_ERR_INVALID_ARG (NULL status), MOE_ERR_NO_DEVICE, MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
@@ -428,7 +429,7 @@ MOE_API moe_status_t moe_route_backward(const float* logits, const int32_t* topk
 
 /* ------------------------------------------------------------------------
  * The whole layer forward (Algorithm 1, stages 1-5) on one stream, with no
- * host synchronisation: route + histogram, look-back index pass, permute,
+ * host synchronisation: route + per-chunk counts, index pass, permute,
  * gate/up GEMM with SwiGLU, down GEMM (rows left ungated), combine weighted
  * by the TopK weights.  The layout's y therefore holds each routed row's
  * expert output before its gate; row_w still holds the gate of every row.
@@ -437,9 +438,6 @@ MOE_API moe_status_t moe_route_backward(const float* logits, const int32_t* topk
  *   fp32 out, optional (the workspace keeps its own copy).
  * Workspace: moe_forward_workspace_bytes(T, E, k, d, f); the intermediates
  * stay there after the call at the byte offsets moe_forward_layout gives.
- * If a look-back wait of the index pass runs out, its pairs get dest_row
- * = -1, the permute and the combine skip them, and the status word reads
- * MOE_ERR_TIMEOUT; the output rows of those tokens are then incomplete.
  * Errors: as the stages.
  * ---------------------------------------------------------------------- */
 typedef struct {
@@ -525,7 +523,7 @@ MOE_API moe_status_t moe_forward_gathered_timed(const void* x, const float* logi
  * moe_forward with stage timing: identical work, plus cudaEventRecord of
  * events[i] (caller-created cudaEvent_t handles, MOE_FORWARD_STAGES + 1 of
  * them) on `stream` at the stage boundaries
- *   0 start | route | 1 | look-back index | 2 | permute | 3 | gate/up GEMM |
+ *   0 start | route | 1 | index | 2 | permute | 3 | gate/up GEMM |
  *   4 | down GEMM | 5 | combine | 6
  * so that cudaEventElapsedTime(events[i], events[i+1]) is the time of one
  * stage's kernel (stage 0 also holds the workspace clear).

@@ -88,7 +88,7 @@ moe_status_t device_info(DeviceInfo* info) {
 
 // ---- moe_forward workspace layout
 struct ForwardLayout {
-  size_t header, flags_end, counts, dispatch_state, offsets;
+  size_t header, hist, counts, offsets;
   size_t topk_idx, topk_w, src_token, dest_row, row_w, x_perm, h, y, total;
   size_t clear_bytes;
 };
@@ -98,14 +98,12 @@ ForwardLayout forward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t
   ForwardLayout L{};
   size_t o = 0;
   L.header = o;
-  o = dispatch_clear_bytes(P);  // header + look-back flags
-  L.flags_end = o;
+  o = sizeof(WsHeader);
+  L.hist = o;                   // the per-chunk count table, filled by atomic adds of the route kernel
+  o += dispatch_hist_bytes(P, E);
+  L.clear_bytes = o;            // the header and the table start at zero
   L.counts = o;
   o += align_up(static_cast<size_t>(E) * 4);
-  L.clear_bytes = o;            // header, flags and counts start at zero
-  L.dispatch_state = o;
-  // flags live in the cleared region; the state's agg/incl arrays follow
-  o += dispatch_state_bytes(P, E);
   L.offsets = o;
   o += align_up(static_cast<size_t>(E + 1) * 4);
   L.topk_idx = o;
@@ -151,14 +149,6 @@ BackwardLayout backward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32
   o += align_up(static_cast<size_t>(P) * 4);
   L.total = o;
   return L;
-}
-
-// Dispatch state inside a workspace: flags right after the header (cleared
-// with it), agg/incl at `state_at` (not cleared).
-DispatchState dispatch_state_split(void* ws, size_t state_at, int64_t P, int E) {
-  DispatchState st = dispatch_state_at(static_cast<char*>(ws) + state_at, P, E);
-  st.flags = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(WsHeader));
-  return st;
 }
 
 }  // namespace
@@ -294,8 +284,7 @@ moe_status_t moe_router_topk(const void* x, const void* router_packed, int64_t T
 
 size_t moe_dispatch_workspace_bytes(int64_t T, int32_t E, int32_t k) {
   if (T < 0 || E < 1 || k < 1) return 0;
-  const int64_t P = T * k;
-  return dispatch_clear_bytes(P) + dispatch_state_bytes(P, E);
+  return sizeof(WsHeader) + dispatch_hist_bytes(T * k, E);
 }
 
 moe_status_t moe_dispatch_scan(const int32_t* topk_idx, const float* topk_w, int64_t T, int32_t E, int32_t k,
@@ -313,16 +302,17 @@ moe_status_t moe_dispatch_scan(const int32_t* topk_idx, const float* topk_w, int
   if ((s = device_info(&dev)) != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t P = T * k;
-  MOE_CUDA(cudaMemsetAsync(workspace, 0, dispatch_clear_bytes(P), st), "workspace clear");
-  MOE_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, st), "counts clear");
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st), "workspace clear");
   if (P == 0) {
+    MOE_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, st), "counts clear");
     MOE_CUDA(cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st), "offsets clear");
     return MOE_OK;
   }
   auto* hdr = static_cast<WsHeader*>(workspace);
-  MOE_CUDA(launch_histogram(topk_idx, P, E, counts, &hdr->status, dev.num_sms, st), "histogram launch");
-  DispatchState dst = dispatch_state_split(workspace, dispatch_clear_bytes(P), P, E);
-  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, workspace, dst, st),
+  auto* hist = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + sizeof(WsHeader));
+  MOE_CUDA(launch_chunk_histogram(topk_idx, P, E, hist, &hdr->status, st), "histogram launch");
+  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, hist, counts, offsets, src_token, dest_row, row_w, &hdr->status,
+                        st),
            "index launch");
   return MOE_OK;
 }
@@ -611,6 +601,7 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* router
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   auto* hdr = reinterpret_cast<WsHeader*>(ws);
+  auto* hist = reinterpret_cast<int32_t*>(ws + L.hist);
   auto* counts = reinterpret_cast<int32_t*>(ws + L.counts);
   auto* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   int32_t* topk_idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t*>(ws + L.topk_idx);
@@ -628,23 +619,23 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* router
   MOE_CUDA(mark(0), "event record");
   MOE_CUDA(cudaMemsetAsync(ws, 0, L.clear_bytes, st), "workspace clear");
   if (T == 0) {
+    MOE_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, st), "counts clear");
     MOE_CUDA(cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st), "offsets clear");
     for (int i = 1; i <= MOE_FORWARD_STAGES; ++i) MOE_CUDA(mark(i), "event record");
     return MOE_OK;
   }
-  // stage 1 (+ token counts)
+  // stage 1 (+ the per-chunk token counts)
   if (router_packed) {
-    MOE_CUDA(launch_router_topk(x, router_packed, T, d, E, k, renormalize, topk_idx, topk_w, counts, &hdr->status,
-                                st),
+    MOE_CUDA(launch_router_topk(x, router_packed, T, d, E, k, renormalize, topk_idx, topk_w, hist, &hdr->status, st),
              "router launch");
   } else {
-    MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, counts, dev.num_sms, st),
+    MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, hist, dev.num_sms, st),
              "route launch");
   }
   MOE_CUDA(mark(1), "event record");
-  // stages 2-3: offsets, index maps and the gate of every row
-  DispatchState dstate = dispatch_state_split(ws, L.dispatch_state, P, E);
-  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, ws, dstate, st),
+  // stages 2-3: counts, offsets, index maps and the gate of every row
+  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, hist, counts, offsets, src_token, dest_row, row_w, &hdr->status,
+                        st),
            "index launch");
   MOE_CUDA(mark(2), "event record");
   // stage 4
@@ -889,6 +880,7 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   char* ws = static_cast<char*>(workspace);
   auto* hdr = reinterpret_cast<WsHeader*>(ws);
   const ForwardLayout& F = L.F;
+  auto* hist = reinterpret_cast<int32_t*>(ws + F.hist);
   auto* counts = reinterpret_cast<int32_t*>(ws + F.counts);
   auto* offsets = reinterpret_cast<int32_t*>(ws + F.offsets);
   auto* topk_idx = reinterpret_cast<int32_t*>(ws + F.topk_idx);
@@ -939,10 +931,10 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   }
   // forward recomputation: stages 1-4 with G and U kept; the down GEMM
   // leaves its rows ungated (the gates enter in the output reduction)
-  MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, counts, dev.num_sms, st),
+  MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, hist, dev.num_sms, st),
            "route launch");
-  DispatchState dstate = dispatch_state_split(ws, F.dispatch_state, P, E);
-  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, ws, dstate, st),
+  MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, hist, counts, offsets, src_token, dest_row, row_w, &hdr->status,
+                        st),
            "index launch");
   MOE_CUDA(launch_permute(x, T, d, dest_row, k, x_perm, &hdr->status, dev.num_sms, st), "permute launch");
   MOE_CUDA(mark(1), "event record");

@@ -17,7 +17,7 @@ enum : int32_t {
 // Every workspace starts with this header; one memset clears it per call.
 struct WsHeader {
   int32_t status;          // first device error, or 0
-  int32_t ticket;          // dynamic block ticket of the look-back pass
+  int32_t unused;
   int32_t tile_counter[6]; // persistent-GEMM tile counters (forward: gate/up, down;
                            // backward: dgrad down, dgrad gate/up, wgrad down, wgrad gate/up)
   int32_t reserved[56];

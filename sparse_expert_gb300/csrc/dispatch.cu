@@ -6,79 +6,57 @@
 // (expert, thread), prefix-sum the expert-major count table, and let each
 // (expert, thread) write rows from its base with a running counter.  The
 // result is a stable counting sort of the pairs by expert.  Here the same
-// sort is done by blocks of 2,048 consecutive pairs:
-//   1. a histogram gives complete per-expert counts (or the route kernel
-//      produces them on the fly);
-//   2. one pass in which every block ranks its pairs within the block
-//      (warp match + per-warp running counts), publishes its per-expert
-//      aggregate, and takes the exclusive per-expert prefix of all earlier
-//      blocks by decoupled look-back (Merrill & Garland's single-pass scan,
-//      applied to an E-wide vector, with the predecessors' flags read 32 at
-//      a time so that the walk costs one round trip per 32 blocks).  Block
-//      order comes from an atomic ticket, so a block only ever waits for
-//      blocks that are already running, and every wait is bounded.
+// sort is done by chunks of 2,048 consecutive pairs:
+//   1. a table of per-chunk counts, hist[c][e]: the route kernel adds each
+//      pair it selects into it (the forward), or a histogram kernel writes
+//      one chunk's row per block (moe_dispatch_scan);
+//   2. one pass, one block per chunk: the block sums the table's columns --
+//      over every chunk for the expert totals (the counts, and the offsets
+//      by an exclusive scan), over the chunks before its own for its
+//      per-expert base -- ranks its pairs within the chunk (warp match +
+//      per-warp running counts) and writes every pair's row.
+// The table is complete before the pass starts, so no block ever waits for
+// another: the pass is one round of loads, a scan and the writes.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 
 constexpr int kWarps = kDispatchThreads / 32;
-constexpr int32_t kFlagAggregate = 1;
-constexpr int32_t kFlagInclusive = 2;
 
-size_t dispatch_clear_bytes(int64_t P) {
-  return sizeof(WsHeader) + align_up(static_cast<size_t>(dispatch_blocks(P)) * sizeof(int32_t));
-}
+int dispatch_hist_stride(int E) { return (E + 3) & ~3; }
 
-size_t dispatch_state_bytes(int64_t P, int E) {
-  const size_t nb = static_cast<size_t>(dispatch_blocks(P));
-  return align_up(nb * sizeof(int32_t)) + 2 * align_up(nb * static_cast<size_t>(E) * sizeof(int32_t));
-}
-
-DispatchState dispatch_state_at(void* base, int64_t P, int E) {
-  const size_t nb = static_cast<size_t>(dispatch_blocks(P));
-  char* p = static_cast<char*>(base);
-  DispatchState st;
-  st.flags = reinterpret_cast<int32_t*>(p);
-  p += align_up(nb * sizeof(int32_t));
-  st.agg = reinterpret_cast<int32_t*>(p);
-  p += align_up(nb * static_cast<size_t>(E) * sizeof(int32_t));
-  st.incl = reinterpret_cast<int32_t*>(p);
-  return st;
+size_t dispatch_hist_bytes(int64_t P, int E) {
+  return align_up(static_cast<size_t>(dispatch_blocks(P)) * dispatch_hist_stride(E) * sizeof(int32_t));
 }
 
 namespace {
 
-__device__ __forceinline__ int32_t load_acquire(const int32_t* p) {
-  int32_t v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void store_release(int32_t* p, int32_t v) {
-  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__global__ void __launch_bounds__(256) histogram_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
-                                                        int32_t* __restrict__ counts, int32_t* status) {
+// One chunk's row of the count table, written in full (zeros included), so
+// the table needs no clearing.
+__global__ void __launch_bounds__(kDispatchThreads)
+chunk_histogram_kernel(const int32_t* __restrict__ idx, int64_t P, int E, int E4, int32_t* __restrict__ hist,
+                       int32_t* status) {
   extern __shared__ int32_t s_hist[];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+  for (int e = threadIdx.x; e < E4; e += kDispatchThreads) s_hist[e] = 0;
   __syncthreads();
   bool bad = false;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < P; p += stride) {
-    const int e = __ldg(idx + p);
-    if (e >= 0 && e < E)
-      atomicAdd(&s_hist[e], 1);
-    else
-      bad = true;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kDispatchChunk;
+#pragma unroll
+  for (int r = 0; r < kDispatchPairsPerThread; ++r) {
+    const int64_t p = base + r * kDispatchThreads + threadIdx.x;
+    if (p < P) {
+      const int e = __ldg(idx + p);
+      if (e >= 0 && e < E)
+        atomicAdd(&s_hist[e], 1);
+      else
+        bad = true;
+    }
   }
   if (bad) record_status(status, kStatusBadIndex);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int c = s_hist[e];
-    if (c) atomicAdd(&counts[e], c);
-  }
+  int32_t* row = hist + static_cast<int64_t>(blockIdx.x) * E4;
+  for (int e = threadIdx.x; e < E4; e += kDispatchThreads) row[e] = s_hist[e];
 }
 
 // Exclusive scan of s_in[0..n) into s_out[0..n], s_out[n] = total, by one
@@ -119,32 +97,26 @@ __device__ void block_exclusive_scan(const int32_t* s_in, int32_t* s_out, int n,
   __syncthreads();
 }
 
+__device__ __forceinline__ int4 add4(int4 a, int4 b) { return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+
 __global__ void __launch_bounds__(kDispatchThreads)
-index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t P, int E, int k,
-             const int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ src_token,
-             int32_t* __restrict__ dest_row, float* __restrict__ row_w, WsHeader* hdr, int32_t* flags,
-             int32_t* agg, int32_t* incl) {
+index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t P, int E, int E4, int k,
+             const int32_t* __restrict__ hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+             int32_t* __restrict__ src_token, int32_t* __restrict__ dest_row, float* __restrict__ row_w,
+             int32_t* status) {
   extern __shared__ int32_t smem[];
-  int32_t* s_cnt = smem;                    // [E]
-  int32_t* s_off = s_cnt + E;               // [E+1]
+  int32_t* s_tot = smem;                    // [E4]: pairs per expert
+  int32_t* s_excl = s_tot + E4;             // [E4]: pairs of earlier chunks per expert
+  int32_t* s_off = s_excl + E4;             // [E+1]
   int32_t* s_warp = s_off + E + 1;          // [kWarps][E]: per-warp counts, then per-warp bases
-  int32_t* s_agg = s_warp + kWarps * E;     // [E]: this block's per-expert totals
-  int32_t* s_excl = s_agg + E;              // [E]: pairs of earlier blocks per expert
+  __shared__ int4 s_part[2][kDispatchThreads];  // column partial sums of each row group: totals, earlier chunks
   __shared__ int32_t s_tmp[kWarps];
-  __shared__ int32_t s_block;
-  __shared__ int32_t s_flag;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) s_block = atomicAdd(&hdr->ticket, 1);
-  for (int e = tid; e < E; e += kDispatchThreads) {
-    s_cnt[e] = __ldcg(counts + e);
-    s_excl[e] = 0;
-  }
-  for (int i = tid; i < kWarps * E; i += kDispatchThreads) s_warp[i] = 0;
-  __syncthreads();
-  const int64_t b = s_block;
-  // this thread's pairs and gates, all in flight before the scan below
-  const int64_t base = b * kDispatchChunk + static_cast<int64_t>(warp) * (32 * kDispatchPairsPerThread);
+  const int b = blockIdx.x;
+  const int nchunks = gridDim.x;
+  // this thread's pairs and gates, in flight before the column sums below
+  const int64_t base = static_cast<int64_t>(b) * kDispatchChunk + static_cast<int64_t>(warp) * (32 * kDispatchPairsPerThread);
   int my_e[kDispatchPairsPerThread];
   float my_w[kDispatchPairsPerThread];
 #pragma unroll
@@ -153,7 +125,40 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
     my_e[r] = (p < P) ? __ldcg(topk_idx + p) : -1;
     my_w[r] = (p < P && row_w) ? __ldcg(topk_w + p) : 0.0f;
   }
-  block_exclusive_scan(s_cnt, s_off, E, s_tmp);
+  for (int i = tid; i < kWarps * E; i += kDispatchThreads) s_warp[i] = 0;
+
+  // column sums of the count table, four experts per 16-byte load: thread
+  // (row group g, column quad q) walks rows g, g + G, ... with all its loads
+  // in flight, then the G row groups are added in shared memory
+  const int Q = E4 / 4;
+  const int G = kDispatchThreads / Q;  // >= 1: E4 <= 1024
+  const int q = tid % Q, g = tid / Q;
+  if (g < G) {
+    const int4* h4 = reinterpret_cast<const int4*>(hist);
+    int4 tot = make_int4(0, 0, 0, 0), ex = make_int4(0, 0, 0, 0);
+#pragma unroll 16
+    for (int r = g; r < nchunks; r += G) {
+      const int4 v = __ldcg(h4 + static_cast<int64_t>(r) * Q + q);
+      tot = add4(tot, v);
+      if (r < b) ex = add4(ex, v);
+    }
+    s_part[0][tid] = tot;
+    s_part[1][tid] = ex;
+  }
+  __syncthreads();
+  for (int qq = tid; qq < Q; qq += kDispatchThreads) {
+    int4 tot = s_part[0][qq], ex = s_part[1][qq];
+    for (int gg = 1; gg < G; ++gg) {
+      tot = add4(tot, s_part[0][gg * Q + qq]);
+      ex = add4(ex, s_part[1][gg * Q + qq]);
+    }
+    reinterpret_cast<int4*>(s_tot)[qq] = tot;
+    reinterpret_cast<int4*>(s_excl)[qq] = ex;
+  }
+  __syncthreads();
+  if (b == 0)
+    for (int e = tid; e < E; e += kDispatchThreads) counts[e] = s_tot[e];
+  block_exclusive_scan(s_tot, s_off, E, s_tmp);
   if (b == 0)
     for (int e = tid; e <= E; e += kDispatchThreads) offsets[e] = s_off[e];
 
@@ -178,10 +183,10 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
     my_e[r] = e;
     my_rank[r] = rank;
   }
-  if (bad) record_status(&hdr->status, kStatusBadIndex);
+  if (bad) record_status(status, kStatusBadIndex);
   __syncthreads();
 
-  // per-warp bases inside the block and the block's aggregate
+  // per-warp bases inside the chunk
   for (int e = tid; e < E; e += kDispatchThreads) {
     int32_t run = 0;
 #pragma unroll
@@ -190,79 +195,10 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
       s_warp[w * E + e] = run;
       run += c;
     }
-    s_agg[e] = run;
-    (b == 0 ? incl : agg)[b * E + e] = run;
   }
-  __threadfence();
   __syncthreads();
-  if (tid == 0) store_release(&flags[b], b == 0 ? kFlagInclusive : kFlagAggregate);
 
-  // decoupled look-back over the earlier blocks, a window of 32 at a time:
-  // warp 0 reads the flags of blocks hi, hi-1, ..., hi-31 at once and waits
-  // (bounded) until each has published at least its aggregate; the block
-  // then adds the vectors of the blocks from hi down to the nearest one that
-  // has published its inclusive prefix, or of the whole window, and goes on
-  // below it.  Block 0 publishes its inclusive prefix first, so the walk
-  // ends there at the latest.
-  if (b > 0) {
-    int64_t hi = b - 1;
-    for (;;) {
-      if (warp == 0) {
-        const int64_t c = hi - lane;
-        int32_t f = (c >= 0) ? load_acquire(flags + c) : kFlagAggregate;
-        if (__any_sync(0xffffffffu, f == 0)) {
-          const uint64_t t0 = global_timer_ns();
-          for (;;) {
-            __nanosleep(64);
-            if (f == 0) f = load_acquire(flags + c);
-            if (!__any_sync(0xffffffffu, f == 0)) break;
-            if (__any_sync(0xffffffffu, global_timer_ns() - t0 > kWaitLimitNs)) {
-              if (f == 0) f = -1;
-              break;
-            }
-          }
-        }
-        const unsigned inclusive = __ballot_sync(0xffffffffu, c >= 0 && f == kFlagInclusive);
-        const bool lost = __any_sync(0xffffffffu, f < 0);
-        // lane of the nearest inclusive block, 32 when the window has none
-        if (lane == 0) s_flag = lost ? -1 : (inclusive ? __ffs(inclusive) - 1 : 32);
-      }
-      __syncthreads();
-      const int32_t stop = s_flag;
-      if (stop < 0) {
-        if (tid == 0) record_status(&hdr->status, kStatusTimeout);
-        // this block's pairs get no row: -1 tells the permute and the
-        // combine to skip them (their rows in the expert groups stay unwritten)
-#pragma unroll
-        for (int r = 0; r < kDispatchPairsPerThread; ++r) {
-          const int64_t p = base + r * 32 + lane;
-          if (p < P) dest_row[p] = -1;
-        }
-        return;  // successors walk past this block on its aggregate
-      }
-      // every load of the window in flight at once: one L2 round trip
-      const int n_agg = min(stop, 32);
-      for (int e = tid; e < E; e += kDispatchThreads) {
-        int32_t part[33];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) part[i] = (i < n_agg) ? __ldcg(agg + (hi - i) * E + e) : 0;
-        part[32] = (stop < 32) ? __ldcg(incl + (hi - stop) * E + e) : 0;
-        int32_t acc = 0;
-#pragma unroll
-        for (int i = 0; i < 33; ++i) acc += part[i];
-        s_excl[e] += acc;
-      }
-      __syncthreads();  // s_flag is rewritten next round
-      if (stop < 32) break;
-      hi -= 32;
-    }
-    for (int e = tid; e < E; e += kDispatchThreads) incl[b * E + e] = s_excl[e] + s_agg[e];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) store_release(&flags[b], kFlagInclusive);
-  }
-
-  // rows: expert base + earlier blocks + earlier warps + rank within the warp
+  // rows: expert base + earlier chunks + earlier warps + rank within the warp
 #pragma unroll
   for (int r = 0; r < kDispatchPairsPerThread; ++r) {
     const int64_t p = base + r * 32 + lane;
@@ -281,29 +217,32 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
 
 }  // namespace
 
-cudaError_t launch_histogram(const int32_t* topk_idx, int64_t P, int E, int32_t* counts, int32_t* status,
-                             int num_sms, cudaStream_t stream) {
-  if (P == 0) return cudaSuccess;
-  const int64_t want = (P + 255) / 256;
-  const int grid = static_cast<int>(want < num_sms * 4 ? want : num_sms * 4);
-  histogram_kernel<<<grid, 256, E * sizeof(int32_t), stream>>>(topk_idx, P, E, counts, status);
+cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int64_t P, int E, int32_t* hist, int32_t* status,
+                                   cudaStream_t stream) {
+  const int64_t nb = dispatch_blocks(P);
+  if (nb == 0) return cudaSuccess;
+  const int E4 = dispatch_hist_stride(E);
+  chunk_histogram_kernel<<<static_cast<unsigned>(nb), kDispatchThreads, E4 * sizeof(int32_t), stream>>>(
+      topk_idx, P, E, E4, hist, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P, int E, int k,
-                         const int32_t* counts, int32_t* offsets, int32_t* src_token, int32_t* dest_row,
-                         float* row_w, void* header, DispatchState st, cudaStream_t stream) {
+cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P, int E, int k, const int32_t* hist,
+                         int32_t* counts, int32_t* offsets, int32_t* src_token, int32_t* dest_row, float* row_w,
+                         int32_t* status, cudaStream_t stream) {
   const int64_t nb = dispatch_blocks(P);
   if (nb == 0) return cudaSuccess;
-  const size_t smem = static_cast<size_t>(E + (E + 1) + kWarps * E + E + E) * sizeof(int32_t);
-  if (smem > 48 * 1024) {
+  const int E4 = dispatch_hist_stride(E);
+  const size_t smem = static_cast<size_t>(E4 + E4 + (E + 1) + kWarps * E) * sizeof(int32_t);
+  // the static arrays (column partial sums, scan scratch) count against the same 48 KB default
+  constexpr size_t kStaticSmem = 2 * kDispatchThreads * sizeof(int4) + kWarps * sizeof(int32_t);
+  if (smem + kStaticSmem > 48 * 1024) {
     cudaError_t err = cudaFuncSetAttribute(index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
   index_kernel<<<static_cast<unsigned>(nb), kDispatchThreads, smem, stream>>>(
-      topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, static_cast<WsHeader*>(header),
-      st.flags, st.agg, st.incl);
+      topk_idx, topk_w, P, E, E4, k, hist, counts, offsets, src_token, dest_row, row_w, status);
   return cudaGetLastError();
 }
 

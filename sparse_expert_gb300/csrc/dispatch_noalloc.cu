@@ -6,9 +6,9 @@
 // every device allocation and passes only the input and output tensors to
 // the enqueue call, and latency-critical loops that must not call
 // cudaMalloc (it can synchronise the device, and under memory pressure it
-// can fail in the middle of a run).  For them, the scratch of the look-back
-// pass (status word, block ticket, per-block flags and per-expert
-// aggregates) lives in a fixed device array compiled into the library.
+// can fail in the middle of a run).  For them, the scratch of the dispatch
+// pass (status word and the per-chunk count table) lives in a fixed device
+// array compiled into the library.
 //
 // The array is kStaticScratchBytes (4 MiB) per GPU and every GPU that loads
 // the library keeps it until the process exits.  All calls share it and it
@@ -20,9 +20,9 @@
 // before any stream capture.  The call itself allocates nothing: no
 // cudaMalloc, no cudaFree, no allocating library routine.
 //
-// Errors the kernels find (an expert index outside [0, E), a look-back wait
-// that ran out) land in the status word at the start of the array, which the
-// next call clears; moe_dispatch_noalloc_status reads it back.
+// Errors the kernels find (an expert index outside [0, E)) land in the
+// status word at the start of the array, which the next call clears;
+// moe_dispatch_noalloc_status reads it back.
 #include <mutex>
 #include <string>
 
@@ -80,8 +80,7 @@ extern "C" moe_status_t moe_dispatch_scan_noalloc(const int32_t* topk_idx, const
   if (T > 0 && (!topk_idx || !src_token || !dest_row)) return noalloc_fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (row_w && !topk_w) return noalloc_fail(MOE_ERR_INVALID_ARG, "row_w needs topk_w");
   const int64_t P = T * k;
-  const size_t clear = dispatch_clear_bytes(P);
-  const size_t need = clear + dispatch_state_bytes(P, E);
+  const size_t need = sizeof(WsHeader) + dispatch_hist_bytes(P, E);
   if (need > kStaticScratchBytes)
     return noalloc_fail(MOE_ERR_UNSUPPORTED,
                         "this problem needs " + std::to_string(need) + " bytes of scratch; the static scratch of "
@@ -96,23 +95,22 @@ extern "C" moe_status_t moe_dispatch_scan_noalloc(const int32_t* topk_idx, const
   if ((e = scratch_address(&ws)) != cudaSuccess)
     return noalloc_fail(MOE_ERR_CUDA, std::string("static scratch address: ") + cudaGetErrorName(e));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the header (status, ticket) and the look-back flags must start at zero
-  if ((e = cudaMemsetAsync(ws, 0, clear, st)) != cudaSuccess)
+  // the header (status word) must start at zero; the histogram kernel writes
+  // every row of the count table
+  if ((e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), st)) != cudaSuccess)
     return noalloc_fail(MOE_ERR_CUDA, std::string("scratch clear: ") + cudaGetErrorName(e));
-  if ((e = cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, st)) != cudaSuccess)
-    return noalloc_fail(MOE_ERR_CUDA, std::string("counts clear: ") + cudaGetErrorName(e));
   if (P == 0) {
-    if ((e = cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st)) != cudaSuccess)
-      return noalloc_fail(MOE_ERR_CUDA, std::string("offsets clear: ") + cudaGetErrorName(e));
+    if ((e = cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st)) != cudaSuccess)
+      return noalloc_fail(MOE_ERR_CUDA, std::string("counts/offsets clear: ") + cudaGetErrorName(e));
     return MOE_OK;
   }
   auto* hdr = static_cast<WsHeader*>(ws);
-  if ((e = launch_histogram(topk_idx, P, E, counts, &hdr->status, dev.num_sms, st)) != cudaSuccess)
+  auto* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(WsHeader));
+  if ((e = launch_chunk_histogram(topk_idx, P, E, hist, &hdr->status, st)) != cudaSuccess)
     return noalloc_fail(MOE_ERR_CUDA, std::string("histogram launch: ") + cudaGetErrorName(e));
-  DispatchState state = dispatch_state_at(static_cast<char*>(ws) + clear, P, E);
-  state.flags = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(WsHeader));
-  if ((e = launch_index(topk_idx, topk_w, P, E, k, counts, offsets, src_token, dest_row, row_w, ws, state, st)) !=
-      cudaSuccess)
+  if ((e = launch_index(topk_idx, topk_w, P, E, k, hist, counts, offsets, src_token, dest_row, row_w, &hdr->status,
+                        st)) != cudaSuccess)
     return noalloc_fail(MOE_ERR_CUDA, std::string("index launch: ") + cudaGetErrorName(e));
   return MOE_OK;
 }

@@ -78,32 +78,42 @@ constexpr int kBBytes = kHalfRows * BK * 2;          // one token part
 constexpr int kStageBytes = kABytes + 2 * kBBytes;   // A | B part 1 | B part 2
 constexpr int kEpiParts = 2;     // epilogue warps per TMEM lane quadrant, each a share of the token chunks
 constexpr int kEpiWarps = 4 * kEpiParts;
-constexpr int kHoldH = 4;       // gate/up epilogue: chunks of H a warp holds in registers across the hand-back
 constexpr int kTmemCols = 512;    // one accumulator: the tile's weight rows x up to 512 tokens
 constexpr int kEpiBytes = kEpiWarps * 32 * 64;   // per epilogue warp 2 KB: the staging of its stores
 constexpr int kRing = 4;                          // tile ids published ahead
 constexpr int kCodeBytes = kHalfRows * BK;        // FP8 codes of one CTA's weight rows and K block
 
-// Per-instantiation layout.  The FP8-weight form adds four converter warps
-// (one weight row per thread) and a code-producer warp, and a ring of code
-// stages (8 KB of 64-byte-swizzled codes and one scale record each) deep
-// enough to keep the halved weight stream's HBM latency hidden; it keeps
-// three MMA stages so that everything fits in 227 KB of shared memory.
+// Per-instantiation layout.  The bf16 form has one ring of stages, each
+// A | B part 1 | B part 2.  The FP8-weight form adds four converter warps
+// (a slice of a weight row per thread) and a code-producer warp, and splits
+// the ring: a ring of A slots that the converters fill (four deep, so a
+// slot is converted, fenced and signalled across the pair while the MMA
+// works through the three before it), a ring of token stages (B parts 1 and
+// 2, three deep) and a ring of code stages (8 KB of 64-byte-swizzled codes
+// and one scale record each), all within 227 KB of shared memory.
 template <bool kFp8>
 struct Cfg {
-  static constexpr int kStages = kFp8 ? 3 : 4;
+  static constexpr int kStages = kFp8 ? 3 : 4;                         // stages of the producer's ring
+  static constexpr int kSlotBytes = kFp8 ? 2 * kBBytes : kStageBytes;  // one stage of that ring
+  static constexpr int kAStages = kFp8 ? 4 : 0;                        // A slots the converters fill
+  // A slots per cluster-scope release of the peer's signaller: the release
+  // is the one serial step per stage that crosses the pair, so it covers two
+  // slots (K blocks come in pairs: the FP8 form needs K % 128 == 0)
+  static constexpr int kSigGroup = 2;
   static constexpr int kConvWarps = kFp8 ? 4 : 0;
   static constexpr int kCodeWarps = kFp8 ? 1 : 0;
-  static constexpr int kCodeStages = kFp8 ? 6 : 0;
+  static constexpr int kCodeStages = kFp8 ? 4 : 0;
   static constexpr int kCodeStageBytes = 9216;  // codes + a scale record, rounded to 1 KB
   static constexpr int kThreads = 64 + 32 * (kEpiWarps + kConvWarps + kCodeWarps);
   // readers of a ring slot, counted on the leader's rempty: the leader's MMA
-  // thread, the peer's producer, and both CTAs' epilogue, converter and
-  // code-producer warps
-  static constexpr int kRingReaders = 2 + 2 * (kEpiWarps + kConvWarps + kCodeWarps);
-  // row epilogue: chunks a warp holds in registers across the hand-back (the
-  // FP8 form has more warps, so fewer registers per thread)
-  static constexpr int kHold = kFp8 ? 4 : 6;
+  // thread, the peer's producer, both CTAs' epilogue, converter and
+  // code-producer warps, and with FP8 weights the peer's signaller
+  static constexpr int kRingReaders = 2 + 2 * (kEpiWarps + kConvWarps + kCodeWarps) + (kFp8 ? 1 : 0);
+  // chunks an epilogue warp holds in registers across the hand-back, row
+  // epilogue and gate/up epilogue (the FP8 form has more warps, so fewer
+  // registers per thread)
+  static constexpr int kHold = kFp8 ? (kConvWarps > 4 ? 2 : 4) : 6;
+  static constexpr int kHoldH = kFp8 && kConvWarps > 4 ? 2 : 4;
 };
 
 // What the epilogue makes of the accumulator (weight rows x token columns)
@@ -143,6 +153,9 @@ template <bool kFp8>
 struct SmemT {
   uint64_t full[Cfg<kFp8>::kStages], empty[Cfg<kFp8>::kStages];
   uint64_t cfull[kFp8 ? Cfg<kFp8>::kCodeStages : 1], cempty[kFp8 ? Cfg<kFp8>::kCodeStages : 1];
+  uint64_t converted[kFp8 ? Cfg<kFp8>::kAStages : 1];  // this CTA's converter warps have written an A slot
+  uint64_t apeer[kFp8 ? Cfg<kFp8>::kAStages : 1];      // leader: the peer's A slot is written (its signaller)
+  uint64_t aempty[kFp8 ? Cfg<kFp8>::kAStages : 1];     // the MMA is done with an A slot
   uint64_t tfull[2], tempty[2];
   uint64_t rfull[kRing], rempty[kRing];
   int32_t ring[kRing];
@@ -350,14 +363,17 @@ __device__ __forceinline__ float e4m3_times_2m120(uint32_t word, uint32_t sel) {
 // value x scale = (value 2^-120 x 2^112) x (scale x 2^8): both factors exact
 // and in the normal range, so the one fp32 rounding is that of value x
 // scale.
-__device__ __forceinline__ void convert_code_row(const uint8_t* crow, int s, const float* sc, uint8_t* arow) {
-  uint4 q[4];
+// NC of the row's four 16-value pieces, starting at piece c0.
+template <int NC>
+__device__ __forceinline__ void convert_code_row(const uint8_t* crow, int s, int c0, const float* sc, uint8_t* arow) {
+  uint4 q[NC];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) q[c] = *reinterpret_cast<const uint4*>(crow + ((c ^ ((s >> 1) & 3)) << 4));
+  for (int i = 0; i < NC; ++i) q[i] = *reinterpret_cast<const uint4*>(crow + (((c0 + i) ^ ((s >> 1) & 3)) << 4));
   const uint32_t sel[4] = {0x8044u, 0x9144u, 0xA244u, 0xB344u};
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint32_t w[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
+  for (int ci = 0; ci < NC; ++ci) {
+    const int c = c0 + ci;
+    const uint32_t w[4] = {q[ci].x, q[ci].y, q[ci].z, q[ci].w};
     float scl[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -391,8 +407,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
   constexpr int kStages = C::kStages;
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_stage0 = base;  // stage s at s_stage0 + s * kStageBytes: A | B part 1 | B part 2
-  uint8_t* s_code0 = s_stage0 + kStages * kStageBytes;  // FP8: code stage c at s_code0 + c * kCodeStageBytes
+  uint8_t* s_stage0 = base;  // stage s at s_stage0 + s * kSlotBytes: [A |] B part 1 | B part 2
+  uint8_t* s_a0 = s_stage0 + kStages * C::kSlotBytes;   // FP8: A slot a at s_a0 + a * kABytes
+  uint8_t* s_code0 = s_a0 + C::kAStages * kABytes;      // FP8: code stage c at s_code0 + c * kCodeStageBytes
   uint8_t* s_epi = s_code0 + C::kCodeStages * C::kCodeStageBytes;
   Smem* S = reinterpret_cast<Smem*>(s_epi + kEpiBytes);
   int32_t* s_off = reinterpret_cast<int32_t*>(S + 1);
@@ -429,14 +446,17 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     tmem_alloc_pair(&S->tmem_base, kTmemCols);
   } else if (warp == 2 && lane == 0) {
     for (int i = 0; i < kStages; ++i) {
-      // the leader's producer (bytes to come), and with FP8 weights every
-      // converter warp of both CTAs once its rows are in the A slot
-      mbar_init(&S->full[i], 1 + 2 * C::kConvWarps);
+      mbar_init(&S->full[i], 1);  // the leader's producer: the bytes to come
       mbar_init(&S->empty[i], 1);
     }
     for (int i = 0; i < C::kCodeStages; ++i) {
       mbar_init(&S->cfull[i], 1);
       mbar_init(&S->cempty[i], C::kConvWarps);
+    }
+    for (int i = 0; i < C::kAStages; ++i) {
+      mbar_init(&S->converted[i], C::kConvWarps);
+      mbar_init(&S->apeer[i], 1);
+      mbar_init(&S->aempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S->tfull[i], 1);
@@ -515,7 +535,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             break;
           }
           const uint32_t lead_full = leader_addr(&S->full[stage]);
-          uint8_t* st = s_stage0 + stage * kStageBytes;
+          uint8_t* st = s_stage0 + stage * C::kSlotBytes;
           if (rank == 0) mbar_arrive_expect_tx(&S->full[stage], bytes);
           if constexpr (kFp8) {
             // the code producer and the converters fill the A slot
@@ -532,8 +552,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           } else {
             tma_load_3d_pair(st, &tm_w, lead_full, 0, wrow, wblk + kb);
           }
-          tma_load_2d_pair(st + kABytes, &tm_x, lead_full, kb * BK, xrow1);
-          if (n2 > 0) tma_load_2d_pair(st + kABytes + kBBytes, &tm_x, lead_full, kb * BK, xrow2);
+          uint8_t* sb = st + (kFp8 ? 0 : kABytes);  // B part 1, then part 2
+          tma_load_2d_pair(sb, &tm_x, lead_full, kb * BK, xrow1);
+          if (n2 > 0) tma_load_2d_pair(sb + kBBytes, &tm_x, lead_full, kb * BK, xrow2);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -548,6 +569,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       const int num_kb = p.K / BK;
       int stage = 0;
       uint32_t phase = 0;
+      int astage = 0;  // FP8: A slot
+      uint32_t asphase = 0;
       uint32_t aphase = 0;
       const uint32_t idesc0 = umma_idesc_bf16_f32_major(2 * kHalfRows, 16, p.a_mn != 0, false) & ~(0x3Fu << 17);
       int rs = 0;
@@ -576,13 +599,17 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&S->full[stage], phase, abort_flag)) {
+          // FP8 weights: this CTA's A rows come with its converters'
+          // arrivals, the peer's with its signaller's cluster release
+          if (!mbar_wait(&S->full[stage], phase, abort_flag) ||
+              (kFp8 && (!mbar_wait(&S->converted[astage], asphase, abort_flag) ||
+                        (kb % C::kSigGroup == 0 && !wait_cluster(&S->apeer[astage], asphase, abort_flag))))) {
             failed = true;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a0 = smem_addr(s_stage0 + stage * kStageBytes);
-          const uint32_t b1 = a0 + kABytes;
+          const uint32_t a0 = kFp8 ? smem_addr(s_a0 + astage * kABytes) : smem_addr(s_stage0 + stage * kStageBytes);
+          const uint32_t b1 = kFp8 ? smem_addr(s_stage0 + stage * C::kSlotBytes) : a0 + kABytes;
           const uint32_t b2 = b1 + kBBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
@@ -599,24 +626,73 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             stage = 0;
             phase ^= 1u;
           }
+          if constexpr (kFp8) {
+            umma_commit_pair(&S->aempty[astage]);
+            if (++astage == C::kAStages) {
+              astage = 0;
+              asphase ^= 1u;
+            }
+          }
         }
         if (failed) break;
         umma_commit_pair(&S->tfull[0]);
         aphase ^= 1u;
       }
       umma_commit_pair(&S->drain);
+    } else if (kFp8 && rank == 1 && lane == 0) {
+      // ------------------------------------ FP8 signaller (peer CTA only)
+      // per group of A slots: once this CTA's converter warps have written
+      // their rows (their CTA-scope arrivals on `converted`), one
+      // cluster-scope release arrive on the leader's apeer barrier of the
+      // group's first slot makes the rows visible to the leader's MMA; the
+      // converters never wait on that release themselves
+      const int num_kb = p.K / BK;
+      int astage = 0;
+      uint32_t asphase = 0;
+      int rs = 0;
+      uint32_t rphase = 0;
+      for (;;) {
+        if (!wait_cluster(&S->rfull[rs], rphase, abort_flag)) {
+          failed = true;
+          break;
+        }
+        const int t = S->ring[rs];
+        arrive_remote(leader_addr(&S->rempty[rs]));
+        if (++rs == kRing) {
+          rs = 0;
+          rphase ^= 1u;
+        }
+        if (t < 0) break;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&S->converted[astage], asphase, abort_flag)) {
+            failed = true;
+            break;
+          }
+          // one release for the group's slots, on the group's first slot
+          if (kb % C::kSigGroup == C::kSigGroup - 1)
+            arrive_remote(leader_addr(&S->apeer[astage - (C::kSigGroup - 1)]));
+          if (++astage == C::kAStages) {
+            astage = 0;
+            asphase ^= 1u;
+          }
+        }
+        if (failed) break;
+      }
     }
   } else if (kFp8 && warp >= 2 + kEpiWarps && warp < 2 + kEpiWarps + C::kConvWarps) {
     // ------------------------------------------------ FP8 code converters
-    // thread = one of this CTA's 128 weight rows, per K block: its codes and
-    // the block's scales from the code stage to bf16 in the MMA stage's A
-    // slot, then a release arrive on the leader's stage barrier
-    const int row = (warp - 2 - kEpiWarps) * 32 + lane;
+    // thread = a slice of one of this CTA's 128 weight rows, per K block: its
+    // codes and the block's scales from the code stage to bf16 in the MMA
+    // stage's A slot, then a CTA-scope arrive on `converted`
+    constexpr int kPieces = 16 / (kFp8 ? C::kConvWarps : 4);  // 16-value pieces per thread
+    const int ci = (warp - 2 - kEpiWarps) * 32 + lane;
+    const int row = ci % kHalfRows;
+    const int piece0 = (ci / kHalfRows) * kPieces;
     // gate/up rows come in quarter order: 16 gate rows, then 16 up rows
     const int half = (kMode == kModeSwiGLU) ? ((row >> 4) & 1) : 0;
     const int num_kb = p.K / BK;
-    int stage = 0, cstage = 0;
-    uint32_t phase = 0, cphase = 0;
+    int astage = 0, cstage = 0;
+    uint32_t asphase = 0, cphase = 0;
     int rs = 0;
     uint32_t rphase = 0;
     const uint32_t lead_rempty0 = leader_addr(&S->rempty[0]);
@@ -636,23 +712,24 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       for (int kb = 0; kb < num_kb; ++kb) {
         // the codes have landed, and the MMA is done with the A slot
         if (!mbar_wait_warp(&S->cfull[cstage], cphase, abort_flag) ||
-            !mbar_wait_warp(&S->empty[stage], phase ^ 1u, abort_flag)) {
+            !mbar_wait_warp(&S->aempty[astage], asphase ^ 1u, abort_flag)) {
           failed = true;
           break;
         }
         const uint8_t* cs = s_code0 + cstage * C::kCodeStageBytes;
-        convert_code_row(cs + row * BK, row, reinterpret_cast<const float*>(cs + kCodeBytes) + half * 68,
-                         s_stage0 + stage * kStageBytes + row * (BK * 2));
+        convert_code_row<kPieces>(cs + row * BK, row, piece0,
+                                  reinterpret_cast<const float*>(cs + kCodeBytes) + half * 68,
+                                  s_a0 + astage * kABytes + row * (BK * 2));
         // the generic-proxy stores become visible to the tensor cores' reads
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          arrive_remote(leader_addr(&S->full[stage]));
+          mbar_arrive(&S->converted[astage]);  // CTA scope: the leader's MMA thread or the peer's signaller
           mbar_arrive(&S->cempty[cstage]);
         }
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        if (++astage == C::kAStages) {
+          astage = 0;
+          asphase ^= 1u;
         }
         if (++cstage == C::kCodeStages) {
           cstage = 0;
@@ -799,7 +876,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         // as in the row epilogue, the warp's last kHoldH chunks of H stay in
         // registers until the accumulator has been handed back
         const int n_chunks = c_begin < c_end ? (c_end - c_begin + 31) >> 5 : 0;
-        const int n_stream = max(n_chunks - kHoldH, 0);
+        const int n_stream = max(n_chunks - C::kHoldH, 0);
 #pragma unroll 1
         for (int i = 0; i < n_stream; ++i) {
           const int c = c_begin + 32 * i;
@@ -809,9 +886,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           rows16f_to_global(tbuf, lane, hcol + static_cast<int64_t>(c) * p.out_cols, p.out_cols, x.valid - c);
           tmem_ld_wait();
         }
-        uint32_t held[kHoldH][8];
+        uint32_t held[C::kHoldH][8];
 #pragma unroll
-        for (int hh = 0; hh < kHoldH; ++hh) {
+        for (int hh = 0; hh < C::kHoldH; ++hh) {
           const int c = c_begin + 32 * (n_stream + hh);
           if (c < c_end) {
             if (c + 32 >= c_end) release();
@@ -820,7 +897,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           }
         }
 #pragma unroll
-        for (int hh = 0; hh < kHoldH; ++hh) {
+        for (int hh = 0; hh < C::kHoldH; ++hh) {
           const int c = c_begin + 32 * (n_stream + hh);
           if (c < c_end) {
             stage_rows_16f(held[hh], tbuf, lane);
@@ -992,7 +1069,8 @@ namespace {
 
 template <bool kFp8>
 constexpr size_t smem_bytes(int E) {
-  return 1024 + static_cast<size_t>(Cfg<kFp8>::kStages) * kStageBytes +
+  return 1024 + static_cast<size_t>(Cfg<kFp8>::kStages) * Cfg<kFp8>::kSlotBytes +
+         static_cast<size_t>(Cfg<kFp8>::kAStages) * kABytes +
          static_cast<size_t>(Cfg<kFp8>::kCodeStages) * Cfg<kFp8>::kCodeStageBytes + kEpiBytes +
          sizeof(SmemT<kFp8>) + 2 * static_cast<size_t>(E + 1) * sizeof(int32_t);
 }
@@ -1000,6 +1078,8 @@ constexpr size_t smem_bytes(int E) {
 // the largest expert count the library takes still fits the opt-in 227 KB
 static_assert(smem_bytes<false>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory of the paired GEMM");
 static_assert(smem_bytes<true>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory of the FP8-weight paired GEMM");
+static_assert(Cfg<true>::kAStages % Cfg<true>::kSigGroup == 0 && (128 / BK) % Cfg<true>::kSigGroup == 0,
+              "signal groups align with the A ring and with K blocks of a K % 128 == 0 problem");
 
 template <bool kFp8>
 cudaError_t launch_pairs(const CUtensorMap& mw, const CUtensorMap& mx, const Params& prm, int64_t P, int num_sms,

@@ -14,16 +14,16 @@ namespace moe {
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
-// ---- stage 1
+// ---- stage 1 (hist: the per-chunk count table of stages 2-3, or null)
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int n_groups, int renormalize,
-                              int32_t* topk_idx, float* topk_w, int32_t* counts, int num_sms, cudaStream_t stream);
+                              int32_t* topk_idx, float* topk_w, int32_t* hist, int num_sms, cudaStream_t stream);
 
 // ---- stage 1 with the router linear layer fused
 int router_e_pad(int E);  // E rounded up to a multiple of 128
 size_t router_smem_bytes(int E);
 cudaError_t launch_pack_router(const void* w_router, int d, int E, void* packed, cudaStream_t stream);
 cudaError_t launch_router_topk(const void* x, const void* w_packed, int64_t T, int d, int E, int k, int renormalize,
-                               int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* status,
+                               int32_t* topk_idx, float* topk_w, int32_t* hist, int32_t* status,
                                cudaStream_t stream);
 
 // ---- backward of stage 5 and of the routing
@@ -58,21 +58,20 @@ constexpr int kDispatchChunk = kDispatchThreads * kDispatchPairsPerThread;  // p
 
 inline int64_t dispatch_blocks(int64_t P) { return (P + kDispatchChunk - 1) / kDispatchChunk; }
 
-// Look-back state inside a workspace, after the 256-byte header.
-struct DispatchState {
-  int32_t* flags;  // [NB], cleared with the header
-  int32_t* agg;    // [NB, E]
-  int32_t* incl;   // [NB, E]
-};
-size_t dispatch_state_bytes(int64_t P, int E);            // flags + agg + incl, aligned
-size_t dispatch_clear_bytes(int64_t P);                   // header + flags
-DispatchState dispatch_state_at(void* base, int64_t P, int E);  // base = just after the header
+// The per-chunk count table: hist[c][e] = pairs of chunk c (pairs
+// 2048c .. 2048c + 2047) routed to expert e, int32, rows of
+// dispatch_hist_stride(E) (E rounded up to 4) entries.
+int dispatch_hist_stride(int E);
+size_t dispatch_hist_bytes(int64_t P, int E);  // 256-byte aligned
 
-cudaError_t launch_histogram(const int32_t* topk_idx, int64_t P, int E, int32_t* counts, int32_t* status,
-                             int num_sms, cudaStream_t stream);
-cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P, int E, int k,
-                         const int32_t* counts, int32_t* offsets, int32_t* src_token, int32_t* dest_row,
-                         float* row_w, void* header, DispatchState st, cudaStream_t stream);
+// Writes every row of the table from topk_idx (no clearing needed).
+cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int64_t P, int E, int32_t* hist, int32_t* status,
+                                   cudaStream_t stream);
+// counts, offsets, dest_row, src_token and row_w (optional) from topk_idx and
+// the complete table, one block per chunk and no block waiting on another.
+cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P, int E, int k, const int32_t* hist,
+                         int32_t* counts, int32_t* offsets, int32_t* src_token, int32_t* dest_row, float* row_w,
+                         int32_t* status, cudaStream_t stream);
 
 // ---- stage 4 data movement and stage 5
 // A dest_row entry outside [0, T*k) is skipped (no copy; no term of the sum)

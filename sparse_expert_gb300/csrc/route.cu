@@ -1,8 +1,9 @@
 // Stage 1 of the layer: Softmax and TopK of the router logits, one warp per
 // token ("Scalable Pretraining of Large MoE LMs on Aurora Super Computer",
-// §3.1, Algorithm 1, stage 1).  Optionally adds each selection to a
-// per-expert histogram (the token counts of stage 2) so that the index pass
-// can start from complete counts without another read of the indices.
+// §3.1, Algorithm 1, stage 1).  Optionally adds each selection to the
+// per-chunk count table of stage 2 (one atomic add per pair into
+// hist[pair / 2048][expert]) so that the index pass starts from complete
+// counts without another read of the indices.
 #include "common.cuh"
 #include "internal.h"
 
@@ -14,11 +15,14 @@ constexpr int kRouteWarps = 8;  // tokens per block
 // (logit, expert) as one 64-bit key whose unsigned order is the selection
 // order: larger logit first, then the smaller expert index.  The high word
 // is the float's bits made monotone (negative values inverted, sign bit set
-// on the others) after folding -0.0 onto +0.0; the low word decreases with
-// the expert index.  Key 0 is below every finite logit's key.
+// on the others) after folding -0.0 onto +0.0 (x + 0.0f: -0.0 + 0.0 is +0.0
+// under round to nearest, and every other finite x is unchanged); the low
+// word decreases with the expert index.  Key 0 is below every finite
+// logit's key.
 __device__ __forceinline__ uint32_t route_hi(float x) {
-  const uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(__fadd_rn(x, 0.0f));
+  const uint32_t neg = static_cast<uint32_t>(static_cast<int32_t>(u) >> 31);  // all ones when negative
+  return u ^ (neg | 0x80000000u);
 }
 
 __device__ __forceinline__ uint64_t route_key_hi(uint32_t hi, int e) {
@@ -92,14 +96,16 @@ __device__ __forceinline__ uint64_t topk_rounds(const float (&v)[NV], int E, int
   return mine;
 }
 
-// NV logits per lane: lane l holds experts l, l+32, ..., l+32*(NV-1).
+// NV logits per lane: lane l holds experts l, l+32, ..., l+32*(NV-1); with
+// kFull every lane holds exactly NV (E = 32 NV) and no index is tested.
 //
 // Without groups the selection first narrows the field.  Let H be the k-th
-// largest of the 32 lanes' maximum high words (the logit part of the key).
-// At least k lanes hold a logit whose high word is >= H, so the k-th
-// largest key has a high word >= H and every selected expert is among the
-// candidates with high word >= H.  (If H is the 0 of a lane without
-// experts, every expert is a candidate.)  For N(0,1) logits over 384
+// largest of the 32 lanes' maximum high words (the logit part of the key),
+// or, for k <= 16, the k-th largest of the 16 maxima of lane pairs (l,
+// l + 16).  Either way at least k distinct experts have a high word >= H, so
+// the k-th largest key has a high word >= H and every selected expert is
+// among the candidates with high word >= H.  (If H is the 0 of a lane
+// without experts, every expert is a candidate.)  For N(0,1) logits over 384
 // experts there are about nine candidates; when they number at most 32 the
 // warp gathers their full keys into one lane each and a bitonic sort of
 // the smallest width that holds them puts the k winners in lanes 0..k-1.
@@ -111,18 +117,13 @@ __device__ __forceinline__ uint64_t topk_rounds(const float (&v)[NV], int E, int
 // infrastructure", Group-limited expert routing), group g = experts
 // [g*E/G, (g+1)*E/G) gets k/G rounds restricted to its own experts, and a
 // warp sort puts the k winners back in descending slot order.
-template <int NV>
+template <int NV, bool kFull>
 __global__ void __launch_bounds__(kRouteWarps * 32, NV <= 12 ? 4 : NV <= 16 ? 2 : 1)
 route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int n_groups, int renormalize,
-                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts) {
-  extern __shared__ int32_t s_hist[];  // [E] when counts != nullptr
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ hist, int E4) {
   __shared__ uint64_t s_cand[kRouteWarps * 32];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  if (counts) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
-    __syncthreads();
-  }
   uint64_t* cand = s_cand + warp * 32;
 
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kRouteWarps;
@@ -132,7 +133,7 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (e < E) ? __ldg(row + e) : 0.0f;
+      v[i] = (kFull || e < E) ? __ldg(row + e) : 0.0f;
     }
     uint64_t mine = 0, first = 0;
     if (n_groups == 1) {
@@ -141,12 +142,18 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         hw[i] = route_hi(v[i]);
-        if (lane + 32 * i < E) hm = max(hm, hw[i]);
+        if (kFull || lane + 32 * i < E) hm = max(hm, hw[i]);
       }
-      const uint32_t H = __shfl_sync(0xffffffffu, warp_sort_desc<32>(hm, lane), k - 1);
+      uint32_t H;
+      if (k <= 16) {
+        const uint32_t hp = max(hm, __shfl_xor_sync(0xffffffffu, hm, 16));
+        H = __shfl_sync(0xffffffffu, warp_sort_desc<16>(hp, lane), k - 1);
+      } else {
+        H = __shfl_sync(0xffffffffu, warp_sort_desc<32>(hm, lane), k - 1);
+      }
       uint32_t cnt = 0;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) cnt += (lane + 32 * i < E && hw[i] >= H) ? 1u : 0u;
+      for (int i = 0; i < NV; ++i) cnt += ((kFull || lane + 32 * i < E) && hw[i] >= H) ? 1u : 0u;
       uint32_t incl = cnt;
 #pragma unroll
       for (int s = 1; s < 32; s <<= 1) {
@@ -159,7 +166,7 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
           const int e = lane + 32 * i;
-          if (e < E && hw[i] >= H) cand[pos++] = route_key_hi(hw[i], e);
+          if ((kFull || e < E) && hw[i] >= H) cand[pos++] = route_key_hi(hw[i], e);
         }
         __syncwarp();
         uint64_t c = (static_cast<uint32_t>(lane) < C) ? cand[lane] : 0ull;
@@ -218,17 +225,10 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
     denom = __shfl_sync(0xffffffffu, denom, 0);  // one rounding for every slot
     if (lane < k) {
       const int e = key_expert(mine);
-      topk_idx[t * k + lane] = e;
-      topk_w[t * k + lane] = z / denom;
-      if (counts) atomicAdd(&s_hist[e], 1);
-    }
-  }
-
-  if (counts) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      const int c = s_hist[e];
-      if (c) atomicAdd(&counts[e], c);
+      const int64_t p = t * k + lane;
+      topk_idx[p] = e;
+      topk_w[p] = z / denom;
+      if (hist) atomicAdd(hist + (p / kDispatchChunk) * E4 + e, 1);
     }
   }
 }
@@ -236,16 +236,20 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int n_groups, int renormalize,
-                              int32_t* topk_idx, float* topk_w, int32_t* counts, int num_sms, cudaStream_t stream) {
+                              int32_t* topk_idx, float* topk_w, int32_t* hist, int num_sms, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int64_t blocks_needed = (T + kRouteWarps - 1) / kRouteWarps;
   const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
   const int grid = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
-  const size_t smem = counts ? static_cast<size_t>(E) * sizeof(int32_t) : 0;
+  const int E4 = dispatch_hist_stride(E);
   const int nv = (E + 31) / 32;
-#define MOE_ROUTE_CASE(NV)                                                                                     \
-  route_topk_kernel<NV><<<grid, kRouteWarps * 32, smem, stream>>>(logits, T, E, k, n_groups, renormalize, topk_idx, \
-                                                                  topk_w, counts);                             \
+#define MOE_ROUTE_CASE(NV)                                                                                    \
+  if (E == 32 * (NV))                                                                                           \
+    route_topk_kernel<NV, true><<<grid, kRouteWarps * 32, 0, stream>>>(logits, T, E, k, n_groups, renormalize,  \
+                                                                       topk_idx, topk_w, hist, E4);             \
+  else                                                                                                          \
+    route_topk_kernel<NV, false><<<grid, kRouteWarps * 32, 0, stream>>>(logits, T, E, k, n_groups, renormalize, \
+                                                                        topk_idx, topk_w, hist, E4);            \
   break;
   switch (nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : nv <= 12 ? 12 : nv <= 16 ? 16 : 32) {
     case 1: MOE_ROUTE_CASE(1)

@@ -36,7 +36,8 @@ struct RouterParams {
   int E, E_pad, K, k, renormalize;
   int32_t* topk_idx;
   float* topk_w;
-  int32_t* counts;
+  int32_t* hist;   // per-chunk count table [pairs / 2048][E4], or null
+  int E4;
   int32_t* status;
 };
 
@@ -64,7 +65,6 @@ router_topk_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
   __shared__ uint64_t full[8], empty[8], tfull;
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag_s;
-  int32_t* s_hist = reinterpret_cast<int32_t*>(base + stages * stage_bytes);  // [E] with counts
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &abort_flag_s;
@@ -84,8 +84,6 @@ router_topk_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     abort_flag_s = 0;
     fence_barrier_init();
   }
-  if (p.counts)
-    for (int e = threadIdx.x; e < p.E; e += kThreads) s_hist[e] = 0;
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -222,9 +220,10 @@ router_topk_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         for (int j = 0; j < KMAX; ++j) {
           if (j < p.k) {
             const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best[j]));
-            p.topk_idx[t * p.k + j] = e;
-            p.topk_w[t * p.k + j] = expf(key_logit(best[j]) - mx) / denom;
-            if (p.counts) atomicAdd(&s_hist[e], 1);
+            const int64_t pr = t * p.k + j;
+            p.topk_idx[pr] = e;
+            p.topk_w[pr] = expf(key_logit(best[j]) - mx) / denom;
+            if (p.hist) atomicAdd(p.hist + (pr / kDispatchChunk) * p.E4 + e, 1);
           }
         }
       }
@@ -234,11 +233,6 @@ router_topk_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (p.counts)
-    for (int e = threadIdx.x; e < p.E; e += kThreads) {
-      const int c = s_hist[e];
-      if (c) atomicAdd(&p.counts[e], c);
-    }
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem_base, tmem_cols);
@@ -277,7 +271,7 @@ size_t router_smem_bytes(int E) {
 }
 
 cudaError_t launch_router_topk(const void* x, const void* w_packed, int64_t T, int d, int E, int k, int renormalize,
-                               int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* status,
+                               int32_t* topk_idx, float* topk_w, int32_t* hist, int32_t* status,
                                cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int e_pad = router_e_pad(E);
@@ -294,7 +288,8 @@ cudaError_t launch_router_topk(const void* x, const void* w_packed, int64_t T, i
   prm.renormalize = renormalize;
   prm.topk_idx = topk_idx;
   prm.topk_w = topk_w;
-  prm.counts = counts;
+  prm.hist = hist;
+  prm.E4 = dispatch_hist_stride(E);
   prm.status = status;
   const size_t smem = router_smem_bytes(E);
   const unsigned grid = static_cast<unsigned>((T + BM - 1) / BM);

@@ -31,9 +31,9 @@ def test_noalloc_dispatch_matches_workspace_dispatch_on_consecutive_calls():
     import sparse_expert_gb300 as moe
 
     cases = [
-        _routing("t1", 0),                                                  # 131,072 pairs: 64 look-back blocks
+        _routing("t1", 0),                                                  # 131,072 pairs: 64 chunks
         _routing(workloads.custom("few", T=300, d=64, E=8, k=2, f=64), 1),  # smaller call right after
-        _routing(workloads.custom("wide", T=20000, d=64, E=384, k=8, f=64), 5),  # 79 blocks: a wider cleared region
+        _routing(workloads.custom("wide", T=20000, d=64, E=384, k=8, f=64), 5),  # 79 chunks: a wider count table
         _routing("skew", 2),                                                # many empty experts
         _routing(workloads.custom("few2", T=77, d=64, E=16, k=3, f=64), 6),  # a small call after the wide ones
     ]
@@ -87,7 +87,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     from sparse_expert_gb300._lib import lib
 
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check fails first
-    status = lib.moe_dispatch_scan_noalloc(fake, fake, 400000, 384, 8, fake, fake, fake, fake, fake, None)
+    status = lib.moe_dispatch_scan_noalloc(fake, fake, 800000, 384, 8, fake, fake, fake, fake, fake, None)
     assert status == 2  # MOE_ERR_UNSUPPORTED
     msg = lib.moe_last_error().decode()
     assert "static scratch" in msg and str(4 << 20) in msg
