@@ -1,8 +1,9 @@
 """Row indices outside [0, T*k) never become addresses.
 
 The dispatch pass writes dest_row = -1 for a pair it cannot place (an
-expert index outside [0, E)), and a caller may pass anything.  moe_permute, moe_combine and moe_combine_backward must
-then skip that pair and touch no memory outside their buffers.  Each buffer
+expert index outside [0, E)), and a caller may pass anything.  moe_permute,
+moe_combine and moe_combine_backward must then skip that pair and touch no
+memory outside their buffers.  Each buffer
 here is a view into a larger allocation with one guard row on each side, so
 a missing check would land in the guard rows (inside the allocation) rather
 than fault; the guards are filled with a sentinel, or NaN where a read would
