@@ -287,7 +287,7 @@ MOE_API moe_status_t moe_dequantize_fp8_blockwise(const uint8_t* codes, const fl
  *           holds gate features 64t .. 64t+63 and the same up features,
  *           16 gate rows then their 16 up rows, down tile t output features
  *           128t .. 128t+127), then per (expert, 128-feature block, K block)
- *           a record of that block's 64 scales of each projection, times 2^8.
+ *           a record of that block's 64 scales of each projection.
  * moe_forward_fp8 is moe_forward with those weights: each GEMM stage's codes
  * are dequantised in shared memory to bf16(E4M3 value x scale), the product
  * rounded once in fp32 -- exactly what moe_dequantize_fp8_blockwise gives --

@@ -107,8 +107,7 @@ __global__ void __launch_bounds__(256) pack_codes_kernel(const uint8_t* __restri
 // Scales of one projection (one fp32 per 128 consecutive stored values, so
 // per (expert, K row, 128-feature block)) to one record per (expert,
 // feature block, K block): gate/up 136 floats (64 gate scales, 4 zeros, 64 up
-// scales, 4 zeros), down 64.  Each scale is stored times 2^8 (exact for
-// every finite fp32 scale of a bf16 block: amax / 448 < 2^120).
+// scales, 4 zeros), down 64.  The scales are stored as they are.
 __global__ void __launch_bounds__(256) pack_scales_kernel(const float* __restrict__ gate_or_down,
                                                           const float* __restrict__ up, float* __restrict__ dst,
                                                           int E, int K, int C, int gate_up) {
@@ -128,7 +127,7 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const float* __restric
       src = up;
       kk = j - 68;
     }
-    if (kk < 64) v = __ldg(src + (e * K + kb * 64 + kk) * nfb + fb) * 256.0f;  // exact: a power of two
+    if (kk < 64) v = __ldg(src + (e * K + kb * 64 + kk) * nfb + fb);
     dst[i] = v;
   }
 }

@@ -340,59 +340,71 @@ __device__ __forceinline__ void pack_chunk(const uint32_t (&a)[16], const uint32
   }
 }
 
-// FP8 weights: the fp32 whose bits are byte `sel` picks of `word` (an E4M3
-// code) moved so that its sign is bit 31 and its other seven bits are bits
-// 26..20.  That float is the code's value times 2^-120 exactly: the four
-// exponent bits land in the fp32 exponent with a bias 120 lower, normal
-// codes on normal floats and the subnormal codes (exponent 0) on fp32
-// subnormals of the same significand.  sel = byte b into byte 2, its sign
-// replicated into byte 3, zeros below (prmt selector ((8|b) << 12) | (b << 8)
-// | 0x44).
-__device__ __forceinline__ float e4m3_times_2m120(uint32_t word, uint32_t sel) {
-  uint32_t x;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(x) : "r"(word), "r"(0u), "r"(sel));
-  return __uint_as_float((x << 4) & 0x87F00000u);
+// FP8 weights: the four E4M3 codes of `word` (byte i = code i) as exact
+// fp32 values.  The hardware conversion of a code pair to f16 is exact
+// (every E4M3 value, subnormals included, is an f16 value; the encoder
+// never writes the NaN codes), and so is the widening of f16 to fp32.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t word, float (&v)[4]) {
+  uint32_t h01, h23;
+  asm("{.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(word));
+  asm("{.reg .f16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.f32.f16 %0, a;\n\t"
+      "cvt.f32.f16 %1, b;}"
+      : "=f"(v[0]), "=f"(v[1])
+      : "r"(h01));
+  asm("{.reg .f16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.f32.f16 %0, a;\n\t"
+      "cvt.f32.f16 %1, b;}"
+      : "=f"(v[2]), "=f"(v[3])
+      : "r"(h23));
 }
 
 // One weight row of one K block: its 64 E4M3 codes (a 64-byte row of a tile
 // loaded with 64-byte swizzling: piece c of row s at c ^ ((s >> 1) & 3)) and
-// the K block's 64 scales stored times 2^8 become bf16(value x scale), the
-// product rounded once in fp32 and then to bf16 -- the dequantisation of the
-// "FP8 expert weight all-gather", bit for bit -- written as the row's 128
-// bytes of the 128-byte-swizzled K-major A operand (piece j at j ^ (s & 7)).
-// value x scale = (value 2^-120 x 2^112) x (scale x 2^8): both factors exact
-// and in the normal range, so the one fp32 rounding is that of value x
-// scale.
-// NC of the row's four 16-value pieces, starting at piece c0.
+// the K block's 64 scales become bf16(value x scale), the product of the
+// exact code value and the fp32 scale rounded once in fp32 and then to bf16
+// -- the dequantisation of the "FP8 expert weight all-gather", bit for bit.
+// NC of the row's four 16-value pieces, starting at piece c0, into
+// registers (o[ci] = piece c0 + ci as 16 bf16), so that the conversion runs
+// before the A slot it goes to is free.
 template <int NC>
-__device__ __forceinline__ void convert_code_row(const uint8_t* crow, int s, int c0, const float* sc, uint8_t* arow) {
+__device__ __forceinline__ void convert_code_row(const uint8_t* crow, int s, int c0, const float* sc,
+                                                 uint32_t (&o)[NC][8]) {
   uint4 q[NC];
 #pragma unroll
   for (int i = 0; i < NC; ++i) q[i] = *reinterpret_cast<const uint4*>(crow + (((c0 + i) ^ ((s >> 1) & 3)) << 4));
-  const uint32_t sel[4] = {0x8044u, 0x9144u, 0xA244u, 0xB344u};
 #pragma unroll
   for (int ci = 0; ci < NC; ++ci) {
     const int c = c0 + ci;
     const uint32_t w[4] = {q[ci].x, q[ci].y, q[ci].z, q[ci].w};
-    float scl[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float4 v = *reinterpret_cast<const float4*>(sc + 16 * c + 4 * i);
-      scl[4 * i] = v.x;
-      scl[4 * i + 1] = v.y;
-      scl[4 * i + 2] = v.z;
-      scl[4 * i + 3] = v.w;
+      const float4 scl = *reinterpret_cast<const float4*>(sc + 16 * c + 4 * i);
+      float v[4];
+      e4m3x4_to_f32(w[i], v);
+      o[ci][2 * i] = pack_bf16x2(__fmul_rn(v[0], scl.x), __fmul_rn(v[1], scl.y));
+      o[ci][2 * i + 1] = pack_bf16x2(__fmul_rn(v[2], scl.z), __fmul_rn(v[3], scl.w));
     }
-    uint32_t o[8];
+  }
+}
+
+// The converted pieces as the row's bytes of the 128-byte-swizzled K-major
+// A operand (16-byte piece j of row s at j ^ (s & 7)).
+template <int NC>
+__device__ __forceinline__ void store_a_row(const uint32_t (&o)[NC][8], int s, int c0, uint8_t* arow) {
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int i0 = 2 * m, i1 = 2 * m + 1;
-      const float p0 = __fmul_rn(__fmul_rn(e4m3_times_2m120(w[i0 >> 2], sel[i0 & 3]), 0x1p112f), scl[i0]);
-      const float p1 = __fmul_rn(__fmul_rn(e4m3_times_2m120(w[i1 >> 2], sel[i1 & 3]), 0x1p112f), scl[i1]);
-      o[m] = pack_bf16x2(p0, p1);
-    }
-    *reinterpret_cast<uint4*>(arow + (((2 * c) ^ (s & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4*>(arow + (((2 * c + 1) ^ (s & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  for (int ci = 0; ci < NC; ++ci) {
+    const int c = c0 + ci;
+    *reinterpret_cast<uint4*>(arow + (((2 * c) ^ (s & 7)) << 4)) = make_uint4(o[ci][0], o[ci][1], o[ci][2], o[ci][3]);
+    *reinterpret_cast<uint4*>(arow + (((2 * c + 1) ^ (s & 7)) << 4)) =
+        make_uint4(o[ci][4], o[ci][5], o[ci][6], o[ci][7]);
   }
 }
 
@@ -710,23 +722,28 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       }
       if (t < 0) break;
       for (int kb = 0; kb < num_kb; ++kb) {
-        // the codes have landed, and the MMA is done with the A slot
-        if (!mbar_wait_warp(&S->cfull[cstage], cphase, abort_flag) ||
-            !mbar_wait_warp(&S->aempty[astage], asphase ^ 1u, abort_flag)) {
+        // the codes have landed: convert them into registers and free the
+        // code stage, then wait until the MMA is done with the A slot, so
+        // that only the stores, the fence and the arrive follow that wait
+        if (!mbar_wait_warp(&S->cfull[cstage], cphase, abort_flag)) {
           failed = true;
           break;
         }
         const uint8_t* cs = s_code0 + cstage * C::kCodeStageBytes;
+        uint32_t o[kPieces][8];
         convert_code_row<kPieces>(cs + row * BK, row, piece0,
-                                  reinterpret_cast<const float*>(cs + kCodeBytes) + half * 68,
-                                  s_a0 + astage * kABytes + row * (BK * 2));
+                                  reinterpret_cast<const float*>(cs + kCodeBytes) + half * 68, o);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S->cempty[cstage]);
+        if (!mbar_wait_warp(&S->aempty[astage], asphase ^ 1u, abort_flag)) {
+          failed = true;
+          break;
+        }
+        store_a_row<kPieces>(o, row, piece0, s_a0 + astage * kABytes + row * (BK * 2));
         // the generic-proxy stores become visible to the tensor cores' reads
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&S->converted[astage]);  // CTA scope: the leader's MMA thread or the peer's signaller
-          mbar_arrive(&S->cempty[cstage]);
-        }
+        if (lane == 0) mbar_arrive(&S->converted[astage]);  // CTA scope: the leader's MMA thread or the peer's signaller
         if (++astage == C::kAStages) {
           astage = 0;
           asphase ^= 1u;
