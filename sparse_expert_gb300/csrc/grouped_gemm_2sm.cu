@@ -366,45 +366,18 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t word, float (&v)[4]) {
       : "r"(h23));
 }
 
-// One weight row of one K block: its 64 E4M3 codes (a 64-byte row of a tile
-// loaded with 64-byte swizzling: piece c of row s at c ^ ((s >> 1) & 3)) and
-// the K block's 64 scales become bf16(value x scale), the product of the
-// exact code value and the fp32 scale rounded once in fp32 and then to bf16
-// -- the dequantisation of the "FP8 expert weight all-gather", bit for bit.
-// NC of the row's four 16-value pieces, starting at piece c0, into
-// registers (o[ci] = piece c0 + ci as 16 bf16), so that the conversion runs
-// before the A slot it goes to is free.
-template <int NC>
-__device__ __forceinline__ void convert_code_row(const uint8_t* crow, int s, int c0, const float* sc,
-                                                 uint32_t (&o)[NC][8]) {
-  uint4 q[NC];
+// One 16-value piece of a weight row of one K block: 16 E4M3 codes and
+// their 16 scales become bf16(value x scale), the product of the exact code
+// value and the fp32 scale rounded once in fp32 and then to bf16 -- the
+// dequantisation of the "FP8 expert weight all-gather", bit for bit.
+__device__ __forceinline__ void convert_piece(const uint4& q, const float4 (&scl)[4], uint32_t (&o)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int i = 0; i < NC; ++i) q[i] = *reinterpret_cast<const uint4*>(crow + (((c0 + i) ^ ((s >> 1) & 3)) << 4));
-#pragma unroll
-  for (int ci = 0; ci < NC; ++ci) {
-    const int c = c0 + ci;
-    const uint32_t w[4] = {q[ci].x, q[ci].y, q[ci].z, q[ci].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 scl = *reinterpret_cast<const float4*>(sc + 16 * c + 4 * i);
-      float v[4];
-      e4m3x4_to_f32(w[i], v);
-      o[ci][2 * i] = pack_bf16x2(__fmul_rn(v[0], scl.x), __fmul_rn(v[1], scl.y));
-      o[ci][2 * i + 1] = pack_bf16x2(__fmul_rn(v[2], scl.z), __fmul_rn(v[3], scl.w));
-    }
-  }
-}
-
-// The converted pieces as the row's bytes of the 128-byte-swizzled K-major
-// A operand (16-byte piece j of row s at j ^ (s & 7)).
-template <int NC>
-__device__ __forceinline__ void store_a_row(const uint32_t (&o)[NC][8], int s, int c0, uint8_t* arow) {
-#pragma unroll
-  for (int ci = 0; ci < NC; ++ci) {
-    const int c = c0 + ci;
-    *reinterpret_cast<uint4*>(arow + (((2 * c) ^ (s & 7)) << 4)) = make_uint4(o[ci][0], o[ci][1], o[ci][2], o[ci][3]);
-    *reinterpret_cast<uint4*>(arow + (((2 * c + 1) ^ (s & 7)) << 4)) =
-        make_uint4(o[ci][4], o[ci][5], o[ci][6], o[ci][7]);
+  for (int i = 0; i < 4; ++i) {
+    float v[4];
+    e4m3x4_to_f32(w[i], v);
+    o[2 * i] = pack_bf16x2(__fmul_rn(v[0], scl[i].x), __fmul_rn(v[1], scl[i].y));
+    o[2 * i + 1] = pack_bf16x2(__fmul_rn(v[2], scl[i].z), __fmul_rn(v[3], scl[i].w));
   }
 }
 
@@ -693,15 +666,24 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
     }
   } else if (kFp8 && warp >= 2 + kEpiWarps && warp < 2 + kEpiWarps + C::kConvWarps) {
     // ------------------------------------------------ FP8 code converters
-    // thread = a slice of one of this CTA's 128 weight rows, per K block: its
-    // codes and the block's scales from the code stage to bf16 in the MMA
-    // stage's A slot, then a CTA-scope arrive on `converted`
-    constexpr int kPieces = 16 / (kFp8 ? C::kConvWarps : 4);  // 16-value pieces per thread
+    // thread = one 16-value piece (column c of the K block) of kRowsPer of
+    // this CTA's 128 weight rows, kRowStep apart, per K block: its codes and
+    // the piece's 16 scales from the code stage to bf16 in the MMA stage's A
+    // slot, then a CTA-scope arrive on `converted`.  The rows of one thread
+    // share their scales (same piece, same gate/up half) and their swizzle
+    // offsets; a warp's code loads cover 8 whole 64-byte rows and its stores
+    // 8 whole 128-byte rows, both free of bank conflicts.
+    constexpr int kRowStep = 8 * (kFp8 ? C::kConvWarps : 4);
+    constexpr int kRowsPer = kHalfRows / kRowStep;
     const int ci = (warp - 2 - kEpiWarps) * 32 + lane;
-    const int row = ci % kHalfRows;
-    const int piece0 = (ci / kHalfRows) * kPieces;
+    const int c = ci & 3;
+    const int rg = ci >> 2;
     // gate/up rows come in quarter order: 16 gate rows, then 16 up rows
-    const int half = (kMode == kModeSwiGLU) ? ((row >> 4) & 1) : 0;
+    // (kRowStep is a multiple of 32, so every row of the thread is in the same half)
+    const int half = (kMode == kModeSwiGLU) ? ((rg >> 4) & 1) : 0;
+    const int code_off = rg * BK + ((c ^ ((rg >> 1) & 3)) << 4);
+    const int a_off0 = rg * (BK * 2) + (((2 * c) ^ (rg & 7)) << 4);
+    const int a_off1 = rg * (BK * 2) + (((2 * c + 1) ^ (rg & 7)) << 4);
     const int num_kb = p.K / BK;
     int astage = 0, cstage = 0;
     uint32_t asphase = 0, cphase = 0;
@@ -730,16 +712,26 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           break;
         }
         const uint8_t* cs = s_code0 + cstage * C::kCodeStageBytes;
-        uint32_t o[kPieces][8];
-        convert_code_row<kPieces>(cs + row * BK, row, piece0,
-                                  reinterpret_cast<const float*>(cs + kCodeBytes) + half * 68, o);
+        const float* sc = reinterpret_cast<const float*>(cs + kCodeBytes) + half * 68 + 16 * c;
+        float4 scl[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) scl[i] = *reinterpret_cast<const float4*>(sc + 4 * i);
+        uint32_t o[kRowsPer][8];
+#pragma unroll
+        for (int j = 0; j < kRowsPer; ++j)
+          convert_piece(*reinterpret_cast<const uint4*>(cs + code_off + j * kRowStep * BK), scl, o[j]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S->cempty[cstage]);
         if (!mbar_wait_warp(&S->aempty[astage], asphase ^ 1u, abort_flag)) {
           failed = true;
           break;
         }
-        store_a_row<kPieces>(o, row, piece0, s_a0 + astage * kABytes + row * (BK * 2));
+        uint8_t* as = s_a0 + astage * kABytes;
+#pragma unroll
+        for (int j = 0; j < kRowsPer; ++j) {
+          *reinterpret_cast<uint4*>(as + a_off0 + j * kRowStep * BK * 2) = make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
+          *reinterpret_cast<uint4*>(as + a_off1 + j * kRowStep * BK * 2) = make_uint4(o[j][4], o[j][5], o[j][6], o[j][7]);
+        }
         // the generic-proxy stores become visible to the tensor cores' reads
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
