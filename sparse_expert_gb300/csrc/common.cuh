@@ -107,6 +107,39 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
   }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// suspended until it completes or about hint_ns have passed, instead of
+// returning at once, so a warp that waits long does not spin through the
+// issue slots that the pipeline's producer and MMA threads need.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// mbar_wait_warp for long waits: the same bounded, warp-uniform outcome,
+// each round suspending the warp for up to hint_ns.
+__device__ __forceinline__ bool mbar_wait_warp_suspend(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                       uint32_t hint_ns = 20000, uint64_t limit_ns = kWaitLimitNs) {
+  const uint32_t a = smem_addr(bar);
+  uint64_t t0 = 0;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) t0 = global_timer_ns();
+  for (;;) {
+    const bool ok = mbar_try_wait_hint(a, parity, hint_ns);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    int give_up = 0;
+    if (lane == 0) give_up = (*abort != 0) || (global_timer_ns() - t0 > limit_ns);
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+  }
+}
+
 // ------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
