@@ -595,16 +595,19 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
           tc_fence_after_sync();
           const uint32_t a0 = kFp8 ? smem_addr(s_a0 + astage * kABytes) : smem_addr(s_stage0 + stage * kStageBytes);
           const uint32_t b1 = kFp8 ? smem_addr(s_stage0 + stage * C::kSlotBytes) : a0 + kABytes;
-          const uint32_t b2 = b1 + kBBytes;
+          // the stage's descriptors once; a K step of 16 advances the start
+          // address (16-byte units) by 2 (K-major) or, for MN-major A, by
+          // 16 rows of 128 bytes = 128
+          const uint64_t da0 = p.a_mn ? sw128_mnmajor_desc(a0, kABytes / 2) : sw128_kmajor_desc(a0);
+          const uint64_t da_step = p.a_mn ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
+          const uint64_t db1 = sw128_kmajor_desc(b1);
+          const uint64_t db2 = db1 + (kBBytes >> 4);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // MN-major A: two 8 KB chunks of [64 K][64 M]; 16 K rows = 2 KB
-            const uint64_t da = p.a_mn ? sw128_mnmajor_desc(a0 + kk * UMMA_K * 128, kABytes / 2)
-                                       : sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
+            const uint64_t da = da0 + kk * da_step;
             const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
-            umma_pair(d_tmem, da, sw128_kmajor_desc(b1 + kk * UMMA_K * 2), idesc1, accumulate);
-            if (n2 > 0)
-              umma_pair(d_tmem + kPartN, da, sw128_kmajor_desc(b2 + kk * UMMA_K * 2), idesc2, accumulate);
+            umma_pair(d_tmem, da, db1 + 2 * kk, idesc1, accumulate);
+            if (n2 > 0) umma_pair(d_tmem + kPartN, da, db2 + 2 * kk, idesc2, accumulate);
           }
           umma_commit_pair(&S->empty[stage]);
           if (++stage == kStages) {
@@ -818,7 +821,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       }
       if (t < 0) break;
       const Tile x = decode(t, s_off, s_pre, p.E, p.m_tiles);
-      if (!mbar_wait_warp(&S->tfull[0], aphase, abort_flag)) {
+      if (!mbar_wait_warp_suspend(&S->tfull[0], aphase, abort_flag)) {
         failed = true;
         break;
       }
