@@ -287,14 +287,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
           // (generic proxy); order them before the tensor cores read them
           if constexpr (kGather) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_after_sync();
-          const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
-          const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+          // the stage's descriptors once; a K step of 16 advances the start
+          // address (16-byte units) by 2
+          const uint64_t da = sw128_kmajor_desc(smem_addr(sA + stage * C::kABytes));
+          const uint64_t db = sw128_kmajor_desc(smem_addr(sB + stage * C::kBBytes));
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t da = sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
-            const uint64_t db = sw128_kmajor_desc(b0 + kk * UMMA_K * 2);
-            umma_bf16(d_tmem, da, db, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / UMMA_K; ++kk)
+            umma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
           umma_commit(&S->empty[stage]);  // frees the stage when these MMAs finish
           if (++stage == C::kStages) {
             stage = 0;
@@ -396,7 +395,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       const int64_t wrow0 = static_cast<int64_t>(s_off[e]) + mt * BM + quad * 32;
       const int valid_rows = static_cast<int>(min(static_cast<int64_t>(32), max(static_cast<int64_t>(0),
                                                                                  s_off[e + 1] - wrow0)));
-      if (!mbar_wait_warp(&S->tfull[acc], aphase, abort_flag)) {
+      if (!mbar_wait_warp_suspend(&S->tfull[acc], aphase, abort_flag)) {
         if (lane == 0) {
           record_status(p.status, kStatusTimeout);
           *abort_flag = 1;

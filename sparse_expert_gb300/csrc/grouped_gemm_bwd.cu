@@ -326,16 +326,16 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
           }
         }
         if (lane == 0) {
-          const uint32_t a0 = smem_addr(a_st);
-          const uint32_t b0 = smem_addr(b_st);
+          // the stage's descriptors once; a K step of 16 advances the start
+          // address (16-byte units) by 2 (K-major) or 16 rows of 128 bytes (MN-major)
+          const uint64_t da0 = C::kAMN ? sw128_mnmajor_desc(smem_addr(a_st), kChunk) : sw128_kmajor_desc(smem_addr(a_st));
+          const uint64_t db0 = C::kBMN ? sw128_mnmajor_desc(smem_addr(b_st), kChunk) : sw128_kmajor_desc(smem_addr(b_st));
+          constexpr uint64_t kStepA = C::kAMN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
+          constexpr uint64_t kStepB = C::kBMN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             if (kk >= n_kk) break;
-            const uint64_t da = C::kAMN ? sw128_mnmajor_desc(a0 + kk * UMMA_K * 128, kChunk)
-                                        : sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
-            const uint64_t db = C::kBMN ? sw128_mnmajor_desc(b0 + kk * UMMA_K * 128, kChunk)
-                                        : sw128_kmajor_desc(b0 + kk * UMMA_K * 2);
-            umma_bf16(d_tmem, da, db, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, da0 + kk * kStepA, db0 + kk * kStepB, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit(&S->empty[stage]);
         }
@@ -393,7 +393,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
         valid_rows = static_cast<int>(min(static_cast<int64_t>(32), max(static_cast<int64_t>(0),
                                                                         s_off[e + 1] - wrow0)));
       }
-      if (!mbar_wait_warp(&S->tfull[acc], aphase, abort_flag)) {
+      if (!mbar_wait_warp_suspend(&S->tfull[acc], aphase, abort_flag)) {
         if (lane == 0) {
           record_status(p.status, kStatusTimeout);
           *abort_flag = 1;
