@@ -1,9 +1,9 @@
 #!/usr/bin/env python
 """Throughput of one MoE-layer forward on GB300 (and, on the side, of its backward).
 
-A step is one pass of the whole path — route + token counts, look-back
-index, permute, gate/up grouped GEMM with SwiGLU, down grouped GEMM with
-gate scale, combine — over one batch of T tokens, with inputs and packed
+A step is one pass of the whole path — route + per-chunk token counts,
+index (counts, offsets, rows), permute, gate/up grouped GEMM with SwiGLU,
+down grouped GEMM, gate-weighted combine — over one batch of T tokens, with inputs and packed
 weights resident in HBM.  Default workload: one layer of the 951.9B model
 (T=16,384 tokens, d=6,144, E=384 experts, top-8, f=1,792), seeded
 synthetic inputs.  The working set (25 GB of weights, 201 MB of tokens)
@@ -173,11 +173,14 @@ def recorded_traffic(workload: str):
 
 
 # ------------------------------------------------------- algorithmic work
-def stage_work(cfg):
-    """Algorithmic bytes / FLOPs per launch of each stage (real rows only)."""
+def stage_work(cfg, counts=None, weight_bytes_per_value=2.0):
+    """Algorithmic bytes / FLOPs per launch of each stage (real rows only).
+    Given the token counts, the GEMMs also get their algorithmic bytes: the
+    weights of every expert with rows (weight_bytes_per_value per weight:
+    2 for bf16, codes plus scales for FP8) and their activations once."""
     T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
     P = T * k
-    return {
+    work = {
         "route": {"bytes": T * E * 4 + P * 8},
         "index": {"bytes": P * 4 + P * 4 + 3 * P * 4 + E * 8},
         "permute": {"bytes": T * d * 2 + P * d * 2 + P * 4},
@@ -185,6 +188,12 @@ def stage_work(cfg):
         "down": {"flops": 2 * P * d * f},
         "combine": {"bytes": P * d * 2 + T * d * 2 + P * 4 + P * 4},   # rows, out, dest_row, gates
     }
+    if counts is not None:
+        nonempty = int((np.asarray(counts) > 0).sum())
+        w = nonempty * d * f * weight_bytes_per_value
+        work["gate_up"]["bytes"] = int(2 * w + P * d * 2 + P * f * 2)   # Wg, Wu; x_perm read, H written
+        work["down"]["bytes"] = int(w + P * f * 2 + P * d * 2)          # Wd; H read, Y written
+    return work
 
 
 def backward_gemm_flops(cfg):
@@ -309,15 +318,15 @@ def time_oracle(cfg, sample):
 
 
 def stage_table(stage_ms, work, peaks):
-    """Per-stage ms with TFLOP/s and fraction of the bf16 peak (GEMMs) or GB/s
-    and fraction of the HBM copy bandwidth (the rest)."""
+    """Per-stage ms with TFLOP/s and fraction of the bf16 peak (GEMMs) and/or
+    GB/s and fraction of the HBM copy bandwidth (every stage with bytes)."""
     stages = {}
     for name, ms in stage_ms.items():
         st = {"ms": round(ms, 4)}
         if "flops" in work[name]:
             st["tflops"] = round(work[name]["flops"] / (ms * 1e-3) / 1e12, 2)
             st["frac_bf16_peak"] = round(st["tflops"] / peaks["bf16_tflops"], 4)
-        else:
+        if "bytes" in work[name]:
             st["gbs"] = round(work[name]["bytes"] / (ms * 1e-3) / 1e9, 1)
             st["frac_hbm"] = round(st["gbs"] / peaks["hbm_gbs"], 4)
         stages[name] = st
@@ -362,7 +371,7 @@ def measure_workload(moe, name, seed, steps, warmup, world, local):
     stage_ms = {nm: statistics.mean(events[s_][i].elapsed_time(events[s_][i + 1]) for s_ in range(steps))
                 for i, nm in enumerate(moe.FORWARD_STAGES)}
     peaks = load_peaks()
-    work = stage_work(cfg)
+    work = stage_work(cfg, counts)
     stages = stage_table(stage_ms, work, peaks)
     gemm_ms = stage_ms["gate_up"] + stage_ms["down"]
     gemm_tf = (work["gate_up"]["flops"] + work["down"]["flops"]) / (gemm_ms * 1e-3) / 1e12
@@ -427,7 +436,7 @@ def gpu_arm(args):
 
     stage_ms = {name: statistics.mean(events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps))
                 for i, name in enumerate(moe.FORWARD_STAGES)}
-    work = stage_work(cfg)
+    work = stage_work(cfg, counts)
     peaks = load_peaks()
     stages = stage_table(stage_ms, work, peaks)
     gemm_ms = stage_ms["gate_up"] + stage_ms["down"]
@@ -495,6 +504,7 @@ def gpu_arm(args):
     if not args.no_fp8:
         q = [moe.moe_quantize_fp8_blockwise(inp[n].reshape(-1)) for n in ("w_gate", "w_up", "w_down")]
         packed_fp8 = moe.moe_pack_weights_fp8(q[0], q[1], q[2], E, d, f)
+        fp8_bytes = moe.moe_fp8_packed_weight_bytes(E, d, f)  # codes and scale records
         del q
         fev = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)] for _ in range(args.steps)]
         for _ in range(args.warmup):
@@ -516,8 +526,9 @@ def gpu_arm(args):
         fstage = {name: statistics.mean(fev[s_][i].elapsed_time(fev[s_][i + 1]) for s_ in range(args.steps))
                   for i, name in enumerate(moe.FORWARD_STAGES)}
         fp8 = {"value": round(job_throughput(T * args.steps, world, fp8_s), 1), "unit": "tokens/s",
-               "ms_per_step": round(fp8_s * 1e3 / args.steps, 4), "stages": stage_table(fstage, work, peaks),
-               "weight_bytes_read": moe.moe_fp8_packed_weight_bytes(E, d, f), "clocks": fclk,
+               "ms_per_step": round(fp8_s * 1e3 / args.steps, 4),
+               "stages": stage_table(fstage, stage_work(cfg, counts, fp8_bytes / (3 * E * d * f)), peaks),
+               "weight_bytes_read": fp8_bytes, "clocks": fclk,
                "note": "not the headline: weights stored as E4M3 codes with one fp32 scale per 128 values (lower "
                        "weight precision); the GEMMs dequantise each stage in shared memory, bit-identical to the "
                        "bf16 path on the dequantised weights, and read about half the weight bytes"}
