@@ -534,6 +534,36 @@ def gpu_arm(args):
                        "bf16 path on the dequantised weights, and read about half the weight bytes"}
         del packed_fp8
 
+    # the same forward captured once into a CUDA graph and replayed: no host
+    # work between steps and no launch gaps inside one
+    graph_fwd = None
+    if not args.no_graph:
+        gstream = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(gstream):
+            with torch.cuda.graph(graph, stream=gstream):
+                moe.moe_forward(x, logits, packed, E, k, f, cfg.renormalize, workspace=ws, out=out, stream=gstream)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        if moe.moe_read_device_status(ws) != 0:
+            raise SystemExit("device status after the graph replays")
+        barrier(world)
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        graph_s = max_over_ranks(g0.elapsed_time(g1) / 1e3, world, device="cuda")
+        graph_fwd = {"value": round(job_throughput(T * args.steps, world, graph_s), 1), "unit": "tokens/s",
+                     "ms_per_step": round(graph_s * 1e3 / args.steps, 4),
+                     "note": "moe_forward captured once into a CUDA graph (torch.cuda.CUDAGraph) and replayed per step"}
+        del graph
+
     # the layer from the tokens: fused router (router GEMM + top-k) instead of given logits
     routed = None
     if not args.no_routed:
@@ -664,7 +694,7 @@ def gpu_arm(args):
                              "weight_bytes_read": weight_bytes_read(cfg, counts)},
             "permute_gbs": stages["permute"]["gbs"],
             "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed,
-            "gathered_forward": gathered, "fp8_weights_forward": fp8,
+            "gathered_forward": gathered, "fp8_weights_forward": fp8, "graph_forward": graph_fwd,
             "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk,
             "backward": backward, "configs": configs,
         }
@@ -755,6 +785,7 @@ def parse_args(argv):
     ap.add_argument("--no-gathered", action="store_true", help="skip the gathered (no x_perm) forward measurement")
     ap.add_argument("--no-configs", action="store_true", help="skip the other seeded workloads (small, skew, long)")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight forward measurement")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the forward")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048,
                     help="tokens of the CPU baseline's permute/combine sample")
     ap.add_argument("--cpu-sample-experts", type=int, default=16,
