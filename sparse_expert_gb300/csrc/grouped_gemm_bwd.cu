@@ -48,6 +48,9 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kRing = 4;
 constexpr int kStoreStageBytes = kEpiWarps * 32 * 64;
 constexpr int kStageBudget = 227 * 1024 - 1024 - 1024 - 2 * 1025 * 4 - 1024 - kStoreStageBytes;
+// weight gradients: 64-column chunks whose rows past an expert's last row are
+// zeroed before the last K block's MMAs (A's: BM / 64 of them)
+constexpr int kZeroChunks = BM / 64;
 
 enum class Mode { kGateUpSave, kDgradSwiGLU, kDgradPlain, kWgrad };
 
@@ -309,14 +312,16 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_c
             n_kk = (valid + UMMA_K - 1) / UMMA_K;
             const int zend = n_kk * UMMA_K;
             if (valid < zend) {
-              // rows valid .. zend-1 of every chunk belong to the next expert
-              // (or lie past the matrix): a whole 128-byte row is zero
-              // whatever the swizzle does inside it
+              // rows valid .. zend-1 belong to the next expert (or lie past
+              // the matrix, where TMA filled zeros): zeroing them in A's
+              // chunks alone removes their products, since B's rows there are
+              // finite; a whole 128-byte row is zero whatever the swizzle
+              // does inside it
               // lane: 16-byte piece lane % 8 of rows valid + lane / 8, +4, ...
               const uint4 zero = make_uint4(0, 0, 0, 0);
               const int piece = lane & 7;
 #pragma unroll
-              for (int c = 0; c < (BM + BN) / 64; ++c) {
+              for (int c = 0; c < kZeroChunks; ++c) {
                 uint8_t* cb = c < BM / 64 ? a_st + c * kChunk : b_st + (c - BM / 64) * kChunk;
                 for (int r = valid + (lane >> 3); r < zend; r += 4) reinterpret_cast<uint4*>(cb + r * 128)[piece] = zero;
               }
