@@ -143,9 +143,12 @@ route_backward_kernel(const float* __restrict__ logits, const int32_t* __restric
   }
 }
 
+// One token per warp up to 16 blocks per SM (two rounds of resident blocks):
+// at 16k tokens each warp then takes one token and finished blocks make room
+// for the rest, instead of every resident warp looping over 1-2 tokens.
 int token_grid(int64_t T, int num_sms) {
   const int64_t want = (T + kWarps - 1) / kWarps;
-  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
   return static_cast<int>(want < cap ? want : cap);
 }
 
