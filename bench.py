@@ -564,6 +564,52 @@ def gpu_arm(args):
                      "note": "moe_forward captured once into a CUDA graph (torch.cuda.CUDAGraph) and replayed per step"}
         del graph
 
+    # the dynamic tile schedule against a static one, with a kernel holding
+    # 40 SMs on a second stream for the first half of every step (the
+    # SonicMoE page's measurement, a dummy kernel occupying 40 SMs)
+    contention = None
+    if not args.no_contention:
+        busy = 40
+        side = torch.cuda.Stream()
+        n_sms = torch.cuda.get_device_properties(local).multi_processor_count
+        csteps = max(3, min(args.steps, 10))
+
+        def timed(loaded, hold_ns):
+            for _ in range(2):
+                moe.moe_forward(x, logits, packed, E, k, f, cfg.renormalize, workspace=ws, out=out)
+            torch.cuda.synchronize()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(csteps + 1)]
+            ev[0].record(stream)
+            for i in range(csteps):
+                if loaded:
+                    # the occupier starts with the step: the side stream waits for the step boundary
+                    side.wait_event(ev[i])
+                    moe.moe_occupy_sms(busy, hold_ns, stream=side)
+                moe.moe_forward(x, logits, packed, E, k, f, cfg.renormalize, workspace=ws, out=out)
+                ev[i + 1].record(stream)
+            torch.cuda.synchronize()
+            return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(csteps))
+
+        cres = {}
+        hold_ns = 0
+        for mode, name in ((moe.TILE_SCHEDULE_DYNAMIC, "dynamic"), (moe.TILE_SCHEDULE_STATIC, "static")):
+            moe.moe_set_tile_schedule(mode)
+            free_ms = timed(False, 0)
+            if name == "dynamic":
+                hold_ns = int(free_ms * 0.5e6)  # half of an unloaded step
+            busy_ms = timed(True, hold_ns)
+            cres[name] = {"ms_per_step": round(free_ms, 4), "ms_per_step_loaded": round(busy_ms, 4),
+                          "slowdown": round(busy_ms / free_ms, 4)}
+        moe.moe_set_tile_schedule(moe.TILE_SCHEDULE_DYNAMIC)
+        if moe.moe_read_device_status(ws) != 0:
+            raise SystemExit("device status after the contention steps")
+        contention = {"busy_sms": busy, "sms": n_sms, "hold_ms": round(hold_ns / 1e6, 4),
+                      # the step's SM-time lost to the occupier, as a fraction of the unloaded step
+                      "sm_time_lost": round(busy * hold_ns / 1e6 / (n_sms * cres["dynamic"]["ms_per_step"]), 4),
+                      **cres,
+                      "note": "median step times; the occupier (moe_occupy_sms) holds busy_sms SMs for hold_ms from the "
+                              "start of each step"}
+
     # the layer from the tokens: fused router (router GEMM + top-k) instead of given logits
     routed = None
     if not args.no_routed:
@@ -695,6 +741,7 @@ def gpu_arm(args):
             "permute_gbs": stages["permute"]["gbs"],
             "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed,
             "gathered_forward": gathered, "fp8_weights_forward": fp8, "graph_forward": graph_fwd,
+            "contention": contention,
             "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk,
             "backward": backward, "configs": configs,
         }
@@ -786,6 +833,8 @@ def parse_args(argv):
     ap.add_argument("--no-configs", action="store_true", help="skip the other seeded workloads (small, skew, long)")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight forward measurement")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the forward")
+    ap.add_argument("--no-contention", action="store_true",
+                    help="skip the tile-schedule measurement beside a kernel holding 40 SMs")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048,
                     help="tokens of the CPU baseline's permute/combine sample")
     ap.add_argument("--cpu-sample-experts", type=int, default=16,

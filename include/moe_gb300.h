@@ -616,6 +616,33 @@ MOE_API moe_status_t moe_get_device_status(const void* workspace, moe_stream_t s
 MOE_API moe_status_t moe_selftest_activation(const float* z, int64_t n, float* silu, float* sigmoid,
                                              moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Measurement tools for the expert GEMMs' tile scheduling ("Training a
+ * 1T-Params MoE on EU public infrastructure", *Dynamic tile scheduling in
+ * SonicMoE*: tiles handed out at run time keep throughput when part of the
+ * GPU is busy with other work; the page measures it against a dummy kernel
+ * occupying 40 SMs).
+ *
+ * moe_set_tile_schedule: the tile schedule of the paired-SM expert GEMMs
+ * launched afterwards by this process: MOE_TILE_SCHEDULE_DYNAMIC (the
+ * default: every SM pair takes its next tile from a shared atomic counter)
+ * or MOE_TILE_SCHEDULE_STATIC (pair i takes tiles i, i + pairs, i + 2 pairs,
+ * ... whatever the others do).  Results are identical under both; only the
+ * order in which tiles run differs.  Not thread-safe against concurrent
+ * launches.  Errors: MOE_ERR_INVALID_ARG (another mode).
+ *
+ * moe_occupy_sms: a kernel of n_sms blocks on `stream` (0 <= n_sms <= the
+ * device's SM count), each holding one SM (it takes most of the SM's shared
+ * memory, so no expert-GEMM block fits beside it) and returning after
+ * duration_ns (0 .. 10^10 ns); kernels on other streams run on the other
+ * SMs meanwhile.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_NO_DEVICE,
+ * MOE_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+#define MOE_TILE_SCHEDULE_DYNAMIC 0
+#define MOE_TILE_SCHEDULE_STATIC 1
+MOE_API moe_status_t moe_set_tile_schedule(int32_t mode);
+MOE_API moe_status_t moe_occupy_sms(int32_t n_sms, int64_t duration_ns, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -83,6 +83,8 @@ SIGNATURES = {
     "moe_dispatch_noalloc_status": (_S, [_P, ctypes.POINTER(_I32)]),
     "moe_selftest_wait_timeout": (_S, [_P, _SZ, _I64, _P]),
     "moe_selftest_activation": (_S, [_P, _I64, _P, _P, _P]),
+    "moe_set_tile_schedule": (_S, [_I32]),
+    "moe_occupy_sms": (_S, [_I32, _I64, _P]),
     "moe_forward_host_stream": (_S, [_P, _P, _P, _I32, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
                                      _P, _P, _P]),
     "moe_grouped_gate_up_save": (_S, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -603,6 +605,20 @@ def moe_selftest_activation(z, stream=None):
     _check(lib.moe_selftest_activation(_ptr(z), z.numel(), _ptr(silu), _ptr(sig), _stream(stream)),
            "moe_selftest_activation")
     return silu, sig
+
+
+TILE_SCHEDULE_DYNAMIC = 0
+TILE_SCHEDULE_STATIC = 1
+
+
+def moe_set_tile_schedule(mode):
+    """The paired expert GEMMs' tile schedule for the rest of the process (measurement)."""
+    _check(lib.moe_set_tile_schedule(int(mode)), "moe_set_tile_schedule")
+
+
+def moe_occupy_sms(n_sms, duration_ns, stream=None):
+    """A kernel holding n_sms SMs for duration_ns on `stream` (measurement)."""
+    _check(lib.moe_occupy_sms(int(n_sms), int(duration_ns), _stream(stream)), "moe_occupy_sms")
 
 
 def forward_intermediates(workspace, T, E, k, d, f):

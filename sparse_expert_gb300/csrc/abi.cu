@@ -1005,6 +1005,24 @@ moe_status_t moe_selftest_activation(const float* z, int64_t n, float* silu, flo
   return MOE_OK;
 }
 
+moe_status_t moe_set_tile_schedule(int32_t mode) {
+  if (mode != MOE_TILE_SCHEDULE_DYNAMIC && mode != MOE_TILE_SCHEDULE_STATIC)
+    return fail(MOE_ERR_INVALID_ARG, "tile schedule must be MOE_TILE_SCHEDULE_DYNAMIC or MOE_TILE_SCHEDULE_STATIC");
+  set_static_tile_schedule(mode == MOE_TILE_SCHEDULE_STATIC);
+  return MOE_OK;
+}
+
+moe_status_t moe_occupy_sms(int32_t n_sms, int64_t duration_ns, moe_stream_t stream) {
+  DeviceInfo dev;
+  moe_status_t s = device_info(&dev);
+  if (s != MOE_OK) return s;
+  if (n_sms < 0 || n_sms > dev.num_sms) return fail(MOE_ERR_INVALID_ARG, "n_sms outside [0, the SM count]");
+  if (duration_ns < 0 || duration_ns > 10000000000LL) return fail(MOE_ERR_INVALID_ARG, "duration_ns outside [0, 1e10]");
+  MOE_CUDA(launch_occupy(n_sms, static_cast<uint64_t>(duration_ns), static_cast<cudaStream_t>(stream)),
+           "occupy launch");
+  return MOE_OK;
+}
+
 moe_status_t moe_read_device_status(const void* workspace, moe_stream_t stream, int32_t* status) {
   if (!workspace || !status) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   MOE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");

@@ -66,6 +66,11 @@
 #include "moe_gb300.h"
 
 namespace moe {
+
+// the paired GEMMs' tile schedule for this process (set through the C ABI
+// for measurement; dynamic by default)
+static bool g_static_tiles = false;
+
 namespace {
 
 constexpr int BK = 64;
@@ -147,6 +152,7 @@ struct Params {
   int sc_tiles;         // scale tiles per expert
   int sc_per_cta;       // 1: each CTA of a pair has its own scale tile (down); 0: one per pair (gate/up)
   int rec_floats;
+  int static_tiles;     // 1: pair i takes tiles i, i + pairs, ... (measurement); 0: a shared counter
 };
 
 template <bool kFp8>
@@ -473,6 +479,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
       uint32_t phase = 0;
       int rs = 0;
       uint32_t rphase = 0;
+      int claimed = 0;
       for (;;) {
         // tiles come from a shared counter (dynamic scheduling): the leader
         // claims one and publishes it in both CTAs' rings
@@ -482,7 +489,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             failed = true;
             break;
           }
-          t = atomicAdd(p.tile_counter, 1);
+          // static schedule (for measurement): pair i takes tiles i, i + pairs, ...
+          t = p.static_tiles ? static_cast<int>(blockIdx.x >> 1) + claimed++ * static_cast<int>(gridDim.x >> 1)
+                             : atomicAdd(p.tile_counter, 1);
           if (t >= total) t = -1;
           S->ring[rs] = t;
           st_cluster(pair_addr(&S->ring[rs], 1), t);
@@ -1118,6 +1127,7 @@ cudaError_t launch_pairs(const CUtensorMap& mw, const CUtensorMap& mx, const Par
 
 Params base_params(const int32_t* offsets, int E, int K, int32_t* tile_counter, int32_t* status) {
   Params prm{};
+  prm.static_tiles = g_static_tiles ? 1 : 0;
   prm.offsets = offsets;
   prm.status = status;
   prm.tile_counter = tile_counter;
@@ -1127,6 +1137,8 @@ Params base_params(const int32_t* offsets, int E, int K, int32_t* tile_counter, 
 }
 
 }  // namespace
+
+void set_static_tile_schedule(bool on) { g_static_tiles = on; }
 
 cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream) {
   if (pb.P == 0) return cudaSuccess;

@@ -112,6 +112,11 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pb, Epilogue epi, int 
 // The paired-SM form (weights as the 256-row operand, up to 512 of an
 // expert's tokens as N): used by launch_grouped_gemm when the weight rows
 // per expert (2f, or d) are a multiple of 256.
+// The paired GEMMs' tile schedule for the rest of the process: a shared
+// atomic counter (default) or a static stride over the pairs (measurement).
+void set_static_tile_schedule(bool on);
+// A kernel holding n_sms SMs (one block each) for duration_ns.
+cudaError_t launch_occupy(int n_sms, uint64_t duration_ns, cudaStream_t stream);
 bool grouped_gemm_2sm_supported(const GroupedGemmProblem& pb, Epilogue epi);
 cudaError_t launch_grouped_gemm_2sm(const GroupedGemmProblem& pb, Epilogue epi, int num_sms, cudaStream_t stream);
 // The paired form reading FP8 weights (moe_pack_weights_fp8's layout): b =

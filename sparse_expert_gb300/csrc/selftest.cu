@@ -3,7 +3,9 @@
 // MOE_ERR_TIMEOUT in the workspace status word and returns, leaving the
 // context usable (nothing here faults, traps or spins without a bound).  The
 // activation functions: the exact device functions the expert-GEMM
-// epilogues apply, elementwise, so that their error can be measured.
+// epilogues apply, elementwise, so that their error can be measured.  And a
+// measurement tool: a kernel that holds a number of SMs for a bounded time,
+// to see how the dynamically scheduled GEMMs share the rest.
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,7 +43,29 @@ __global__ void activation_kernel(const float* __restrict__ z, int64_t n, float*
   }
 }
 
+// One block per SM it occupies: the block's dynamic shared memory (set by
+// the launch) keeps any kernel that needs most of an SM's shared memory off
+// that SM, and one thread sleeps until the block has existed for
+// duration_ns.
+__global__ void __launch_bounds__(32) occupy_kernel(uint64_t duration_ns) {
+  extern __shared__ uint8_t hold[];
+  if (threadIdx.x == 0) {
+    hold[0] = 0;
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < duration_ns) __nanosleep(2000);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_occupy(int n_sms, uint64_t duration_ns, cudaStream_t stream) {
+  if (n_sms == 0 || duration_ns == 0) return cudaSuccess;
+  constexpr int kHold = 160 * 1024;  // over half of an SM's 228 KB: one block per SM
+  cudaError_t err = cudaFuncSetAttribute(occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHold);
+  if (err != cudaSuccess) return err;
+  occupy_kernel<<<n_sms, 32, kHold, stream>>>(duration_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_activation(const float* z, int64_t n, float* silu, float* sigmoid, int num_sms,
                               cudaStream_t stream) {

@@ -163,6 +163,13 @@ def test_activation_check_argument_errors():
     assert lib.moe_selftest_activation(FAKE, 4, FAKE, NULL, NULL) == INVALID
 
 
+def test_tile_schedule_argument_errors():
+    assert lib.moe_set_tile_schedule(2) == INVALID
+    assert lib.moe_set_tile_schedule(-1) == INVALID
+    assert lib.moe_set_tile_schedule(1) == 0
+    assert lib.moe_set_tile_schedule(0) == 0  # back to the default
+
+
 # The boundary the hot path was specified against: each call with its
 # parameter names (bf16 buffers are void*, cudaStream_t is moe_stream_t).
 CONTRACT = {
