@@ -317,6 +317,21 @@ def time_oracle(cfg, sample):
     return time.perf_counter() - t0
 
 
+def stage_breakdown(moe, events, run_timed):
+    """Per-stage mean times from as many steps as the timed region, run again
+    after it, each with CUDA events at its stage boundaries (the timed region
+    itself runs without them).  A short pass would not do: under the power cap
+    the SM clock recovers in the idle gap before it, and a 20-step pass read
+    gate/up 4 % faster than the steady state."""
+    n = len(events)
+    torch.cuda.synchronize()
+    for s in range(n):
+        run_timed(events[s])
+    torch.cuda.synchronize()
+    return {name: statistics.mean(events[s][i].elapsed_time(events[s][i + 1]) for s in range(n))
+            for i, name in enumerate(moe.FORWARD_STAGES)}
+
+
 def stage_table(stage_ms, work, peaks):
     """Per-stage ms with TFLOP/s and fraction of the bf16 peak (GEMMs) and/or
     GB/s and fraction of the HBM copy bandwidth (every stage with bytes)."""
@@ -348,7 +363,7 @@ def measure_workload(moe, name, seed, steps, warmup, world, local):
     nstage = len(moe.FORWARD_STAGES)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)] for _ in range(steps)]
     for _ in range(warmup):
-        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, events[0], cfg.renormalize, stream)
+        moe.moe_forward(x, logits, packed, E, k, f, cfg.renormalize, workspace=ws, out=out, stream=stream)
     torch.cuda.synchronize()
     if moe.moe_read_device_status(ws) != 0:
         raise SystemExit(f"device status after the {name} warm-up")
@@ -360,7 +375,7 @@ def measure_workload(moe, name, seed, steps, warmup, world, local):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for s_ in range(steps):
-        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, events[s_], cfg.renormalize, stream)
+        moe.moe_forward(x, logits, packed, E, k, f, cfg.renormalize, workspace=ws, out=out, stream=stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -368,8 +383,8 @@ def measure_workload(moe, name, seed, steps, warmup, world, local):
     if moe.moe_read_device_status(ws) != 0:
         raise SystemExit(f"device status after the {name} steps")
     max_s = max_over_ranks(t0.elapsed_time(t1) / 1e3, world, device="cuda")
-    stage_ms = {nm: statistics.mean(events[s_][i].elapsed_time(events[s_][i + 1]) for s_ in range(steps))
-                for i, nm in enumerate(moe.FORWARD_STAGES)}
+    stage_ms = stage_breakdown(moe, events, lambda ev: moe.moe_forward_timed(
+        x, logits, packed, E, k, f, ws, out, ev, cfg.renormalize, stream))
     peaks = load_peaks()
     work = stage_work(cfg, counts)
     stages = stage_table(stage_ms, work, peaks)
@@ -405,14 +420,21 @@ def gpu_arm(args):
     stream = torch.cuda.current_stream()
     nstage = len(moe.FORWARD_STAGES)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)] for _ in range(args.steps)]
-    warm_events = [torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)]
 
     for _ in range(args.warmup):
-        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, warm_events, cfg.renormalize, stream)
+        moe.moe_forward(x, logits, packed, E, k, f, cfg.renormalize, workspace=ws, out=out, stream=stream)
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(ws) == 0, "device status after warm-up"
     inter = moe.forward_intermediates(ws, T, E, k, d, f)
     counts = inter["counts"].cpu().numpy()
+
+    # events only at the GEMMs' boundaries (3: gate/up, 4: down, 5: combine): the roofline's kernel
+    # time comes from the timed region itself, at the cost of three events a step; each is recorded
+    # once here so that its handle exists before the timed region
+    gemm_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for ev3 in gemm_ev:
+        for e in ev3:
+            e.record(stream)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -422,7 +444,9 @@ def gpu_arm(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for s in range(args.steps):
-        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, events[s], cfg.renormalize, stream)
+        ev = [None] * (nstage + 1)
+        ev[3], ev[4], ev[5] = gemm_ev[s]
+        moe.moe_forward_timed(x, logits, packed, E, k, f, ws, out, ev, cfg.renormalize, stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -434,39 +458,43 @@ def gpu_arm(args):
     max_s = max_over_ranks(elapsed_ms / 1e3, world, device="cuda")
     value = job_throughput(T * args.steps, world, max_s)
 
-    stage_ms = {name: statistics.mean(events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps))
-                for i, name in enumerate(moe.FORWARD_STAGES)}
+    region_ms = {"gate_up": statistics.mean(a.elapsed_time(b) for a, b, _ in gemm_ev),
+                 "down": statistics.mean(b.elapsed_time(c) for _, b, c in gemm_ev)}
+    stage_ms = stage_breakdown(moe, events, lambda ev: moe.moe_forward_timed(
+        x, logits, packed, E, k, f, ws, out, ev, cfg.renormalize, stream))
     work = stage_work(cfg, counts)
     peaks = load_peaks()
     stages = stage_table(stage_ms, work, peaks)
     gemm_ms = stage_ms["gate_up"] + stage_ms["down"]
     gemm_tflops = (work["gate_up"]["flops"] + work["down"]["flops"]) / (gemm_ms * 1e-3) / 1e12
-    dominant = max(("gate_up", "down"), key=lambda n: stage_ms[n])
-    achieved = work[dominant]["flops"] / (stage_ms[dominant] * 1e-3) / 1e12
+    dominant = max(("gate_up", "down"), key=lambda n: region_ms[n])
+    achieved = work[dominant]["flops"] / (region_ms[dominant] * 1e-3) / 1e12
     traffic = recorded_traffic(args.workload) if dominant == "gate_up" else None
     roofline = {"bound": "tensor", "kernel": f"grouped_gemm_2sm_kernel ({dominant})", "achieved": round(achieved, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": traffic, "peak_source": f"bf16 dense burst, {peaks['source']}"}
+                "traffic": traffic, "peak_source": f"bf16 dense burst, {peaks['source']}",
+                "kernel_ms": round(region_ms[dominant], 4),
+                "timing": "mean over the timed steps of the CUDA events recorded around the kernel inside them"}
 
     # the same layer with the permute fused into the gate/up GEMM (TMA gathers of x[src_token])
     gathered = None
     if not args.no_gathered:
         gev = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)] for _ in range(args.steps)]
         for _ in range(args.warmup):
-            moe.moe_forward_gathered_timed(x, logits, packed, E, k, f, ws, out, warm_events, cfg.renormalize, stream)
+            moe.moe_forward_gathered(x, logits, packed, E, k, f, cfg.renormalize, workspace=ws, out=out, stream=stream)
         torch.cuda.synchronize()
         barrier(world)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         g0.record(stream)
         for s_ in range(args.steps):
-            moe.moe_forward_gathered_timed(x, logits, packed, E, k, f, ws, out, gev[s_], cfg.renormalize, stream)
+            moe.moe_forward_gathered(x, logits, packed, E, k, f, cfg.renormalize, workspace=ws, out=out, stream=stream)
         g1.record(stream)
         torch.cuda.synchronize()
         if moe.moe_read_device_status(ws) != 0:
             raise SystemExit("device status after the gathered forward")
         gat_s = max_over_ranks(g0.elapsed_time(g1) / 1e3, world, device="cuda")
-        gstage = {name: round(statistics.mean(gev[s_][i].elapsed_time(gev[s_][i + 1]) for s_ in range(args.steps)), 4)
-                  for i, name in enumerate(moe.FORWARD_STAGES) if name != "permute"}
+        gstage = {name: round(ms, 4) for name, ms in stage_breakdown(moe, gev, lambda ev: moe.moe_forward_gathered_timed(
+            x, logits, packed, E, k, f, ws, out, ev, cfg.renormalize, stream)).items() if name != "permute"}
         gathered = {"value": round(job_throughput(T * args.steps, world, gat_s), 1), "unit": "tokens/s",
                     "ms_per_step": round(gat_s * 1e3 / args.steps, 4), "stages_ms": gstage,
                     "gate_up_tflops": round(work["gate_up"]["flops"] / (gstage["gate_up"] * 1e-3) / 1e12, 1),
@@ -508,7 +536,7 @@ def gpu_arm(args):
         del q
         fev = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)] for _ in range(args.steps)]
         for _ in range(args.warmup):
-            moe.moe_forward_fp8_timed(x, logits, packed_fp8, E, k, f, ws, out, warm_events, cfg.renormalize, stream)
+            moe.moe_forward_fp8(x, logits, packed_fp8, E, k, f, cfg.renormalize, workspace=ws, out=out, stream=stream)
         torch.cuda.synchronize()
         fclocks = ClockSampler(local)
         fclocks.start()
@@ -516,15 +544,15 @@ def gpu_arm(args):
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
         for s_ in range(args.steps):
-            moe.moe_forward_fp8_timed(x, logits, packed_fp8, E, k, f, ws, out, fev[s_], cfg.renormalize, stream)
+            moe.moe_forward_fp8(x, logits, packed_fp8, E, k, f, cfg.renormalize, workspace=ws, out=out, stream=stream)
         f1.record(stream)
         torch.cuda.synchronize()
         fclk = fclocks.stop()
         if moe.moe_read_device_status(ws) != 0:
             raise SystemExit("device status after the FP8-weight forward")
         fp8_s = max_over_ranks(f0.elapsed_time(f1) / 1e3, world, device="cuda")
-        fstage = {name: statistics.mean(fev[s_][i].elapsed_time(fev[s_][i + 1]) for s_ in range(args.steps))
-                  for i, name in enumerate(moe.FORWARD_STAGES)}
+        fstage = stage_breakdown(moe, fev, lambda ev: moe.moe_forward_fp8_timed(
+            x, logits, packed_fp8, E, k, f, ws, out, ev, cfg.renormalize, stream))
         fp8 = {"value": round(job_throughput(T * args.steps, world, fp8_s), 1), "unit": "tokens/s",
                "ms_per_step": round(fp8_s * 1e3 / args.steps, 4),
                "stages": stage_table(fstage, stage_work(cfg, counts, fp8_bytes / (3 * E * d * f)), peaks),

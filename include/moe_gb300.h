@@ -484,7 +484,8 @@ MOE_API moe_status_t moe_forward_routed(const void* x, const void* router_packed
  * caller-created cudaEvent_t) at the boundaries
  *   0 route+index+permute 1 gate/up 2 down 3 output-reduction and logit
  *   backward 4 dgrad down 5 dgrad gate/up 6 wgrad down 7 wgrad gate/up 8
- *   un-permute 9.
+ *   un-permute 9; a NULL entry records nothing at its boundary, the array
+ *   itself must not be NULL.
  * ---------------------------------------------------------------------- */
 #define MOE_BACKWARD_STAGES 9
 MOE_API size_t moe_backward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f);
@@ -526,7 +527,10 @@ MOE_API moe_status_t moe_forward_gathered_timed(const void* x, const float* logi
  *   0 start | route | 1 | index | 2 | permute | 3 | gate/up GEMM |
  *   4 | down GEMM | 5 | combine | 6
  * so that cudaEventElapsedTime(events[i], events[i+1]) is the time of one
- * stage's kernel (stage 0 also holds the workspace clear).
+ * stage's kernel (stage 0 also holds the workspace clear).  A NULL entry
+ * records nothing at that boundary (each recorded event separates two
+ * kernels and costs a step some microseconds, so a caller timing one stage
+ * passes only its two boundaries).  events itself must not be NULL.
  * ---------------------------------------------------------------------- */
 #define MOE_FORWARD_STAGES 6
 MOE_API moe_status_t moe_forward_timed(const void* x, const float* logits, const void* packed,

@@ -116,6 +116,14 @@ def _stream(stream=None):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _event_handles(events, stream):
+    """cudaEvent_t handles of torch events (None: no event at that boundary)."""
+    for ev in events:
+        if ev is not None and ev.cuda_event == 0:
+            ev.record(stream)  # materialise the handle
+    return (ctypes.c_void_p * len(events))(*[0 if ev is None else ev.cuda_event for ev in events])
+
+
 def _contig(t, dtype, name):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -304,10 +312,7 @@ def moe_forward_fp8_timed(x, logits, packed_fp8, E, k, f, workspace, out, events
     """moe_forward_fp8 recording events[0..6] at the stage boundaries."""
     T, d = x.shape
     s = stream if stream is not None else torch.cuda.current_stream()
-    for ev in events:
-        if ev.cuda_event == 0:
-            ev.record(s)
-    handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    handles = _event_handles(events, s)
     _check(lib.moe_forward_fp8_timed(_ptr(x), _ptr(logits), _ptr(packed_fp8), T, d, E, k, f, int(bool(renormalize)),
                                      _ptr(out), _ptr(workspace), workspace.numel(), _stream(s), handles),
            "moe_forward_fp8_timed")
@@ -407,13 +412,10 @@ BACKWARD_STAGES = ("recompute_route_index_permute", "recompute_gate_up", "recomp
 
 
 def moe_backward_timed(x, logits, packed, dout, E, k, f, workspace, grads, events, renormalize=True, stream=None):
-    """moe_backward recording events[0..9] at the stage boundaries (BACKWARD_STAGES)."""
+    """moe_backward recording events[0..9] at the stage boundaries (BACKWARD_STAGES); a None entry records nothing."""
     T, d = x.shape
     s = stream if stream is not None else torch.cuda.current_stream()
-    for ev in events:
-        if ev.cuda_event == 0:
-            ev.record(s)
-    handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    handles = _event_handles(events, s)
     g = grads
     _check(lib.moe_backward_timed(_ptr(x), _ptr(logits), _ptr(packed), _ptr(dout), T, d, E, k, f,
                                   int(bool(renormalize)), _ptr(g["dx"]), _ptr(g["d_logits"]), _ptr(g["dw_gate"]),
@@ -521,10 +523,7 @@ def moe_forward_gathered_timed(x, logits, packed, E, k, f, workspace, out, event
     """moe_forward_gathered recording events[0..6] at the stage boundaries."""
     T, d = x.shape
     s = stream if stream is not None else torch.cuda.current_stream()
-    for ev in events:
-        if ev.cuda_event == 0:
-            ev.record(s)
-    handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    handles = _event_handles(events, s)
     _check(lib.moe_forward_gathered_timed(_ptr(x), _ptr(logits), _ptr(packed), T, d, E, k, f, int(bool(renormalize)),
                                           _ptr(out), _ptr(workspace), workspace.numel(), _stream(s), handles),
            "moe_forward_gathered_timed")
@@ -548,13 +547,11 @@ def moe_forward_routed(x, router_packed, packed, E, k, f, renormalize=True, work
 
 def moe_forward_timed(x, logits, packed, E, k, f, workspace, out, events, renormalize=True, stream=None):
     """moe_forward that records events[0..6] (torch.cuda.Event, timing enabled)
-    at the stage boundaries on the launching stream."""
+    at the stage boundaries on the launching stream; a None entry records
+    nothing at its boundary."""
     T, d = x.shape
     s = stream if stream is not None else torch.cuda.current_stream()
-    for ev in events:
-        if ev.cuda_event == 0:
-            ev.record(s)  # materialise the handle
-    handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    handles = _event_handles(events, s)
     _check(lib.moe_forward_timed(_ptr(x), _ptr(logits), _ptr(packed), T, d, E, k, f, int(bool(renormalize)),
                                  _ptr(out), _ptr(workspace), workspace.numel(), _stream(s), handles),
            "moe_forward_timed")

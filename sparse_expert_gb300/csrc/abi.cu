@@ -614,7 +614,7 @@ moe_status_t forward_impl(const void* x, const float* logits, const void* router
   void* y = ws + L.y;
 
   auto mark = [&](int i) -> cudaError_t {
-    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+    return events && events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
   };
   MOE_CUDA(mark(0), "event record");
   MOE_CUDA(cudaMemsetAsync(ws, 0, L.clear_bytes, st), "workspace clear");
@@ -700,8 +700,6 @@ moe_status_t moe_forward_timed(const void* x, const float* logits, const void* p
                                int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out, void* workspace,
                                size_t workspace_bytes, moe_stream_t stream, void* const* events) {
   if (!events) return fail(MOE_ERR_INVALID_ARG, "NULL events");
-  for (int i = 0; i <= MOE_FORWARD_STAGES; ++i)
-    if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "NULL event handle");
   return forward_impl(x, logits, nullptr, packed, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
                       workspace_bytes, stream, events);
 }
@@ -758,8 +756,6 @@ moe_status_t moe_forward_fp8_timed(const void* x, const float* logits, const voi
                                    int32_t E, int32_t k, int32_t f, int32_t renormalize, void* out, void* workspace,
                                    size_t workspace_bytes, moe_stream_t stream, void* const* events) {
   if (!events) return fail(MOE_ERR_INVALID_ARG, "NULL events");
-  for (int i = 0; i <= MOE_FORWARD_STAGES; ++i)
-    if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "NULL event handle");
   return forward_impl(x, logits, nullptr, packed_fp8, T, d, E, k, f, renormalize, out, nullptr, nullptr, workspace,
                       workspace_bytes, stream, events, false, true);
 }
@@ -897,7 +893,7 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   void* dy = ws + L.dy;
   void* dgu = ws + L.dgu;
   auto mark = [&](int i) -> cudaError_t {
-    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+    return events && events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
   };
   MOE_CUDA(mark(0), "event record");
   MOE_CUDA(cudaMemsetAsync(ws, 0, F.clear_bytes, st), "workspace clear");

@@ -631,7 +631,7 @@ cudaError_t launch_gate_up_save(const BackwardGemmArgs& a, int num_sms, cudaStre
 cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
                                          void* const* events) {
   auto mark = [&](int i) -> cudaError_t {
-    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
+    return events && events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
   };
   const auto* wgu = static_cast<const __nv_bfloat16*>(a.w_gate_up);
   const auto* wdn = static_cast<const __nv_bfloat16*>(a.w_down);

@@ -144,6 +144,18 @@ def test_gemm_and_forward_argument_errors():
     assert lib.moe_read_device_status(NULL, NULL, NULL) == INVALID
 
 
+def test_timed_entry_points_reject_a_null_event_array():
+    need = lib.moe_forward_workspace_bytes(256, 8, 2, 128, 64)
+    fwd = [FAKE, FAKE, FAKE, 256, 128, 8, 2, 64, 1, FAKE, FAKE, need, NULL]
+    for name in ("moe_forward_timed", "moe_forward_gathered_timed", "moe_forward_fp8_timed"):
+        assert getattr(lib, name)(*fwd, NULL) == INVALID, name
+        assert "events" in _last(), name
+    bwd = [FAKE, FAKE, FAKE, FAKE, 256, 128, 8, 2, 64, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+           lib.moe_backward_workspace_bytes(256, 8, 2, 128, 64), NULL]
+    assert lib.moe_backward_timed(*bwd, NULL) == INVALID
+    assert "events" in _last()
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_call_without_a_device_reports_no_device():
     assert lib.moe_route_topk(FAKE, 10, 8, 2, 1, FAKE, FAKE, NULL) == NO_DEVICE
