@@ -17,6 +17,8 @@
 //      per-warp running counts) and writes every pair's row.
 // The table is complete before the pass starts, so no block ever waits for
 // another: the pass is one round of loads, a scan and the writes.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -99,13 +101,18 @@ __device__ void block_exclusive_scan(const int32_t* s_in, int32_t* s_out, int n,
 
 __device__ __forceinline__ int4 add4(int4 a, int4 b) { return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
 __global__ void __launch_bounds__(kDispatchThreads)
 index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t P, int E, int E4, int k,
              const int32_t* __restrict__ hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
              int32_t* __restrict__ src_token, int32_t* __restrict__ dest_row, float* __restrict__ row_w,
-             int32_t* status) {
-  extern __shared__ int32_t smem[];
-  int32_t* s_tot = smem;                    // [E4]: pairs per expert
+             int32_t* status, int slab_rows) {
+  extern __shared__ __align__(16) int32_t smem[];
+  int4* s_slab = reinterpret_cast<int4*>(smem);      // [slab_rows][E4 / 4]: rows of the count table
+  int32_t* s_tot = smem + slab_rows * E4;   // [E4]: pairs per expert
   int32_t* s_excl = s_tot + E4;             // [E4]: pairs of earlier chunks per expert
   int32_t* s_off = s_excl + E4;             // [E+1]
   int32_t* s_warp = s_off + E + 1;          // [kWarps][E]: per-warp counts, then per-warp bases
@@ -127,33 +134,44 @@ index_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ top
   }
   for (int i = tid; i < kWarps * E; i += kDispatchThreads) s_warp[i] = 0;
 
-  // column sums of the count table, four experts per 16-byte load: thread
-  // (row group g, column quad q) walks rows g, g + G, ... with all its loads
-  // in flight, then the G row groups are added in shared memory
+  // column sums of the count table, four experts per 16-byte word: the
+  // table comes into shared memory in slabs of slab_rows rows, every copy of
+  // a slab in flight at once (cp.async), and thread (row group g, column
+  // quad q) adds rows g, g + G, ... of the slab; the G row groups are then
+  // added in shared memory
   const int Q = E4 / 4;
   const int G = kDispatchThreads / Q;  // >= 1: E4 <= 1024
   const int q = tid % Q, g = tid / Q;
-  if (g < G) {
-    const int4* h4 = reinterpret_cast<const int4*>(hist);
-    int4 tot = make_int4(0, 0, 0, 0), ex = make_int4(0, 0, 0, 0);
-#pragma unroll 16
-    for (int r = g; r < nchunks; r += G) {
-      const int4 v = __ldcg(h4 + static_cast<int64_t>(r) * Q + q);
-      tot = add4(tot, v);
-      if (r < b) ex = add4(ex, v);
+  const int4* h4 = reinterpret_cast<const int4*>(hist);
+  int4 tot = make_int4(0, 0, 0, 0), ex = make_int4(0, 0, 0, 0);
+  for (int r0 = 0; r0 < nchunks; r0 += slab_rows) {
+    const int rows = min(slab_rows, nchunks - r0);
+    const int words = rows * Q;
+    for (int i = tid; i < words; i += kDispatchThreads) cp_async_16(s_slab + i, h4 + static_cast<int64_t>(r0) * Q + i);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (g < G) {
+      for (int r = g; r < rows; r += G) {
+        const int4 v = s_slab[r * Q + q];
+        tot = add4(tot, v);
+        if (r0 + r < b) ex = add4(ex, v);
+      }
     }
+    __syncthreads();
+  }
+  if (g < G) {
     s_part[0][tid] = tot;
     s_part[1][tid] = ex;
   }
   __syncthreads();
   for (int qq = tid; qq < Q; qq += kDispatchThreads) {
-    int4 tot = s_part[0][qq], ex = s_part[1][qq];
+    int4 col_tot = s_part[0][qq], col_ex = s_part[1][qq];
     for (int gg = 1; gg < G; ++gg) {
-      tot = add4(tot, s_part[0][gg * Q + qq]);
-      ex = add4(ex, s_part[1][gg * Q + qq]);
+      col_tot = add4(col_tot, s_part[0][gg * Q + qq]);
+      col_ex = add4(col_ex, s_part[1][gg * Q + qq]);
     }
-    reinterpret_cast<int4*>(s_tot)[qq] = tot;
-    reinterpret_cast<int4*>(s_excl)[qq] = ex;
+    reinterpret_cast<int4*>(s_tot)[qq] = col_tot;
+    reinterpret_cast<int4*>(s_excl)[qq] = col_ex;
   }
   __syncthreads();
   if (b == 0)
@@ -233,7 +251,12 @@ cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P
   const int64_t nb = dispatch_blocks(P);
   if (nb == 0) return cudaSuccess;
   const int E4 = dispatch_hist_stride(E);
-  const size_t smem = static_cast<size_t>(E4 + E4 + (E + 1) + kWarps * E) * sizeof(int32_t);
+  // slabs of the count table up to 96 KB (the whole table at 2^18 pairs and
+  // E = 384), beside the block's other shared arrays
+  const int64_t row_bytes = static_cast<int64_t>(E4) * sizeof(int32_t);
+  const int slab_rows = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(nb, (96 * 1024) / row_bytes)));
+  const size_t smem = static_cast<size_t>(slab_rows) * row_bytes +
+                      static_cast<size_t>(E4 + E4 + (E + 1) + kWarps * E) * sizeof(int32_t);
   // the static arrays (column partial sums, scan scratch) count against the same 48 KB default
   constexpr size_t kStaticSmem = 2 * kDispatchThreads * sizeof(int4) + kWarps * sizeof(int32_t);
   if (smem + kStaticSmem > 48 * 1024) {
@@ -242,7 +265,7 @@ cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P
     if (err != cudaSuccess) return err;
   }
   index_kernel<<<static_cast<unsigned>(nb), kDispatchThreads, smem, stream>>>(
-      topk_idx, topk_w, P, E, E4, k, hist, counts, offsets, src_token, dest_row, row_w, status);
+      topk_idx, topk_w, P, E, E4, k, hist, counts, offsets, src_token, dest_row, row_w, status, slab_rows);
   return cudaGetLastError();
 }
 

@@ -52,8 +52,8 @@ cudaError_t launch_pack_weights_fp8(const uint8_t* gate_codes, const float* gate
                                     int E, int d, int f, void* packed, int num_sms, cudaStream_t stream);
 
 // ---- stages 2-3
-constexpr int kDispatchThreads = 256;
-constexpr int kDispatchPairsPerThread = 8;
+constexpr int kDispatchThreads = 512;
+constexpr int kDispatchPairsPerThread = 4;
 constexpr int kDispatchChunk = kDispatchThreads * kDispatchPairsPerThread;  // pairs per block
 
 inline int64_t dispatch_blocks(int64_t P) { return (P + kDispatchChunk - 1) / kDispatchChunk; }

@@ -69,28 +69,39 @@ __device__ __forceinline__ Key warp_sort_desc(Key v, int lane) {
 
 // Exact top-k of one token's keys by k rounds of warp arg-max: round j takes
 // the warp maximum of the lanes' best keys, and only the lane that held it
-// drops that key and rescans its own values.  Lane j < k gets the j-th key.
+// marks that key taken and rescans its own values.  Keys are rebuilt from
+// the logits on each scan (a taken bit per value instead of a held key), so
+// this rarely taken path costs no registers across the common one.  Lane
+// j < k gets the j-th key.
 template <int NV>
-__device__ __forceinline__ uint64_t topk_rounds(const float (&v)[NV], int E, int k, int lane) {
-  uint64_t key[NV];
-  uint64_t lbest = 0;
+__device__ __forceinline__ uint64_t lane_best_key(const float (&v)[NV], int E, int lane, uint32_t taken) {
+  uint64_t b = 0;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
-    key[i] = (e < E) ? route_key(v[i], e) : 0ull;
-    lbest = key[i] > lbest ? key[i] : lbest;
+    if (e < E && !((taken >> i) & 1u)) {
+      const uint64_t key = route_key(v[i], e);
+      b = key > b ? key : b;
+    }
   }
+  return b;
+}
+
+template <int NV>
+__device__ __forceinline__ uint64_t topk_rounds(const float (&v)[NV], int E, int k, int lane) {
+  uint32_t taken = 0;
+  uint64_t lbest = lane_best_key<NV>(v, E, lane, taken);
   uint64_t mine = 0;
   for (int j = 0; j < k; ++j) {
     const uint64_t b = warp_max_u64(lbest);
     if (lane == j) mine = b;
     if (lbest == b) {  // keys are unique: exactly one lane held it
-      lbest = 0;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
-        if (key[i] == b) key[i] = 0;
-        lbest = key[i] > lbest ? key[i] : lbest;
+        const int e = lane + 32 * i;
+        if (e < E && route_key(v[i], e) == b) taken |= 1u << i;
       }
+      lbest = lane_best_key<NV>(v, E, lane, taken);
     }
   }
   return mine;
@@ -100,24 +111,27 @@ __device__ __forceinline__ uint64_t topk_rounds(const float (&v)[NV], int E, int
 // kFull every lane holds exactly NV (E = 32 NV) and no index is tested.
 //
 // Without groups the selection first narrows the field.  Let H be the k-th
-// largest of the 32 lanes' maximum high words (the logit part of the key),
-// or, for k <= 16, the k-th largest of the 16 maxima of lane pairs (l,
-// l + 16).  Either way at least k distinct experts have a high word >= H, so
-// the k-th largest key has a high word >= H and every selected expert is
-// among the candidates with high word >= H.  (If H is the 0 of a lane
-// without experts, every expert is a candidate.)  For N(0,1) logits over 384
-// experts there are about nine candidates; when they number at most 32 the
-// warp gathers their full keys into one lane each and a bitonic sort of
-// the smallest width that holds them puts the k winners in lanes 0..k-1.
-// Otherwise (wide ties) the k rounds of topk_rounds decide.  Both give the
-// k largest keys in descending order, so the result does not depend on the
-// path taken.
+// largest of the 32 lanes' maximum logits, or, for k <= 16, the k-th
+// largest of the 16 maxima of lane pairs (l, l + 16).  Either way at least k
+// distinct experts have a logit >= H, so an expert below H has at least k
+// keys above it and cannot be selected: every selected expert is among the
+// candidates (logit >= H as a float compare, where -0.0 equals +0.0 exactly
+// as in the key order).  A lane without experts contributes -inf, which
+// makes every expert a candidate.  For N(0,1) logits over 384 experts there
+// are about nine candidates.  When they number at most 32 each is written
+// once into the warp's shared buffer and ranked by counting the candidate
+// keys above it, and the k of rank < k land in slot order.  Otherwise (wide
+// ties) the k rounds of topk_rounds decide.  Both give the k largest keys in
+// descending order, so the result does not depend on the path taken.
 //
 // With n_groups > 1 ("Training a 1T-Params MoE on EU public
 // infrastructure", Group-limited expert routing), group g = experts
 // [g*E/G, (g+1)*E/G) gets k/G rounds restricted to its own experts, and a
 // warp sort puts the k winners back in descending slot order.
-template <int NV, bool kFull>
+//
+// The loads of a warp's next token are issued before the current token's
+// selection, so their latency overlaps it.
+template <int NV, bool kFull, bool kGrouped>
 __global__ void __launch_bounds__(kRouteWarps * 32, NV <= 12 ? 4 : NV <= 16 ? 2 : 1)
 route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int n_groups, int renormalize,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ hist, int E4) {
@@ -127,57 +141,71 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
   uint64_t* cand = s_cand + warp * 32;
 
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kRouteWarps;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp; t < T; t += warps_total) {
-    const float* row = logits + t * E;
-    float v[NV];
+  int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
+  float v[NV];
+  if (!kGrouped && t < T) {
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (kFull || e < E) ? __ldg(row + e) : 0.0f;
+      v[i] = (kFull || e < E) ? __ldg(logits + t * E + e) : 0.0f;
     }
-    uint64_t mine = 0, first = 0;
-    if (n_groups == 1) {
-      uint32_t hw[NV];
-      uint32_t hm = 0;
+  }
+  for (; t < T; t += warps_total) {
+    const int64_t tn = t + warps_total;
+    float vn[NV];
+    if (kGrouped) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
-        hw[i] = route_hi(v[i]);
-        if (kFull || lane + 32 * i < E) hm = max(hm, hw[i]);
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? __ldg(logits + t * E + e) : 0.0f;
       }
-      uint32_t H;
+    } else if (tn < T) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        vn[i] = (kFull || e < E) ? __ldg(logits + tn * E + e) : 0.0f;
+      }
+    }
+    uint64_t mine = 0, first = 0;
+    if (!kGrouped) {
+      float hm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (kFull || lane + 32 * i < E) hm = fmaxf(hm, v[i]);
+      float H;  // the same in every lane
       if (k <= 16) {
-        const uint32_t hp = max(hm, __shfl_xor_sync(0xffffffffu, hm, 16));
+        const float hp = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 16));
         H = __shfl_sync(0xffffffffu, warp_sort_desc<16>(hp, lane), k - 1);
       } else {
         H = __shfl_sync(0xffffffffu, warp_sort_desc<32>(hm, lane), k - 1);
       }
-      uint32_t cnt = 0;
+      // candidates column by column: one ballot per column, skipped by the
+      // whole warp when the column holds none; the buffer takes the first
+      // 32 in (column, lane) order and C counts them all
+      const unsigned lanes_below = (1u << lane) - 1u;
+      uint32_t C = 0;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) cnt += ((kFull || lane + 32 * i < E) && hw[i] >= H) ? 1u : 0u;
-      uint32_t incl = cnt;
-#pragma unroll
-      for (int s = 1; s < 32; s <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, s);
-        if (lane >= s) incl += o;
-      }
-      const uint32_t C = __shfl_sync(0xffffffffu, incl, 31);
-      if (C <= 32) {
-        uint32_t pos = incl - cnt;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          const int e = lane + 32 * i;
-          if ((kFull || e < E) && hw[i] >= H) cand[pos++] = route_key_hi(hw[i], e);
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        const bool is_cand = (kFull || e < E) && v[i] >= H;
+        const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
+        if (mask) {
+          const uint32_t pos = C + __popc(mask & lanes_below);
+          if (is_cand && pos < 32) cand[pos] = route_key(v[i], e);
+          C += __popc(mask);
         }
+      }
+      if (C <= 32) {
         __syncwarp();
-        uint64_t c = (static_cast<uint32_t>(lane) < C) ? cand[lane] : 0ull;
+        const uint64_t c = (static_cast<uint32_t>(lane) < C) ? cand[lane] : 0ull;
+        uint32_t rank = 0;
+#pragma unroll 4
+        for (uint32_t j = 0; j < C; ++j) rank += cand[j] > c ? 1u : 0u;
         __syncwarp();
-        if (C <= 8)
-          c = warp_sort_desc<8>(c, lane);
-        else if (C <= 16)
-          c = warp_sort_desc<16>(c, lane);
-        else
-          c = warp_sort_desc<32>(c, lane);
-        mine = c;
+        if (static_cast<uint32_t>(lane) < C && rank < static_cast<uint32_t>(k)) cand[rank] = c;
+        __syncwarp();
+        mine = (lane < k) ? cand[lane] : 0ull;
+        __syncwarp();
       } else {
         mine = topk_rounds<NV>(v, E, k, lane);
       }
@@ -230,6 +258,10 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int
       topk_w[p] = z / denom;
       if (hist) atomicAdd(hist + (p / kDispatchChunk) * E4 + e, 1);
     }
+    if (!kGrouped) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = vn[i];
+    }
   }
 }
 
@@ -243,13 +275,17 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int 
   const int grid = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
   const int E4 = dispatch_hist_stride(E);
   const int nv = (E + 31) / 32;
-#define MOE_ROUTE_CASE(NV)                                                                                    \
-  if (E == 32 * (NV))                                                                                           \
-    route_topk_kernel<NV, true><<<grid, kRouteWarps * 32, 0, stream>>>(logits, T, E, k, n_groups, renormalize,  \
-                                                                       topk_idx, topk_w, hist, E4);             \
-  else                                                                                                          \
-    route_topk_kernel<NV, false><<<grid, kRouteWarps * 32, 0, stream>>>(logits, T, E, k, n_groups, renormalize, \
-                                                                        topk_idx, topk_w, hist, E4);            \
+#define MOE_ROUTE_LAUNCH(NV, FULL, GROUPED)                                                               \
+  route_topk_kernel<NV, FULL, GROUPED><<<grid, kRouteWarps * 32, 0, stream>>>(logits, T, E, k, n_groups,      \
+                                                                               renormalize, topk_idx, topk_w, \
+                                                                               hist, E4)
+#define MOE_ROUTE_CASE(NV)                               \
+  if (n_groups > 1)                                      \
+    MOE_ROUTE_LAUNCH(NV, false, true);                   \
+  else if (E == 32 * (NV))                               \
+    MOE_ROUTE_LAUNCH(NV, true, false);                   \
+  else                                                   \
+    MOE_ROUTE_LAUNCH(NV, false, false);                  \
   break;
   switch (nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : nv <= 12 ? 12 : nv <= 16 ? 16 : 32) {
     case 1: MOE_ROUTE_CASE(1)
@@ -260,6 +296,7 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int 
     case 16: MOE_ROUTE_CASE(16)
     default: MOE_ROUTE_CASE(32)
   }
+#undef MOE_ROUTE_LAUNCH
 #undef MOE_ROUTE_CASE
   return cudaGetLastError();
 }
