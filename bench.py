@@ -592,6 +592,60 @@ def gpu_arm(args):
                      "note": "moe_forward captured once into a CUDA graph (torch.cuda.CUDAGraph) and replayed per step"}
         del graph
 
+    # the routing stages alone on the same logits (route with softmax/top-k,
+    # then the count/scan/index pass of moe_dispatch_scan: a histogram kernel
+    # and the index kernel), each call captured `reps` times into a CUDA graph
+    # and replayed, so no host work sits between the launches
+    routing = None
+    if not args.no_routing:
+        reps = 50
+        rws = torch.empty(moe.moe_dispatch_workspace_bytes(T, E, k), dtype=torch.uint8, device="cuda")
+        ridx, rw = moe.moe_route_topk(logits, k, cfg.renormalize)
+        torch.cuda.synchronize()
+
+        def graph_us(call):
+            gs = torch.cuda.Stream()
+            with torch.cuda.stream(gs):
+                for _ in range(3):
+                    call(gs)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(gs):
+                with torch.cuda.graph(g, stream=gs):
+                    for _ in range(reps):
+                        call(gs)
+            # replays until the SM clock has settled at this workload's level (the
+            # GEMM sections before leave it at the power-capped clock)
+            for _ in range(40):
+                g.replay()
+            torch.cuda.synchronize()
+            best = float("inf")
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                best = min(best, a.elapsed_time(b) * 1e3 / reps)
+            del g
+            return best
+
+        route_us = graph_us(lambda st: moe.moe_route_topk(logits, k, cfg.renormalize, stream=st))
+        dispatch_us = graph_us(lambda st: moe.moe_dispatch_scan(ridx, E, topk_w=rw, workspace=rws, stream=st))
+        if moe.moe_read_device_status(rws) != 0:
+            raise SystemExit("device status after the routing calls")
+        rwork = stage_work(cfg)
+        routing = {"route_us": round(route_us, 2), "dispatch_us": round(dispatch_us, 2),
+                   "total_us": round(route_us + dispatch_us, 2),
+                   "route_gbs": round(rwork["route"]["bytes"] / (route_us * 1e-6) / 1e9, 1),
+                   "route_frac_hbm": round(rwork["route"]["bytes"] / (route_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                   "dispatch_gbs": round(rwork["index"]["bytes"] / (dispatch_us * 1e-6) / 1e9, 1),
+                   "note": "moe_route_topk and moe_dispatch_scan (histogram + index kernels) alone on the workload's "
+                           f"logits, best of 5 replays of a CUDA graph holding {reps} calls each, after 40 untimed "
+                           "replays; the forward's route "
+                           "stage also holds the workspace clear (a memset of its header and count table)"}
+        del rws, ridx, rw
+
     # the dynamic tile schedule against a static one, with a kernel holding
     # 40 SMs on a second stream for the first half of every step (the
     # SonicMoE page's measurement, a dummy kernel occupying 40 SMs)
@@ -769,7 +823,7 @@ def gpu_arm(args):
             "permute_gbs": stages["permute"]["gbs"],
             "stages": stages, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "routed_forward": routed,
             "gathered_forward": gathered, "fp8_weights_forward": fp8, "graph_forward": graph_fwd,
-            "contention": contention,
+            "routing": routing, "contention": contention,
             "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clk,
             "backward": backward, "configs": configs,
         }
@@ -861,6 +915,7 @@ def parse_args(argv):
     ap.add_argument("--no-configs", action="store_true", help="skip the other seeded workloads (small, skew, long)")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight forward measurement")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the forward")
+    ap.add_argument("--no-routing", action="store_true", help="skip the routing-only (route + dispatch) measurement")
     ap.add_argument("--no-contention", action="store_true",
                     help="skip the tile-schedule measurement beside a kernel holding 40 SMs")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048,
