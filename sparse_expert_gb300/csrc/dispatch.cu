@@ -251,7 +251,7 @@ cudaError_t launch_index(const int32_t* topk_idx, const float* topk_w, int64_t P
   const int64_t nb = dispatch_blocks(P);
   if (nb == 0) return cudaSuccess;
   const int E4 = dispatch_hist_stride(E);
-  // slabs of the count table up to 96 KB (the whole table at 2^18 pairs and
+  // slabs of the count table up to 96 KB (the whole table up to 2^17 pairs at
   // E = 384), beside the block's other shared arrays
   const int64_t row_bytes = static_cast<int64_t>(E4) * sizeof(int32_t);
   const int slab_rows = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(nb, (96 * 1024) / row_bytes)));
