@@ -160,6 +160,20 @@ def test_layer_backward_matches_oracle(moe, name, renorm):
         assert_values_close(to_np(g[key]), ref[key], key)
 
 
+def test_layer_backward_token_tile_kinds(moe):
+    """The recompute's paired gate/up GEMM (which also keeps G and U) on token
+    tiles of every kind: groups of 9..2,330 rows, so tiles of up to 256 rows
+    (one MMA per K step), of 257..512 (two) and groups split over several."""
+    cfg = workloads.custom("tiles_zipf", T=3000, d=512, E=16, k=2, f=256, routing="zipf")
+    cfg, inp, dout = _layer_inputs(cfg, seed=12)
+    g = _gpu_backward(moe, cfg, inp, dout)
+    ref = oracle.moe_backward(inp["x"].float().numpy(), inp["logits"].numpy(), inp["w_gate"].float().numpy(),
+                              inp["w_up"].float().numpy(), inp["w_down"].float().numpy(), dout.double().numpy(),
+                              cfg.k, True)
+    for key in ("dx", "d_logits", "dw_gate", "dw_up", "dw_down"):
+        assert_values_close(to_np(g[key]), ref[key], key)
+
+
 def test_layer_backward_is_deterministic(moe):
     cfg, inp, dout = _layer_inputs("tiny", seed=3)
     a = _gpu_backward(moe, cfg, inp, dout)

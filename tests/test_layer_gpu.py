@@ -66,6 +66,25 @@ def test_forward_full_parity(moe, name):
     assert_values_close(to_np(out), ref["out"], "out")
 
 
+# Paired-GEMM token tiles of every kind, checked in full: groups of at most
+# 256 rows (one MMA per K step), groups of 257..512 rows in one tile (two
+# MMAs per K step) and groups split into near-equal tiles.  The skewed case
+# has groups of 9..2,330 rows (tiles of 310, 384, 464, 466 and 469 rows among
+# them); forced-uniform routing gives every expert 350 rows.
+@pytest.mark.parametrize("T,E,k,routing,seed", [(3000, 16, 2, "zipf", 12), (1400, 8, 2, "fur", 14)])
+def test_forward_full_parity_token_tile_kinds(moe, T, E, k, routing, seed):
+    cfg = workloads.custom(f"tiles_{routing}", T=T, d=512, E=E, k=k, f=256, routing=routing)
+    inp = {kk: (v.cuda() if torch.is_tensor(v) else v) for kk, v in workloads.generate(cfg, seed=seed).items()}
+    out, ws, _ = _run_forward(moe, inp)
+    inter = moe.forward_intermediates(ws, cfg.T, cfg.E, cfg.k, cfg.d, cfg.f)
+    ref = oracle.moe_forward(to_np(inp["x"]), to_np(inp["logits"]), to_np(inp["w_gate"]), to_np(inp["w_up"]),
+                             to_np(inp["w_down"]), cfg.k, cfg.renormalize)
+    _check_routing_and_index(inter, ref["idx"], ref["w"], cfg.E, cfg.k)
+    assert_values_close(to_np(inter["h"]), ref["h"], "h")
+    assert_values_close(to_np(inter["y"]), ref["y"], "y")
+    assert_values_close(to_np(out), ref["out"], "out")
+
+
 @pytest.mark.parametrize("name", ["t1", "skew", "long"])
 def test_forward_full_size_sampled(moe, name):
     cfg = workloads.get(name)
