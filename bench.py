@@ -309,6 +309,35 @@ def cpu_baseline_stages(cfg, x, logits, w_gate, w_up, w_down, n_tokens, n_expert
     return secs, extrap, desc
 
 
+SINGLE_THREAD_ORACLE = """
+import sys, time
+sys.path.insert(0, sys.argv[1])
+import workloads, oracle
+cfg = workloads.get("tiny")
+inp = workloads.generate(cfg, 0)
+args = (inp["x"].double().numpy(), inp["logits"].numpy(), inp["w_gate"].double().numpy(),
+        inp["w_up"].double().numpy(), inp["w_down"].double().numpy(), cfg.k, cfg.renormalize)
+oracle.moe_forward(*args)
+t0 = time.perf_counter()
+oracle.moe_forward(*args)
+print(cfg.T / (time.perf_counter() - t0))
+"""
+
+
+def single_thread_tiny_oracle():
+    """The whole oracle forward on the tiny workload in a child process whose
+    BLAS and OpenMP pools hold one thread (tokens/s), or None if it fails."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    try:
+        res = subprocess.run([sys.executable, "-c", SINGLE_THREAD_ORACLE, ROOT], env=env, capture_output=True,
+                             text=True, timeout=300)
+        return float(res.stdout.strip().splitlines()[-1]) if res.returncode == 0 else None
+    except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+        return None
+
+
 def time_oracle(cfg, sample):
     import oracle
     x_rows, l_rows, wg, wu, wd, _ = sample
@@ -793,6 +822,9 @@ def gpu_arm(args):
                "sample": desc, "cpu_model": cpu_model(),
                "stages_s": {k_: round(v, 4) for k_, v in secs.items()},
                "extrapolated": sorted(k_ for k_, v in extrap.items() if v),
+               "single_thread_tiny": {"value": single_thread_tiny_oracle(), "unit": "tokens/s", "cores": 1,
+                                      "sample": "the whole oracle forward on the tiny workload (T=256, d=128, E=8, "
+                                                "top-2, f=64), one BLAS/OpenMP thread"},
                "note": "value = T / the sum of the stage times (timed or scaled), one layer forward"}
 
     configs = None
