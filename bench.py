@@ -198,11 +198,13 @@ def stage_work(cfg, counts=None, weight_bytes_per_value=2.0):
 
 def backward_gemm_flops(cfg):
     """Algorithmic FLOPs of the GEMM stages of the layer backward (real rows
-    only): the recomputed forward GEMMs, two dgrad and two wgrad GEMMs."""
+    only): the recomputed gate/up GEMM, two dgrad and two wgrad GEMMs (the
+    down projection is not recomputed: the gate gradient comes from the dgrad
+    down GEMM)."""
     P = cfg.T * cfg.k
     pdf = P * cfg.d * cfg.f
-    return {"recompute_gate_up": 4 * pdf, "recompute_down": 2 * pdf, "dgrad_down": 2 * pdf,
-            "dgrad_gate_up": 4 * pdf, "wgrad_down": 2 * pdf, "wgrad_gate_up": 4 * pdf}
+    return {"recompute_gate_up": 4 * pdf, "dgrad_down": 2 * pdf, "dgrad_gate_up": 4 * pdf, "wgrad_down": 2 * pdf,
+            "wgrad_gate_up": 4 * pdf}
 
 
 def weight_bytes_read(cfg, counts):
@@ -835,8 +837,9 @@ def gpu_arm(args):
                          "peak_source": f"bf16 dense sustained, {peaks['source']}"},
             "clocks": bclk,
             "note": "gradients of x, the router logits and the three expert weight tensors for a given output "
-                    "gradient; the forward is recomputed inside (route, index, permute, gate/up keeping G and U, "
-                    "ungated down); train_step = forward + backward",
+                    "gradient; the forward is recomputed inside (route, index, permute, gate/up keeping G and U; the "
+                    "gate gradient comes from the dgrad down GEMM, so the down projection is not recomputed); "
+                    "train_step = forward + backward",
         }
         del bws, grads
 

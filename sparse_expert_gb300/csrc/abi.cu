@@ -127,11 +127,14 @@ ForwardLayout forward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t
 }
 
 // ---- moe_backward workspace layout (the forward's buffers, then the
-// backward's; y is reused for dx_perm once the output-reduction backward
-// has read it)
+// backward's).  y holds the recomputed expert outputs, or, when the down
+// projection is not recomputed, the output gradient on the rows before the
+// gates; either way it is reused for dx_perm once it has been read.  dh
+// holds the down projection's input gradient before the gates (only used
+// without the recomputation).
 struct BackwardLayout {
   ForwardLayout F;
-  size_t gu, dy, dgu, d_topk_w, total;
+  size_t gu, dy, dgu, d_topk_w, dh, total;
 };
 
 BackwardLayout backward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f) {
@@ -147,6 +150,8 @@ BackwardLayout backward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32
   o += align_up(static_cast<size_t>(P) * 2 * f * 2);
   L.d_topk_w = o;
   o += align_up(static_cast<size_t>(P) * 4);
+  L.dh = o;
+  o += align_up(static_cast<size_t>(P) * f * 2);
   L.total = o;
   return L;
 }
@@ -888,7 +893,7 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   void* x_perm = ws + F.x_perm;
   void* h = ws + F.h;
   void* y = ws + F.y;
-  void* dx_perm = ws + F.y;  // y is dead once the output-reduction backward has read it
+  void* dx_perm = ws + F.y;  // y is dead once read (by the output-reduction backward or the dgrad down GEMM)
   void* gu = ws + L.gu;
   void* dy = ws + L.dy;
   void* dgu = ws + L.dgu;
@@ -919,14 +924,14 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   if (T == 0) {
     // no rows: every weight gradient is zero
     MOE_CUDA(cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st), "offsets clear");
-    for (int i = 1; i <= 4; ++i) MOE_CUDA(mark(i), "event record");
-    MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 5 : nullptr),
+    for (int i = 1; i <= 3; ++i) MOE_CUDA(mark(i), "event record");
+    MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr),
              "backward GEMM launch");
+    MOE_CUDA(mark(8), "event record");
     MOE_CUDA(mark(9), "event record");
     return MOE_OK;
   }
-  // forward recomputation: stages 1-4 with G and U kept; the down GEMM
-  // leaves its rows ungated (the gates enter in the output reduction)
+  // forward recomputation: stages 1-4 with G and U kept
   MOE_CUDA(launch_route_topk(logits, T, E, k, 1, renormalize, topk_idx, topk_w, hist, dev.num_sms, st),
            "route launch");
   MOE_CUDA(launch_index(topk_idx, topk_w, P, E, k, hist, counts, offsets, src_token, dest_row, row_w, &hdr->status,
@@ -936,18 +941,42 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   MOE_CUDA(mark(1), "event record");
   MOE_CUDA(launch_gate_up_save(a, dev.num_sms, st), "gate/up GEMM launch");
   MOE_CUDA(mark(2), "event record");
-  const auto* wdn = static_cast<const __nv_bfloat16*>(a.w_down);
-  GroupedGemmProblem g2{h, wdn, offsets, nullptr, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
-  MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
-  MOE_CUDA(mark(3), "event record");
-  // stage 5 backward, then the gates back to the logits
-  MOE_CUDA(launch_combine_backward(dout, y, dest_row, topk_w, T, k, d, dy, d_topk_w, &hdr->status, dev.num_sms, st),
-           "combine backward launch");
-  MOE_CUDA(launch_route_backward(logits, topk_idx, d_topk_w, T, E, k, renormalize, d_logits, dev.num_sms, st),
-           "route backward launch");
-  MOE_CUDA(mark(4), "event record");
-  // stage 4 backward: dgrad (down, gate/up), wgrad (down, gate/up)
-  MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 5 : nullptr), "backward GEMM launch");
+  if (backward_gate_grad_in_dgrad(E, d, f)) {
+    // the down projection is not recomputed: the output gradient goes to
+    // the rows as it is (the dgrad down GEMM's operand, which applies the
+    // gates itself and keeps its accumulator before them in dh) and gated
+    // (stage 5's mlp_out_grad, for the down weight gradient)
+    void* dout_rows = y;
+    void* dh = ws + L.dh;
+    MOE_CUDA(launch_dout_permute(dout, dest_row, topk_w, T, k, d, dout_rows, dy, &hdr->status, dev.num_sms, st),
+             "output-gradient permute launch");
+    MOE_CUDA(mark(3), "event record");
+    a.dy_dgrad = dout_rows;
+    a.row_w = row_w;
+    a.dh_raw = dh;
+    // stage 4 backward: dgrad (down, gate/up), wgrad (down, gate/up)
+    MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr), "backward GEMM launch");
+    // stage 5's gate gradient as <H, dH before the gates>, then to the logits
+    MOE_CUDA(launch_gate_grad(h, dh, dest_row, T, k, f, d_topk_w, &hdr->status, dev.num_sms, st),
+             "gate gradient launch");
+    MOE_CUDA(launch_route_backward(logits, topk_idx, d_topk_w, T, E, k, renormalize, d_logits, dev.num_sms, st),
+             "route backward launch");
+    MOE_CUDA(mark(8), "event record");
+  } else {
+    // the down GEMM recomputed with ungated rows (the gates enter in the
+    // output reduction), stage 5 backward, the gates back to the logits
+    const auto* wdn = static_cast<const __nv_bfloat16*>(a.w_down);
+    GroupedGemmProblem g2{h, wdn, offsets, nullptr, y, P, E, f, d, d, &hdr->tile_counter[1], &hdr->status};
+    MOE_CUDA(launch_grouped_gemm(g2, Epilogue::kScale, dev.num_sms, st), "down GEMM launch");
+    MOE_CUDA(launch_combine_backward(dout, y, dest_row, topk_w, T, k, d, dy, d_topk_w, &hdr->status, dev.num_sms,
+                                     st),
+             "combine backward launch");
+    MOE_CUDA(launch_route_backward(logits, topk_idx, d_topk_w, T, E, k, renormalize, d_logits, dev.num_sms, st),
+             "route backward launch");
+    MOE_CUDA(mark(3), "event record");
+    MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr), "backward GEMM launch");
+    MOE_CUDA(mark(8), "event record");
+  }
   // the transpose of the permute: each token sums its k row gradients
   MOE_CUDA(launch_combine(dx_perm, dest_row, nullptr, T, k, d, dx, &hdr->status, dev.num_sms, st), "un-permute launch");
   MOE_CUDA(mark(9), "event record");

@@ -130,10 +130,11 @@ enum : int {
 
 struct Params {
   const int32_t* offsets;
-  const float* row_scale;  // kModeRows: gate of each row, or null
+  const float* row_scale;  // kModeRows, kModeSwiGLUBwd: gate of each row, or null
   __nv_bfloat16* out;      // H [P, f], Y [P, d], dX [P, d] or dG,dU [P, 2f] (packed interleave)
   __nv_bfloat16* gu;       // kModeSwiGLU: also G, U [P, 2f] in the packed interleave, or null
   const __nv_bfloat16* gu_in;  // kModeSwiGLUBwd: the saved G, U [P, 2f]
+  __nv_bfloat16* dh_out;       // kModeSwiGLUBwd: also the accumulator as it is (dH before row_scale) [P, f], or null
   int32_t* status;
   int32_t* tile_counter;   // zeroed before launch
   int E;
@@ -933,6 +934,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
         const int64_t gcol0 = static_cast<int64_t>(j0 / 64) * 128 + j0 % 64;
         const __nv_bfloat16* gsrc = p.gu_in + static_cast<int64_t>(x.tok0) * ld + gcol0;
         __nv_bfloat16* gdst = p.out + static_cast<int64_t>(x.tok0) * ld + gcol0;
+        // the accumulator before the row's gate, features j0 .. j0+31 of [P, f]
+        __nv_bfloat16* hraw =
+            p.dh_out ? p.dh_out + static_cast<int64_t>(x.tok0) * p.out_cols + j0 : nullptr;
         // G, U of the next 16 tokens are loaded into registers one half ahead,
         // so their latency overlaps the math and stores of the current half
         uint4 gv[2], uv[2];
@@ -943,12 +947,15 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
 #pragma unroll 1
         for (int c = c_begin; c < c_end; c += 32) {
           if (c + 32 >= c_end) release();
+          // with row gates: lane i holds the gate of token column c + i
+          const float gate_l =
+              p.row_scale != nullptr && c + lane < x.valid ? __ldg(p.row_scale + x.tok0 + c + lane) : 1.0f;
           // two halves of 16 tokens (token groups 2h, 2h + 1) keep the
           // register footprint of G, U and the results small
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int r0 = c + 16 * h;
-            uint32_t pg[8], pu[8];
+            uint32_t pg[8], pu[8], pr[8];
             store_rows16(tbuf, lane, gv);
             rows_to_fragment<2>(tbuf, lane, pg);
             store_rows16(tbuf, lane, uv);
@@ -957,11 +964,17 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             // dG and dU replace G and U in pg, pu
 #pragma unroll
             for (int gg = 0; gg < 2; ++gg) {
+              // thread i's token columns in column group 2h + gg: 8(2h + gg) + 2(i % 4) and +1
+              const float w0 = __shfl_sync(0xffffffffu, gate_l, 8 * (2 * h + gg) + 2 * (lane & 3));
+              const float w1 = __shfl_sync(0xffffffffu, gate_l, 8 * (2 * h + gg) + 2 * (lane & 3) + 1);
 #pragma unroll
               for (int m = 0; m < 4; ++m) {
                 const int i = 4 * (2 * h + gg) + 2 * (m & 1);
-                const float d0 = __uint_as_float(m < 2 ? a[i] : b[i]);
-                const float d1 = __uint_as_float(m < 2 ? a[i + 1] : b[i + 1]);
+                const float r0v = __uint_as_float(m < 2 ? a[i] : b[i]);
+                const float r1v = __uint_as_float(m < 2 ? a[i + 1] : b[i + 1]);
+                pr[4 * gg + m] = pack_bf16x2(r0v, r1v);
+                const float d0 = w0 * r0v;
+                const float d1 = w1 * r1v;
                 const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pg[4 * gg + m]));
                 const float2 uf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pu[4 * gg + m]));
                 const float s0 = sigmoid_f32(gf.x);
@@ -984,6 +997,10 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_c
             rows_to_global<16>(tbuf, lane, gdst + static_cast<int64_t>(r0) * ld, ld, x.valid - r0);
             stage_rows<2>(pu, tbuf, lane);
             rows_to_global<16>(tbuf, lane, gdst + static_cast<int64_t>(r0) * ld + 64, ld, x.valid - r0);
+            if (hraw != nullptr) {
+              stage_rows<2>(pr, tbuf, lane);
+              rows_to_global<16>(tbuf, lane, hraw + static_cast<int64_t>(r0) * p.out_cols, p.out_cols, x.valid - r0);
+            }
           }
           if (c + 32 < c_end) tmem_ld_wait();
         }
@@ -1224,6 +1241,12 @@ cudaError_t launch_dgrad_2sm(const DgradProblem& g, int num_sms, cudaStream_t st
   prm.a_mblocks = g.m_out / 64;
   prm.out_cols = g.m_out;
   prm.mode = g.mode == DgradEpilogue::kSwiGLUBwd ? kModeSwiGLUBwd : kModeRows;
+  if (g.mode == DgradEpilogue::kSwiGLUBwd) {
+    prm.row_scale = g.row_scale;
+    prm.dh_out = static_cast<__nv_bfloat16*>(g.dh_out);
+  } else if (g.row_scale != nullptr || g.dh_out != nullptr) {
+    return cudaErrorNotSupported;
+  }
   return launch_pairs<false>(mw, mx, prm, g.P, num_sms, stream);
 }
 

@@ -628,6 +628,12 @@ cudaError_t launch_gate_up_save(const BackwardGemmArgs& a, int num_sms, cudaStre
                    : launch_mode<128, Mode::kGateUpSave>(ma, mb, prm, max_tiles, num_sms, stream);
 }
 
+bool backward_gate_grad_in_dgrad(int E, int d, int f) {
+  DgradProblem gd{nullptr, nullptr, nullptr, 0, E, d, f, down_tile_n(d), d / down_tile_n(d),
+                  DgradEpilogue::kSwiGLUBwd, nullptr, nullptr, nullptr, nullptr};
+  return dgrad_2sm_supported(gd);
+}
+
 cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
                                          void* const* events) {
   auto mark = [&](int i) -> cudaError_t {
@@ -641,10 +647,12 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
   cudaError_t err = cudaSuccess;
   // the dgrad GEMMs run on SM pairs (grouped_gemm_2sm.cu) where the output
   // features per expert are a multiple of 256, else on single SMs below
-  DgradProblem gd{a.dy, wdn, a.offsets, a.P, a.E, a.d, a.f, bn_dn, a.d / bn_dn, DgradEpilogue::kSwiGLUBwd,
-                  a.gu, a.dgu, a.counters + 2, a.status};
+  DgradProblem gd{a.dy_dgrad ? a.dy_dgrad : a.dy, wdn, a.offsets, a.P, a.E, a.d, a.f, bn_dn, a.d / bn_dn,
+                  DgradEpilogue::kSwiGLUBwd, a.gu, a.dgu, a.counters + 2, a.status, a.row_w, a.dh_raw};
   DgradProblem gx{a.dgu, wgu, a.offsets, a.P, a.E, 2 * a.f, a.d, bn_gu, 2 * a.f / bn_gu, DgradEpilogue::kRows,
                   nullptr, a.dx_perm, a.counters + 3, a.status};
+  const bool gated_dgrad = a.dy_dgrad != nullptr || a.row_w != nullptr || a.dh_raw != nullptr;
+  if (gated_dgrad && !dgrad_2sm_supported(gd)) return cudaErrorNotSupported;
   if (a.P > 0 && dgrad_2sm_supported(gd)) {
     if ((err = launch_dgrad_2sm(gd, num_sms, stream)) != cudaSuccess) return err;
   } else if (a.P > 0) {

@@ -34,6 +34,17 @@ cudaError_t launch_combine_backward(const void* dout, const void* mlp_out, const
                                     int num_sms, cudaStream_t stream);
 cudaError_t launch_route_backward(const float* logits, const int32_t* idx, const float* d_w, int64_t T, int E, int k,
                                   int renormalize, float* d_logits, int num_sms, cudaStream_t stream);
+// The output gradient on the expert rows when the expert outputs are not
+// recomputed: plain[r] = dout[t] and gated[r] = bf16(w[t, j] * dout[t]) for
+// the pair (t, j) at row r (dest_row); a row outside [0, T*k) is skipped and
+// recorded in *status.
+cudaError_t launch_dout_permute(const void* dout, const int32_t* dest_row, const float* w, int64_t T, int k, int d,
+                                void* plain, void* gated, int32_t* status, int num_sms, cudaStream_t stream);
+// The gate gradient from the down projection's input gradient before the
+// gate: d_w[t*k + j] = <h[r], dh_raw[r]> (fp32) for the pair's row r; a row
+// outside [0, T*k) gives 0 and is recorded in *status.
+cudaError_t launch_gate_grad(const void* h, const void* dh_raw, const int32_t* dest_row, int64_t T, int k, int f,
+                             float* d_w, int32_t* status, int num_sms, cudaStream_t stream);
 
 // ---- blockwise FP8 (E4M3) weights
 cudaError_t launch_quantize_fp8(const void* w, int64_t n, uint8_t* codes, float* scales, int num_sms,
@@ -149,6 +160,11 @@ struct DgradProblem {
   void* out;
   int32_t* tile_counter;
   int32_t* status;
+  // kSwiGLUBwd only, both optional: the gate of each row, applied to the
+  // accumulator before dG, dU are formed (the tokens are then the ungated
+  // output gradient), and [P, f] bf16 receiving the accumulator as it is
+  const float* row_scale = nullptr;
+  void* dh_out = nullptr;
 };
 bool dgrad_2sm_supported(const DgradProblem& g);
 cudaError_t launch_dgrad_2sm(const DgradProblem& g, int num_sms, cudaStream_t stream);
@@ -173,7 +189,18 @@ struct BackwardGemmArgs {
                            // [0] gate/up (save), [2..5] dgrad down, dgrad gate/up,
                            // wgrad down, wgrad gate/up
   int32_t* status;
+  // Optional (the layer backward without the recomputed down projection;
+  // needs backward_gate_grad_in_dgrad): the dgrad down GEMM then takes the
+  // ungated output gradient rows dy_dgrad, applies each row's gate row_w to
+  // its accumulator and writes that accumulator before the gate to dh_raw
+  // [P, f]; dy stays the gated rows for the down weight gradient.
+  const void* dy_dgrad;
+  const float* row_w;
+  void* dh_raw;
 };
+// Whether the dgrad down GEMM of this shape runs on SM pairs, where it can
+// take row gates and write dh_raw (BackwardGemmArgs).
+bool backward_gate_grad_in_dgrad(int E, int d, int f);
 // Gate/up GEMM that writes H and, for the backward, G and U.
 cudaError_t launch_gate_up_save(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream);
 // dG,dU (from dY, G, U), dX, and the weight gradients, in that order;
