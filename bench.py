@@ -647,7 +647,7 @@ def gpu_arm(args):
                         call(gs)
             # replays until the SM clock has settled at this workload's level (the
             # GEMM sections before leave it at the power-capped clock)
-            for _ in range(40):
+            for _ in range(200):
                 g.replay()
             torch.cuda.synchronize()
             best = float("inf")
@@ -698,7 +698,7 @@ def gpu_arm(args):
                    "route_frac_hbm": round(rwork["route"]["bytes"] / (route_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                    "dispatch_gbs": round(rwork["index"]["bytes"] / (dispatch_us * 1e-6) / 1e9, 1),
                    "note": "moe_route_topk and moe_dispatch_scan (histogram + index kernels) alone on the workload's "
-                           f"logits, best of 5 replays of a CUDA graph holding {reps} calls each, after 40 untimed "
+                           f"logits, best of 5 replays of a CUDA graph holding {reps} calls each, after 200 untimed "
                            "replays (the 26 MB of logits stay in L2 across the calls; l2_flushed has them cold); "
                            "the forward's route "
                            "stage also holds the workspace clear (a memset of its header and count table)"}
