@@ -373,6 +373,18 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t word, float (&v)[4]) {
       : "r"(h23));
 }
 
+// Two fp32 products, each rounded once to nearest (one packed multiply),
+// then both rounded to bf16.
+__device__ __forceinline__ uint32_t mul_pair_to_bf16x2(float v0, float v1, float s0, float s1) {
+  uint64_t vv, ss, pp;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(vv) : "f"(v0), "f"(v1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ss) : "f"(s0), "f"(s1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(pp) : "l"(vv), "l"(ss));
+  float p0, p1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(p0), "=f"(p1) : "l"(pp));
+  return pack_bf16x2(p0, p1);
+}
+
 // One 16-value piece of a weight row of one K block: 16 E4M3 codes and
 // their 16 scales become bf16(value x scale), the product of the exact code
 // value and the fp32 scale rounded once in fp32 and then to bf16 -- the
@@ -383,8 +395,8 @@ __device__ __forceinline__ void convert_piece(const uint4& q, const float4 (&scl
   for (int i = 0; i < 4; ++i) {
     float v[4];
     e4m3x4_to_f32(w[i], v);
-    o[2 * i] = pack_bf16x2(__fmul_rn(v[0], scl[i].x), __fmul_rn(v[1], scl[i].y));
-    o[2 * i + 1] = pack_bf16x2(__fmul_rn(v[2], scl[i].z), __fmul_rn(v[3], scl[i].w));
+    o[2 * i] = mul_pair_to_bf16x2(v[0], v[1], scl[i].x, scl[i].y);
+    o[2 * i + 1] = mul_pair_to_bf16x2(v[2], v[3], scl[i].z, scl[i].w);
   }
 }
 
