@@ -479,7 +479,8 @@ MOE_API moe_status_t moe_forward_routed(const void* x, const void* router_packed
  * <mlp_out[r], dout[t]> is formed as <H[r], dout[t] Wd^T> -- the same
  * product summed in the other order -- from the dgrad down GEMM, which then
  * takes the ungated rows of dout and applies the gates to its accumulator,
- * so the down projection is not recomputed; where that GEMM does not run on
+ * so the down projection is not recomputed (the down weight gradient H^T dY
+ * is taken as (gated H)^T (ungated rows)); where that GEMM does not run on
  * SM pairs (f not a multiple of 256) the down GEMM is recomputed with
  * ungated rows and the gate gradient read from them.
  *   x [T, d] bf16; logits [T, E] fp32; packed from moe_pack_weights;
@@ -489,11 +490,11 @@ MOE_API moe_status_t moe_forward_routed(const void* x, const void* router_packed
  * forward.  moe_backward_timed records events[i] (MOE_BACKWARD_STAGES + 1
  * caller-created cudaEvent_t) at the boundaries
  *   0 route+index+permute 1 gate/up 2 the output gradient on the expert
- *   rows (gated and ungated; or the recomputed down GEMM, the output-
- *   reduction backward and the logit backward) 3 dgrad down 4 dgrad gate/up
- *   5 wgrad down 6 wgrad gate/up 7 gate gradient and logit backward (empty
- *   when done at 2) 8 un-permute 9; a NULL entry records nothing at its
- *   boundary, the array itself must not be NULL.
+ *   rows (or the recomputed down GEMM, the output-reduction backward and
+ *   the logit backward) 3 dgrad down 4 dgrad gate/up 5 gate gradient and
+ *   logit backward (empty when done at 2) 6 wgrad down 7 wgrad gate/up 8
+ *   un-permute 9; a NULL entry records nothing at its boundary, the array
+ *   itself must not be NULL.
  * ---------------------------------------------------------------------- */
 #define MOE_BACKWARD_STAGES 9
 MOE_API size_t moe_backward_workspace_bytes(int64_t T, int32_t E, int32_t k, int32_t d, int32_t f);

@@ -408,7 +408,7 @@ def moe_backward(x, logits, packed, dout, E, k, f, renormalize=True, workspace=N
 
 
 BACKWARD_STAGES = ("recompute_route_index_permute", "recompute_gate_up", "output_grad_rows", "dgrad_down",
-                   "dgrad_gate_up", "wgrad_down", "wgrad_gate_up", "gate_grad_route_bwd", "unpermute")
+                   "dgrad_gate_up", "gate_grad_route_bwd", "wgrad_down", "wgrad_gate_up", "unpermute")
 
 
 def moe_backward_timed(x, logits, packed, dout, E, k, f, workspace, grads, events, renormalize=True, stream=None):

@@ -127,11 +127,11 @@ ForwardLayout forward_layout(int64_t T, int32_t E, int32_t k, int32_t d, int32_t
 }
 
 // ---- moe_backward workspace layout (the forward's buffers, then the
-// backward's).  y holds the recomputed expert outputs, or, when the down
-// projection is not recomputed, the output gradient on the rows before the
-// gates; either way it is reused for dx_perm once it has been read.  dh
-// holds the down projection's input gradient before the gates (only used
-// without the recomputation).
+// backward's).  y holds the recomputed expert outputs where the down
+// projection is recomputed, and is reused for dx_perm; dy holds the gated
+// output-gradient rows, or, without the recomputation, the ungated ones.
+// dh holds the down projection's input gradient before the gates (only
+// used without the recomputation).
 struct BackwardLayout {
   ForwardLayout F;
   size_t gu, dy, dgu, d_topk_w, dh, total;
@@ -893,7 +893,7 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   void* x_perm = ws + F.x_perm;
   void* h = ws + F.h;
   void* y = ws + F.y;
-  void* dx_perm = ws + F.y;  // y is dead once read (by the output-reduction backward or the dgrad down GEMM)
+  void* dx_perm = ws + F.y;  // y is dead by then (read by the output-reduction backward, or never written)
   void* gu = ws + L.gu;
   void* dy = ws + L.dy;
   void* dgu = ws + L.dgu;
@@ -925,9 +925,9 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
     // no rows: every weight gradient is zero
     MOE_CUDA(cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, st), "offsets clear");
     for (int i = 1; i <= 3; ++i) MOE_CUDA(mark(i), "event record");
-    MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr),
-             "backward GEMM launch");
-    MOE_CUDA(mark(8), "event record");
+    MOE_CUDA(launch_backward_dgrad_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr), "dgrad GEMM launch");
+    MOE_CUDA(mark(6), "event record");
+    MOE_CUDA(launch_backward_wgrad_gemms(a, dev.num_sms, st, events ? events + 7 : nullptr), "wgrad GEMM launch");
     MOE_CUDA(mark(9), "event record");
     return MOE_OK;
   }
@@ -943,25 +943,28 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
   MOE_CUDA(mark(2), "event record");
   if (backward_gate_grad_in_dgrad(E, d, f)) {
     // the down projection is not recomputed: the output gradient goes to
-    // the rows as it is (the dgrad down GEMM's operand, which applies the
-    // gates itself and keeps its accumulator before them in dh) and gated
-    // (stage 5's mlp_out_grad, for the down weight gradient)
-    void* dout_rows = y;
+    // the rows as it is (dout_rows, in the dY buffer), the operand of the
+    // dgrad down GEMM, which applies the gates itself and keeps its
+    // accumulator before them in dh; the gate gradient <H, dh> then leaves
+    // H gated in place, and the down weight gradient takes the gated H with
+    // the ungated rows
+    void* dout_rows = dy;
     void* dh = ws + L.dh;
-    MOE_CUDA(launch_dout_permute(dout, dest_row, topk_w, T, k, d, dout_rows, dy, &hdr->status, dev.num_sms, st),
+    MOE_CUDA(launch_dout_permute(dout, dest_row, topk_w, T, k, d, dout_rows, nullptr, &hdr->status, dev.num_sms, st),
              "output-gradient permute launch");
     MOE_CUDA(mark(3), "event record");
     a.dy_dgrad = dout_rows;
     a.row_w = row_w;
     a.dh_raw = dh;
-    // stage 4 backward: dgrad (down, gate/up), wgrad (down, gate/up)
-    MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr), "backward GEMM launch");
-    // stage 5's gate gradient as <H, dH before the gates>, then to the logits
-    MOE_CUDA(launch_gate_grad(h, dh, dest_row, T, k, f, d_topk_w, &hdr->status, dev.num_sms, st),
+    a.h_wgrad = h;
+    a.dy_wgrad = dout_rows;
+    MOE_CUDA(launch_backward_dgrad_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr), "dgrad GEMM launch");
+    MOE_CUDA(launch_gate_grad(h, dh, dest_row, topk_w, T, k, f, d_topk_w, &hdr->status, dev.num_sms, st),
              "gate gradient launch");
     MOE_CUDA(launch_route_backward(logits, topk_idx, d_topk_w, T, E, k, renormalize, d_logits, dev.num_sms, st),
              "route backward launch");
-    MOE_CUDA(mark(8), "event record");
+    MOE_CUDA(mark(6), "event record");
+    MOE_CUDA(launch_backward_wgrad_gemms(a, dev.num_sms, st, events ? events + 7 : nullptr), "wgrad GEMM launch");
   } else {
     // the down GEMM recomputed with ungated rows (the gates enter in the
     // output reduction), stage 5 backward, the gates back to the logits
@@ -974,8 +977,9 @@ moe_status_t backward_impl(const void* x, const float* logits, const void* packe
     MOE_CUDA(launch_route_backward(logits, topk_idx, d_topk_w, T, E, k, renormalize, d_logits, dev.num_sms, st),
              "route backward launch");
     MOE_CUDA(mark(3), "event record");
-    MOE_CUDA(launch_swiglu_backward_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr), "backward GEMM launch");
-    MOE_CUDA(mark(8), "event record");
+    MOE_CUDA(launch_backward_dgrad_gemms(a, dev.num_sms, st, events ? events + 4 : nullptr), "dgrad GEMM launch");
+    MOE_CUDA(mark(6), "event record");
+    MOE_CUDA(launch_backward_wgrad_gemms(a, dev.num_sms, st, events ? events + 7 : nullptr), "wgrad GEMM launch");
   }
   // the transpose of the permute: each token sums its k row gradients
   MOE_CUDA(launch_combine(dx_perm, dest_row, nullptr, T, k, d, dx, &hdr->status, dev.num_sms, st), "un-permute launch");

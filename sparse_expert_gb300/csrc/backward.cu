@@ -9,13 +9,14 @@
 //
 // Without recomputing the expert outputs (the layer backward when the down
 // projection's input gradient runs on SM pairs), stage 5's backward splits in
-// two.  dout_permute writes each pair's row twice: the output gradient as it
-// is (plain, the operand of the down projection's input gradient, which then
-// applies the gate itself) and gated (mlp_out_grad, the operand of the down
-// weight gradient).  gate_grad forms weights_grad[t, j] = <mlp_out[r],
+// two.  dout_permute writes each pair's row of the output gradient as it is
+// (the operand of the down projection's input gradient, which applies the
+// gate itself, and of the down weight gradient), and optionally gated
+// (mlp_out_grad).  gate_grad forms weights_grad[t, j] = <mlp_out[r],
 // output_grad[t]> as <H[r], dHu[r]>: with mlp_out[r] = H[r] Wd and dHu[r] =
 // output_grad[t] Wd^T (that input gradient before the gate) it is the same
-// product, summed in the other order.
+// product, summed in the other order; it then leaves H[r] gated in place,
+// since H^T mlp_out_grad = (gated H)^T output_grad for the weight gradient.
 //
 // route_backward: the gates' gradient taken back to the router logits
 // (Algorithm 1, stage 1, Softmax and TopK, with the selection held fixed):
@@ -97,8 +98,8 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
 }
 
 // One warp per token: the token's output-gradient row is read once, piece
-// by piece, and each piece written to its k rows as it is and scaled by the
-// slot's gate.
+// by piece, and each piece written to its k rows as it is and (when gated is
+// not null) scaled by the slot's gate.
 template <int KMAX>
 __global__ void __launch_bounds__(kWarps * 32)
 dout_permute_kernel(const uint4* __restrict__ dout, const int32_t* __restrict__ dest_row, const float* __restrict__ w,
@@ -126,11 +127,13 @@ dout_permute_kernel(const uint4* __restrict__ dout, const int32_t* __restrict__ 
           const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
           const float wj = __shfl_sync(0xffffffffu, my_w, j);
           if (active && !((bad_slots >> j) & 1u)) {
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(wj * gf[i].x, wj * gf[i].y);
             plain[row * dvec + v] = gv;
-            gated[row * dvec + v] = make_uint4(o[0], o[1], o[2], o[3]);
+            if (gated != nullptr) {
+              uint32_t o[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(wj * gf[i].x, wj * gf[i].y);
+              gated[row * dvec + v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
           }
         }
       }
@@ -140,9 +143,12 @@ dout_permute_kernel(const uint4* __restrict__ dout, const int32_t* __restrict__ 
 
 // One warp per token: for each of its k rows, <h[r], dh_raw[r]> in fp32 --
 // each lane its 16-byte pieces in order, then a butterfly over the lanes.
+// With w not null each piece of h[r] is replaced, once read, by
+// bf16(w[t, j] * h[r]): the gated rows the down weight gradient takes
+// together with the ungated output-gradient rows.
 __global__ void __launch_bounds__(kWarps * 32)
-gate_grad_kernel(const uint4* __restrict__ h, const uint4* __restrict__ dhu, const int32_t* __restrict__ dest_row,
-                 int64_t T, int k, int fvec, float* __restrict__ d_w, int32_t* status) {
+gate_grad_kernel(uint4* h, const uint4* __restrict__ dhu, const int32_t* __restrict__ dest_row,
+                 const float* __restrict__ w, int64_t T, int k, int fvec, float* __restrict__ d_w, int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int64_t P = T * k;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarps;
@@ -150,22 +156,27 @@ gate_grad_kernel(const uint4* __restrict__ h, const uint4* __restrict__ dhu, con
     const int64_t my_row = lane < k ? __ldg(dest_row + t * k + lane) : 0;
     const unsigned bad_slots = __ballot_sync(0xffffffffu, my_row < 0 || my_row >= P);
     if (bad_slots != 0u && lane == 0) record_status(status, kStatusBadIndex);
+    const float my_w = (w != nullptr && lane < k) ? __ldg(w + t * k + lane) : 0.f;
     for (int j = 0; j < k; ++j) {
       const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
+      const float wj = __shfl_sync(0xffffffffu, my_w, j);
       float s = 0.f;
       if (!((bad_slots >> j) & 1u)) {
         for (int v = lane; v < fvec; v += 32) {
-          const uint4 hv = __ldg(h + row * fvec + v);
+          const uint4 hv = h[row * fvec + v];
           const uint4 dv = __ldg(dhu + row * fvec + v);
           const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&hv);
           const __nv_bfloat162* dh = reinterpret_cast<const __nv_bfloat162*>(&dv);
+          uint32_t o[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 a = __bfloat1622float2(hh[i]);
             const float2 b = __bfloat1622float2(dh[i]);
             s = fmaf(a.x, b.x, s);
             s = fmaf(a.y, b.y, s);
+            o[i] = pack_bf16x2(wj * a.x, wj * a.y);
           }
+          if (w != nullptr) h[row * fvec + v] = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
 #pragma unroll
@@ -274,11 +285,11 @@ cudaError_t launch_dout_permute(const void* dout, const int32_t* dest_row, const
   return cudaGetLastError();
 }
 
-cudaError_t launch_gate_grad(const void* h, const void* dh_raw, const int32_t* dest_row, int64_t T, int k, int f,
-                             float* d_w, int32_t* status, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gate_grad(void* h, const void* dh_raw, const int32_t* dest_row, const float* w, int64_t T, int k,
+                             int f, float* d_w, int32_t* status, int num_sms, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   gate_grad_kernel<<<token_grid(T, num_sms), kWarps * 32, 0, stream>>>(
-      static_cast<const uint4*>(h), static_cast<const uint4*>(dh_raw), dest_row, T, k, f / 8, d_w, status);
+      static_cast<uint4*>(h), static_cast<const uint4*>(dh_raw), dest_row, w, T, k, f / 8, d_w, status);
   return cudaGetLastError();
 }
 

@@ -634,8 +634,8 @@ bool backward_gate_grad_in_dgrad(int E, int d, int f) {
   return dgrad_2sm_supported(gd);
 }
 
-cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
-                                         void* const* events) {
+cudaError_t launch_backward_dgrad_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
+                                        void* const* events) {
   auto mark = [&](int i) -> cudaError_t {
     return events && events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
   };
@@ -702,14 +702,24 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
       if (err != cudaSuccess) return err;
     }
   }
-  if ((err = mark(1)) != cudaSuccess) return err;
+  return mark(1);
+}
+
+cudaError_t launch_backward_wgrad_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
+                                        void* const* events) {
+  auto mark = [&](int i) -> cudaError_t {
+    return events && events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
+  };
+  cudaError_t err = cudaSuccess;
+  const void* h_w = a.h_wgrad ? a.h_wgrad : a.h;
+  const void* dy_w = a.dy_wgrad ? a.dy_wgrad : a.dy;
   // dWd[e] = H_e^T dY_e: M = f, N = d, K = the expert's rows
   if (a.dw_down) {
     const int bn = tile_n_for(a.d);
     CUtensorMap ma, mb;
     const int64_t rows = a.P > 0 ? a.P : 1;
-    if (!make_bf16_map_col_blocks(&ma, a.P > 0 ? a.h : a.dw_down, rows, a.f, BK, BM / 64)) return cudaErrorInvalidValue;
-    if (!make_bf16_map_col_blocks(&mb, a.P > 0 ? a.dy : a.dw_down, rows, a.d, BK, bn / 64)) return cudaErrorInvalidValue;
+    if (!make_bf16_map_col_blocks(&ma, a.P > 0 ? h_w : a.dw_down, rows, a.f, BK, BM / 64)) return cudaErrorInvalidValue;
+    if (!make_bf16_map_col_blocks(&mb, a.P > 0 ? dy_w : a.dw_down, rows, a.d, BK, bn / 64)) return cudaErrorInvalidValue;
     Params prm = base_params(a.offsets, a.E, a.counters + 4, a.status);
     prm.m_tiles = (a.f + BM - 1) / BM;
     prm.n_tiles = a.d / bn;
@@ -723,7 +733,7 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
                                       stream, &mo, &mo);
     if (err != cudaSuccess) return err;
   }
-  if ((err = mark(2)) != cudaSuccess) return err;
+  if ((err = mark(0)) != cudaSuccess) return err;
   // dWg[e] = X_e^T dG_e, dWu[e] = X_e^T dU_e: M = d, N = 2f interleaved
   if (a.dw_gate) {
     const int bn = tile_n_for(2 * a.f);  // may span two interleaved gate/up tiles
@@ -751,7 +761,14 @@ cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms,
                                       stream, &mg, &mu);
     if (err != cudaSuccess) return err;
   }
-  return mark(3);
+  return mark(1);
+}
+
+cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
+                                         void* const* events) {
+  cudaError_t err = launch_backward_dgrad_gemms(a, num_sms, stream, events);
+  if (err != cudaSuccess) return err;
+  return launch_backward_wgrad_gemms(a, num_sms, stream, events ? events + 2 : nullptr);
 }
 
 }  // namespace moe

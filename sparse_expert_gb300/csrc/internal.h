@@ -35,16 +35,17 @@ cudaError_t launch_combine_backward(const void* dout, const void* mlp_out, const
 cudaError_t launch_route_backward(const float* logits, const int32_t* idx, const float* d_w, int64_t T, int E, int k,
                                   int renormalize, float* d_logits, int num_sms, cudaStream_t stream);
 // The output gradient on the expert rows when the expert outputs are not
-// recomputed: plain[r] = dout[t] and gated[r] = bf16(w[t, j] * dout[t]) for
-// the pair (t, j) at row r (dest_row); a row outside [0, T*k) is skipped and
-// recorded in *status.
+// recomputed: plain[r] = dout[t] and, when gated is not null, gated[r] =
+// bf16(w[t, j] * dout[t]) for the pair (t, j) at row r (dest_row); a row
+// outside [0, T*k) is skipped and recorded in *status.
 cudaError_t launch_dout_permute(const void* dout, const int32_t* dest_row, const float* w, int64_t T, int k, int d,
                                 void* plain, void* gated, int32_t* status, int num_sms, cudaStream_t stream);
 // The gate gradient from the down projection's input gradient before the
 // gate: d_w[t*k + j] = <h[r], dh_raw[r]> (fp32) for the pair's row r; a row
-// outside [0, T*k) gives 0 and is recorded in *status.
-cudaError_t launch_gate_grad(const void* h, const void* dh_raw, const int32_t* dest_row, int64_t T, int k, int f,
-                             float* d_w, int32_t* status, int num_sms, cudaStream_t stream);
+// outside [0, T*k) gives 0 and is recorded in *status.  With w (the gates
+// [T, k]) not null, each row of h is then replaced by bf16(w[t, j] h[r]).
+cudaError_t launch_gate_grad(void* h, const void* dh_raw, const int32_t* dest_row, const float* w, int64_t T, int k,
+                             int f, float* d_w, int32_t* status, int num_sms, cudaStream_t stream);
 
 // ---- blockwise FP8 (E4M3) weights
 cudaError_t launch_quantize_fp8(const void* w, int64_t n, uint8_t* codes, float* scales, int num_sms,
@@ -197,6 +198,10 @@ struct BackwardGemmArgs {
   const void* dy_dgrad;
   const float* row_w;
   void* dh_raw;
+  // Optional operands of the down weight gradient in place of h and dy
+  // (its result H^T dY equals (gated H)^T (ungated rows)).
+  const void* h_wgrad;
+  const void* dy_wgrad;
 };
 // Whether the dgrad down GEMM of this shape runs on SM pairs, where it can
 // take row gates and write dh_raw (BackwardGemmArgs).
@@ -207,6 +212,12 @@ cudaError_t launch_gate_up_save(const BackwardGemmArgs& a, int num_sms, cudaStre
 // events[0..3] (optional) are recorded after each of the four GEMMs.
 cudaError_t launch_swiglu_backward_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
                                          void* const* events);
+// The same in two halves: dG,dU then dX (events[0..1] after each), and the
+// down then the gate/up weight gradients (events[0..1] after each).
+cudaError_t launch_backward_dgrad_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
+                                        void* const* events);
+cudaError_t launch_backward_wgrad_gemms(const BackwardGemmArgs& a, int num_sms, cudaStream_t stream,
+                                        void* const* events);
 
 // Tiled bf16 TMA maps, 128-byte swizzle, zero fill outside the tensor.
 // 2-D: row-major [rows, cols], box [box_rows, box_cols].  3-D: dense
