@@ -182,11 +182,12 @@ def test_layer_backward_is_deterministic(moe):
         assert torch.equal(a[key], b[key]), key
 
 
-@pytest.mark.parametrize("name", ["t1", "skew"])
+@pytest.mark.parametrize("name", ["t1", "skew", "long"])
 def test_layer_backward_full_size_sampled(moe, name):
     """16384 tokens, d = 6144, 384 experts, k = 8, f = 1792 (normal routing,
-    and the Zipf-skewed routing whose largest group holds ~16,000 rows and
-    ~200 experts none): the whole backward runs on the GPU; the oracle
+    the Zipf-skewed routing whose largest group holds ~16,000 rows and ~200
+    experts none, and 65,536 tokens with forced-uniform routing: three
+    455-row tiles per expert): the whole backward runs on the GPU; the oracle
     recomputes, one by one, the rows of a seeded token sample (all k slots
     of each) and of two whole experts (the largest group and a random one,
     which may be empty: its weight gradients must then be exactly zero),
